@@ -1,0 +1,204 @@
+/*
+ * fpd.h — C ABI of the GB300 (sm_103a) block-drafter hot path.
+ *
+ * One non-causal block drafter pass of diffusion-drafter speculative decoding, the per-position
+ * constrained argmax over legal vocabulary slices, and the acceptance-length scan.  The method:
+ *
+ *   - VFlash paper (Chinese translation), §2.1 "Preliminaries": features of selected target layers are
+ *     fused and injected as keys and values into every drafter layer; given the start token the drafter
+ *     predicts the masked positions of a block in ONE bidirectional forward pass; greedy verification
+ *     accepts up to the first position that disagrees with the target.
+ *   - VFlash blog, "Method": text runs in verified-SD mode with 16-position blocks (one accepted anchor +
+ *     15 proposals); the target keeps the longest matching prefix plus its own next token.
+ *   - VFlash paper (zh), §2.2: a block of length L is one observed start token followed by L-1 masked
+ *     tokens, all predicted conditionally independently in one pass.
+ *   - VFlash paper (zh), §2.3: coordinates use one of 1001 dedicated tokens, or a fixed-width field of one
+ *     sign slot and five digit slots whose unused high digits are filled with a mask token.
+ *   - VFlash paper (zh), §2.5 "Inference": per-position constraints restrict coordinates and delimiters to
+ *     their legal vocabulary, acting on already-computed logits; a primitive is accepted when its schema
+ *     validator passes, otherwise the first k draft positions are retained.
+ *   - FlashDrive, §3.2 "Diffusion-based drafting": the drafter conditions on fused target hidden states
+ *     written into the draft layers' KV cache and produces a whole candidate block in one pass.
+ *
+ * Conventions (all entry points):
+ *   - Every tensor argument is memory the CALLER owns (device memory unless marked "host").  The library
+ *     never frees caller memory.  Weights are borrowed and must outlive the model handle.
+ *   - Element types: bf16 for activations/weights/KV (passed as void*), int32 ids, fp32 logits.
+ *   - Layouts are row-major.  Weight matrices are [out_features, in_features].
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *     No call synchronises, allocates device memory, or copies host<->device.  Every call validates its
+ *     arguments on the host first and returns an error WITHOUT launching anything when they are wrong.
+ *   - Errors: a non-zero fpd_status; fpd_last_error() returns a message for the calling thread.
+ *     FPD_ERR_CUDA wraps a CUDA runtime error seen at launch.
+ *   - Device pointers passed to the library must be 16-byte aligned.
+ */
+#ifndef FPD_H_
+#define FPD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FPD_MAX_LAYERS 8
+#define FPD_MAX_CLASSES 32   /* vocabulary classes in one layout */
+#define FPD_MAX_RANGES 64    /* [lo,hi) id ranges over all classes of one layout */
+
+typedef enum {
+  FPD_OK = 0,
+  FPD_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, misaligned pointer */
+  FPD_ERR_SHAPE = 2,         /* inconsistent or unsupported sizes */
+  FPD_ERR_CAPACITY = 3,      /* workspace / KV store / position table too small, table limits exceeded */
+  FPD_ERR_UNSUPPORTED = 4,   /* model shape the kernels do not implement */
+  FPD_ERR_CUDA = 5,          /* CUDA runtime/driver error at launch */
+  FPD_ERR_DEVICE_CHECK = 6   /* a kernel reported a failed device-side check (see fpd_device_status) */
+} fpd_status;
+
+/* Drafter shape.  The layer form is a pre-norm transformer layer with per-head q/k RMSNorm, rotate-half
+ * RoPE, grouped-query attention without any mask (bidirectional over context + block) and a SwiGLU MLP;
+ * an untied LM head follows a final RMSNorm.  Supported: head_dim in {64, 128}; d_model, d_ff multiples of
+ * 64; n_q_heads a multiple of n_kv_heads. */
+typedef struct fpd_model_desc {
+  int32_t n_layers;     /* 1..FPD_MAX_LAYERS (5 for the five-layer drafter) */
+  int32_t d_model;      /* d */
+  int32_t n_q_heads;    /* H_q */
+  int32_t n_kv_heads;   /* H_kv */
+  int32_t head_dim;     /* h */
+  int32_t d_ff;         /* SwiGLU inner width F */
+  int32_t vocab;        /* V */
+  int32_t n_feat;       /* number of fused target layers n_f (1..8) */
+  int32_t max_pos;      /* RoPE positions [0, max_pos) are supported: context capacity + block length */
+  float rms_eps;        /* RMSNorm epsilon: y = x / sqrt(mean(x^2) + eps) * g */
+  float rope_theta;     /* RoPE base: angle(pos, i) = pos * theta^(-2i/h), i < h/2 */
+} fpd_model_desc;
+
+/* Borrowed device weights, all bf16, row-major [out, in]. */
+typedef struct fpd_weights {
+  const void* embed;        /* [V, d] token embedding (anchor and mask rows) */
+  const void* w_fc;         /* [d, n_f*d] fusion projection over the concatenated target features */
+  const void* hidden_norm;  /* [d] RMSNorm gain applied to the fused context */
+  const void* final_norm;   /* [d] RMSNorm gain before the LM head */
+  const void* lm_head;      /* [V, d] */
+  const void* attn_norm[FPD_MAX_LAYERS];  /* [d] */
+  const void* wqkv[FPD_MAX_LAYERS];       /* [(H_q + 2 H_kv) h, d]: rows of q heads, then k heads, then v heads */
+  const void* q_norm[FPD_MAX_LAYERS];     /* [h] per-head RMSNorm gain on q */
+  const void* k_norm[FPD_MAX_LAYERS];     /* [h] per-head RMSNorm gain on k (context and block keys) */
+  const void* wo[FPD_MAX_LAYERS];         /* [d, H_q h] */
+  const void* mlp_norm[FPD_MAX_LAYERS];   /* [d] */
+  const void* w_gate_up[FPD_MAX_LAYERS];  /* [2F, d]: rows 0..F-1 gate, rows F..2F-1 up */
+  const void* w_down[FPD_MAX_LAYERS];     /* [d, F] */
+} fpd_weights;
+
+typedef struct fpd_model fpd_model;
+
+/* Per-position legal vocabulary (VFlash paper (zh), §2.5: coordinates and delimiters restricted to their
+ * legal vocabulary).  Class c is the union of id ranges [lo, hi) listed in
+ * class_ranges[2*class_off[c] .. 2*class_off[c+1]).  A class may be the full vocabulary ([0, V)).
+ * The tables are HOST memory (they are part of the declared layout and small); pos_class is DEVICE
+ * memory, one class id per block position of every request, [B*L] int16 (position 0, the anchor, is
+ * ignored).  Ranges of one class must be non-empty, inside [0, V), sorted and disjoint. */
+typedef struct fpd_vocab_layout {
+  int32_t n_class;               /* 1..FPD_MAX_CLASSES */
+  const int32_t* class_off;      /* host [n_class + 1], class_off[0] = 0, total ranges <= FPD_MAX_RANGES */
+  const int32_t* class_ranges;   /* host [2 * class_off[n_class]] (lo, hi) pairs */
+  const int16_t* pos_class;      /* device [B * L] */
+} fpd_vocab_layout;
+
+/* Schema rules for primitive-mode acceptance, one int8 per block position (device [B*L]).
+ * VFlash paper (zh), §2.3 and §2.5: the validator checks the declared layout; fixed-width numerals pad
+ * only their unused HIGH digits with the mask token, so a field reads [sign][pad..pad][digit..digit]. */
+enum {
+  FPD_RULE_NONE = 0,        /* not checked */
+  FPD_RULE_MEMBER = 1,      /* token must lie in its position's class */
+  FPD_RULE_DIGIT = 2,       /* digit slot, not the last of its field: member; pad_id allowed only while the
+                               previous slot is not a digit slot holding a real digit */
+  FPD_RULE_DIGIT_LAST = 3   /* last digit slot of a field: member, must be a real digit (!= pad_id), and
+                               the same ordering rule as FPD_RULE_DIGIT */
+};
+
+enum { FPD_VERIFY_TEXT = 0, FPD_VERIFY_SCHEMA = 1 };
+
+/* ---- model handle ------------------------------------------------------------------------------------
+ * Validates the shape, records the borrowed weight pointers, and builds the model's own small device
+ * tables (the RoPE cos/sin table for max_pos positions and TMA descriptors of the weights).  This is the
+ * one call that allocates device memory (those tables); it synchronises the current device once. */
+fpd_status fpd_model_create(const fpd_model_desc* desc, const fpd_weights* weights, fpd_model** out);
+void fpd_model_destroy(fpd_model* model);
+
+/* Bytes of the caller-allocated context KV store for `batch` requests of at most t_cap context positions.
+ * Layout: [layer][request][K|V][kv_head][t_cap][head_dim] bf16. */
+size_t fpd_kv_store_bytes(const fpd_model* model, int batch, int t_cap);
+
+/* Bytes of caller-allocated scratch ("workspace") that is enough for every call below with these sizes
+ * (block_len <= max_block_len, total context rows <= batch * t_cap).  Workspace contents do not survive
+ * between calls except where stated (fpd_draft_block writes nothing that later calls read). */
+size_t fpd_workspace_bytes(const fpd_model* model, int batch, int max_block_len, int t_cap);
+
+/* ---- a1 + a2: context fusion and per-layer context K/V --------------------------------------------------
+ * VFlash paper (zh), §2.1; FlashDrive §3.2.  For each packed context row r of request b:
+ *   ctx_r = RMSNorm_{hidden_norm}( [F_0,r | F_1,r | ... | F_{n_f-1},r] . w_fc^T )              (bf16)
+ *   for every layer l and kv head g:  K^l_g(pos) = RoPE_pos( RMSNorm_{k_norm[l]}( ctx_r . Wk^l_g^T ) ),
+ *                                     V^l_g(pos) = ctx_r . Wv^l_g^T                              (bf16)
+ * with pos = pos_start[b] + (r - row_off[b]) (pos_start NULL means 0: a fresh context), written into
+ * kv_store at [l][b][K|V][g][pos][:].
+ *   feats      host array of n_feat DEVICE pointers, each [total_rows, d] bf16 (rows of all requests packed)
+ *   row_off    device [batch + 1], row_off[0] = 0, row_off[batch] = total_rows, non-decreasing
+ *   pos_start  device [batch] or NULL; the caller guarantees pos_start[b] + rows_b <= t_cap
+ * Rows beyond the written positions are left untouched. */
+fpd_status fpd_prepare_context(fpd_model* model, int batch, int total_rows, const int32_t* row_off,
+                               const int32_t* pos_start, const void* const* feats, void* kv_store,
+                               int t_cap, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- a3..a7: one bidirectional drafter pass over a block --------------------------------------------------
+ * Block of request b: position 0 holds anchor[b], positions 1..L-1 hold mask_id (VFlash (zh) §2.2).
+ * Block position j sits at RoPE position ctx_len[b] + j.  Every layer attends, without a mask, over the
+ * request's ctx_len[b] context keys/values of that layer followed by the L block keys/values.
+ *   ctx_len       device [batch], 0 <= ctx_len[b] <= t_cap (caller guarantees; kernels clamp)
+ *   anchor        device [batch] token ids in [0, V)
+ *   hidden_out    device [batch * L, d] bf16: residual stream after the last layer (before final norm)
+ *   layer_hidden  device [n_layers, batch * L, d] bf16 or NULL: residual stream after every layer */
+fpd_status fpd_draft_block(fpd_model* model, int batch, int block_len, const void* kv_store, int t_cap,
+                           const int32_t* ctx_len, const int32_t* anchor, int32_t mask_id,
+                           void* hidden_out, void* layer_hidden, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* ---- a8: final RMSNorm, LM head, per-position legal-vocabulary mask, argmax ------------------------------
+ * For block positions j = 1..L-1 of every request: z = RMSNorm_{final_norm}(hidden[b,j]) (bf16), logits
+ * over the LEGAL ids of the position's class only (illegal ids are never computed), token = argmax in fp32
+ * with the lowest id winning ties.
+ *   hidden      device [batch * L, d] bf16 (fpd_draft_block's hidden_out)
+ *   layout      NULL: every position may take any id in [0, V)
+ *   tokens_out  device [batch, L-1] int32
+ *   logits_out  device [batch * (L-1), V] fp32 or NULL; only legal columns are written */
+fpd_status fpd_constrain_argmax(fpd_model* model, int batch, int block_len, const void* hidden,
+                                const fpd_vocab_layout* layout, int32_t* tokens_out, float* logits_out,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- a9: acceptance-length scan ----------------------------------------------------------------------------
+ * FPD_VERIFY_TEXT (VFlash blog "Method"; VFlash (zh) §2.1): target [B, L] holds t_1..t_L, the target's
+ *   greedy token at block positions 1..L (t_L follows the last draft).  n = length of the longest prefix
+ *   with draft[b, i-1] == t_i; accept_len = n + 1; committed = d_1..d_n, t_{n+1}.
+ * FPD_VERIFY_SCHEMA (VFlash (zh) §2.5): position j = 1..L-1 fails when its rule (FPD_RULE_*) fails; with
+ *   p the first failing position, accept_len = p - 1 (all L-1 when none fails); committed = d_1..d_k.
+ *   Needs layout (membership) and rule (device [B*L] int8); target is ignored.
+ *   draft       device [B, L-1] int32
+ *   accept_len  device [B] int32
+ *   committed   device [B, L] int32, entries past accept_len set to -1
+ *   valid_out   device [B] int32 or NULL: 1 when nothing failed (text: n == L-1) */
+fpd_status fpd_verify(int mode, int batch, int block_len, const int32_t* draft, const int32_t* target,
+                      const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id,
+                      int32_t* accept_len, int32_t* committed, int32_t* valid_out, void* stream);
+
+/* ---- diagnostics ---------------------------------------------------------------------------------------- */
+const char* fpd_last_error(void);          /* thread-local message of the last failing call */
+uint64_t fpd_kernel_launches(void);        /* kernels launched by this library since load (all threads) */
+/* Reads and clears the device-side check word (bounded-wait timeouts, bad ids).  Synchronises the stream.
+ * Returns FPD_OK when no kernel recorded a failure, else FPD_ERR_DEVICE_CHECK with *code set. */
+fpd_status fpd_device_status(void* stream, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FPD_H_ */

@@ -1,0 +1,272 @@
+"""CPU oracle of the block-drafter hot path (ctypes wrapper over ``fpd_oracle.c``).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+(and its reference arm) may import this package.  The product path (``block_diffusion_speculative_non_gb300``)
+never imports it and shares no code with it.
+
+Every function takes the seeded inputs from ``synth`` (bf16 as uint16 bit patterns) and returns numpy
+arrays.  Arithmetic is fp64 with bf16 rounding at the storage points documented in ``fpd_oracle.c``.
+
+Parity pins (tests/test_oracle_pins.py) tie each function to something other than itself: closed forms,
+exhaustive enumeration, brute force on tiny inputs, numpy's library routines, degenerate cases.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fpd_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_MAX_LAYERS = 8
+
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i16p = ctypes.POINTER(ctypes.c_int16)
+_i8p = ctypes.POINTER(ctypes.c_int8)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/liboracle.so (gcc, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=gnu11", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _OracleModel(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("d", ctypes.c_int32), ("nq", ctypes.c_int32), ("nkv", ctypes.c_int32),
+        ("h", ctypes.c_int32), ("F", ctypes.c_int32), ("V", ctypes.c_int32), ("nf", ctypes.c_int32),
+        ("eps", ctypes.c_double), ("theta", ctypes.c_double),
+        ("embed", _u16p), ("w_fc", _u16p), ("hidden_norm", _u16p), ("final_norm", _u16p), ("lm_head", _u16p),
+        ("attn_norm", _u16p * _MAX_LAYERS), ("wqkv", _u16p * _MAX_LAYERS), ("q_norm", _u16p * _MAX_LAYERS),
+        ("k_norm", _u16p * _MAX_LAYERS), ("wo", _u16p * _MAX_LAYERS), ("mlp_norm", _u16p * _MAX_LAYERS),
+        ("w_gate_up", _u16p * _MAX_LAYERS), ("w_down", _u16p * _MAX_LAYERS),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        l = ctypes.CDLL(build())
+        l.oracle_round_bf16.restype = ctypes.c_uint16
+        l.oracle_round_bf16.argtypes = [ctypes.c_double]
+        l.oracle_bf16_to_double.restype = ctypes.c_double
+        l.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        l.oracle_silu.restype = ctypes.c_double
+        l.oracle_silu.argtypes = [ctypes.c_double]
+        l.oracle_num_threads.restype = ctypes.c_int
+        l.oracle_rmsnorm.argtypes = [ctypes.c_int, _f64p, _u16p, ctypes.c_double, _f64p]
+        l.oracle_rope.argtypes = [ctypes.c_int, _f64p, ctypes.c_double, ctypes.c_double]
+        l.oracle_linear.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64p, _u16p, _f64p]
+        l.oracle_attention.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int, _u16p, _u16p,
+                                       ctypes.c_int, _f64p, _f64p, ctypes.c_double, _f64p]
+        l.oracle_prepare_context.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _i32p,
+                                             _i32p, ctypes.POINTER(_u16p), _u16p, ctypes.c_int]
+        l.oracle_draft_block.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
+                                         ctypes.c_int, _i32p, _i32p, ctypes.c_int32, _u16p, _u16p]
+        l.oracle_constrain_argmax.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
+                                              ctypes.c_int, _i32p, _i32p, _i16p, _i32p, _f64p, _f64p]
+        l.oracle_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _i32p, ctypes.c_int, _i32p,
+                                    _i32p, _i16p, _i8p, ctypes.c_int32, _i32p, _i32p, _i32p]
+        _lib = l
+    return _lib
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    lib().oracle_set_num_threads(int(n))
+
+
+def _p(a, t):
+    return a.ctypes.data_as(t) if a is not None else None
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---- building blocks (exported for the pins) ------------------------------------------------------------
+
+def round_bf16(x) -> np.ndarray:
+    """fp64 -> bf16 bit patterns, round to nearest even."""
+    x = np.asarray(x, dtype=np.float64)
+    f = lib().oracle_round_bf16
+    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+def bf16_to_f64(b) -> np.ndarray:
+    b = np.asarray(b, dtype=np.uint16)
+    f = lib().oracle_bf16_to_double
+    return np.array([f(int(v)) for v in b.ravel()], dtype=np.float64).reshape(b.shape)
+
+
+def rmsnorm(x, g_bits, eps) -> np.ndarray:
+    x = _c(x, np.float64)
+    g = _c(g_bits, np.uint16)
+    y = np.empty_like(x)
+    lib().oracle_rmsnorm(x.size, _p(x, _f64p), _p(g, _u16p), float(eps), _p(y, _f64p))
+    return y
+
+
+def rope(x, pos, theta) -> np.ndarray:
+    y = _c(x, np.float64).copy()
+    lib().oracle_rope(y.size, _p(y, _f64p), float(pos), float(theta))
+    return y
+
+
+def silu(v: float) -> float:
+    return float(lib().oracle_silu(float(v)))
+
+
+def linear(X, W_bits) -> np.ndarray:
+    X = _c(X, np.float64)
+    W = _c(W_bits, np.uint16)
+    M, K = X.shape
+    N = W.shape[0]
+    assert W.shape[1] == K
+    Y = np.empty((M, N), dtype=np.float64)
+    lib().oracle_linear(M, N, K, _p(X, _f64p), _p(W, _u16p), _p(Y, _f64p))
+    return Y
+
+
+def attention(q, k_ctx_bits, v_ctx_bits, k_blk, v_blk, scale) -> np.ndarray:
+    """q [R, h] f64; context keys/values [n_ctx, h] bf16 bits; block keys/values [n_blk, h] f64."""
+    q = _c(q, np.float64)
+    R, h = q.shape
+    kc = _c(k_ctx_bits, np.uint16).reshape(-1, h)
+    vc = _c(v_ctx_bits, np.uint16).reshape(-1, h)
+    kb = _c(k_blk, np.float64).reshape(-1, h)
+    vb = _c(v_blk, np.float64).reshape(-1, h)
+    o = np.empty((R, h), dtype=np.float64)
+    lib().oracle_attention(h, R, _p(q, _f64p), kc.shape[0], _p(kc, _u16p), _p(vc, _u16p), kb.shape[0],
+                           _p(kb, _f64p), _p(vb, _f64p), float(scale), _p(o, _f64p))
+    return o
+
+
+# ---- the hot path ---------------------------------------------------------------------------------------
+
+class Model:
+    """Holds the weights (bf16 bit patterns from synth.make_weights) and the C struct pointing at them."""
+
+    def __init__(self, shape, weights):
+        self.shape = shape
+        self.w = weights
+        s = _OracleModel()
+        s.n_layers, s.d, s.nq, s.nkv = shape.n_layers, shape.d_model, shape.n_q_heads, shape.n_kv_heads
+        s.h, s.F, s.V, s.nf = shape.head_dim, shape.d_ff, shape.vocab, shape.n_feat
+        s.eps, s.theta = float(shape.rms_eps), float(shape.rope_theta)
+        keep = []
+
+        def ptr(a):
+            a = _c(a, np.uint16)
+            keep.append(a)
+            return a.ctypes.data_as(_u16p)
+
+        s.embed, s.w_fc = ptr(weights["embed"]), ptr(weights["w_fc"])
+        s.hidden_norm, s.final_norm = ptr(weights["hidden_norm"]), ptr(weights["final_norm"])
+        s.lm_head = ptr(weights["lm_head"])
+        for l, lw in enumerate(weights["layers"]):
+            for name in ("attn_norm", "wqkv", "q_norm", "k_norm", "wo", "mlp_norm", "w_gate_up", "w_down"):
+                getattr(s, name)[l] = ptr(lw[name])
+        self._keep = keep
+        self.c = s
+
+
+def prepare_context(model: Model, row_off, feats, t_cap, batch=None, pos_start=None, kv_store=None):
+    """Returns the KV store [layer][b][K|V][kv_head][t_cap][h] (bf16 bits); rows not written stay as given
+    (zero for a new store)."""
+    sh = model.shape
+    row_off = _c(row_off, np.int32)
+    B = len(row_off) - 1 if batch is None else batch
+    total = int(row_off[-1])
+    if kv_store is None:
+        kv_store = np.zeros((sh.n_layers, B, 2, sh.n_kv_heads, t_cap, sh.head_dim), dtype=np.uint16)
+    fs = [_c(f, np.uint16) for f in feats]
+    arr = (_u16p * len(fs))(*[f.ctypes.data_as(_u16p) for f in fs])
+    ps = None if pos_start is None else _c(pos_start, np.int32)
+    rc = lib().oracle_prepare_context(ctypes.byref(model.c), B, total, _p(row_off, _i32p), _p(ps, _i32p), arr,
+                                      _p(kv_store, _u16p), int(t_cap))
+    if rc:
+        raise ValueError("oracle_prepare_context: bad sizes")
+    return kv_store
+
+
+def draft_block(model: Model, kv_store, t_cap, ctx_len, anchor, mask_id, block_len, want_layers=False):
+    """Returns hidden [B*L, d] (bf16 bits) and, when asked, the per-layer residual [n_layers, B*L, d]."""
+    sh = model.shape
+    ctx_len = _c(ctx_len, np.int32)
+    anchor = _c(anchor, np.int32)
+    B = len(anchor)
+    kv = _c(kv_store, np.uint16)
+    hidden = np.empty((B * block_len, sh.d_model), dtype=np.uint16)
+    layers = np.empty((sh.n_layers, B * block_len, sh.d_model), dtype=np.uint16) if want_layers else None
+    rc = lib().oracle_draft_block(ctypes.byref(model.c), B, block_len, _p(kv, _u16p), int(t_cap),
+                                  _p(ctx_len, _i32p), _p(anchor, _i32p), int(mask_id), _p(hidden, _u16p),
+                                  _p(layers, _u16p))
+    if rc:
+        raise ValueError("oracle_draft_block: bad arguments")
+    return (hidden, layers) if want_layers else hidden
+
+
+def constrain_argmax(model: Model, hidden, batch, block_len, layout=None, want_logits=False):
+    """Returns (tokens [B, L-1] int32, margin [B*(L-1)] f64, logits [B*(L-1), V] f64 or None).  Logits of
+    illegal columns are NaN."""
+    sh = model.shape
+    hid = _c(hidden, np.uint16)
+    P = block_len - 1
+    tokens = np.empty((batch, P), dtype=np.int32)
+    margin = np.empty(batch * P, dtype=np.float64)
+    logits = np.full((batch * P, sh.vocab), np.nan, dtype=np.float64) if want_logits else None
+    if layout is None:
+        n_class, co, cr, pc = 0, None, None, None
+    else:
+        n_class = len(layout["class_off"]) - 1
+        co = _c(layout["class_off"], np.int32)
+        cr = _c(layout["class_ranges"], np.int32)
+        pc = _c(np.broadcast_to(layout["pos_class"], (batch, block_len)) if layout["pos_class"].ndim == 1
+                else layout["pos_class"], np.int16)
+    rc = lib().oracle_constrain_argmax(ctypes.byref(model.c), batch, block_len, _p(hid, _u16p), n_class,
+                                       _p(co, _i32p), _p(cr, _i32p), _p(pc, _i16p), _p(tokens, _i32p),
+                                       _p(logits, _f64p), _p(margin, _f64p))
+    if rc:
+        raise ValueError("oracle_constrain_argmax: bad layout")
+    return tokens, margin, logits
+
+
+def verify(mode, draft, target=None, layout=None, rule=None, pad_id=-1):
+    """mode 0 = text, 1 = schema.  Returns (accept_len [B], committed [B, L], valid [B])."""
+    draft = _c(draft, np.int32)
+    B, P = draft.shape
+    L = P + 1
+    acc = np.empty(B, dtype=np.int32)
+    com = np.empty((B, L), dtype=np.int32)
+    val = np.empty(B, dtype=np.int32)
+    tg = _c(target, np.int32) if target is not None else None
+    if mode == 1:
+        n_class = len(layout["class_off"]) - 1
+        co = _c(layout["class_off"], np.int32)
+        cr = _c(layout["class_ranges"], np.int32)
+        pc = _c(np.broadcast_to(layout["pos_class"], (B, L)) if np.asarray(layout["pos_class"]).ndim == 1
+                else layout["pos_class"], np.int16)
+        rl = _c(np.broadcast_to(rule, (B, L)) if np.asarray(rule).ndim == 1 else rule, np.int8)
+    else:
+        n_class, co, cr, pc, rl = 0, None, None, None, None
+    rc = lib().oracle_verify(int(mode), B, L, _p(draft, _i32p), _p(tg, _i32p), n_class, _p(co, _i32p),
+                             _p(cr, _i32p), _p(pc, _i16p), _p(rl, _i8p), int(pad_id), _p(acc, _i32p),
+                             _p(com, _i32p), _p(val, _i32p))
+    if rc:
+        raise ValueError("oracle_verify: bad arguments")
+    return acc, com, val
