@@ -1,0 +1,537 @@
+// fpd_api.cu — the C ABI declared in include/fpd.h: host-side validation, the model handle, workspace
+// carving, and the order of kernel launches of each call.  Every entry point validates all of its arguments
+// before it launches anything and returns an fpd_status; nothing here synchronises, allocates or copies
+// between host and device except fpd_model_create / fpd_model_destroy / fpd_device_status.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "fpd_kernels.cuh"
+
+namespace fpd {
+std::atomic<uint64_t> g_launches{0};
+}
+
+using namespace fpd;
+
+namespace {
+
+thread_local std::string t_err;
+
+fpd_status fail(fpd_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return s;
+}
+
+fpd_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(FPD_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define FPD_CUDA(call, where)                         \
+  do {                                                \
+    cudaError_t e_ = (call);                          \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+  } while (0)
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// ---- workspace carving -------------------------------------------------------------------------------------------
+struct Carver {
+  size_t off = 0;
+  char* base = nullptr;
+  template <class T>
+  T* take(size_t count) {
+    off = align_up(off, 256);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+constexpr int kPrepChunk = 4096;   // context rows per fusion/projection pass (bounds the workspace)
+constexpr int kLmColTile = 128;    // vocabulary ids per LM-head work item (the 128-row MMA operand)
+
+// Largest split-K partial buffer (floats) any row count 1..R_max needs for an N x K GEMM.  The split count
+// only changes where the tile counts change, so the row counts at tile boundaries cover the maximum.
+size_t part_floats_bound(const Model& m, int R_max, int N, int K) {
+  size_t best = 0;
+  auto eval = [&](int R) {
+    if (R < 1 || R > R_max) return;
+    TcPlan pl = tc_plan_gemm(R, N, K, m.num_sms);
+    best = std::max(best, (size_t)pl.splits * R * N);
+  };
+  eval(16); eval(32); eval(64); eval(R_max);
+  for (int R = 128; R <= R_max; R += 128) eval(R);
+  return best;
+}
+
+struct DraftWs {
+  bf16 *xn, *q, *kblk, *vblk, *o, *hmid;
+  float* part;
+  float* o_part;
+  float2* ml;
+  int att_splits, att_chunk;
+  TcPlan p_qkv, p_o, p_gu, p_down;
+};
+
+DraftWs carve_draft(const Model& m, Carver& c, int B, int L, int t_cap) {
+  const auto& d = m.d;
+  DraftWs w{};
+  const int M = B * L;
+  const int nqkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim, nqh = d.n_q_heads * d.head_dim;
+  w.p_qkv = tc_plan_gemm(M, nqkv, d.d_model, m.num_sms);
+  w.p_o = tc_plan_gemm(M, d.d_model, nqh, m.num_sms);
+  w.p_gu = tc_plan_gemm(M, 2 * d.d_ff, d.d_model, m.num_sms);
+  w.p_down = tc_plan_gemm(M, d.d_model, d.d_ff, m.num_sms);
+  size_t part = 0;
+  part = std::max(part, (size_t)w.p_qkv.splits * M * nqkv);
+  part = std::max(part, (size_t)w.p_o.splits * M * d.d_model);
+  part = std::max(part, (size_t)w.p_gu.splits * M * 2 * d.d_ff);
+  part = std::max(part, (size_t)w.p_down.splits * M * d.d_model);
+  w.xn = c.take<bf16>((size_t)M * d.d_model);
+  w.part = c.take<float>(part);
+  w.q = c.take<bf16>((size_t)M * nqh);
+  w.kblk = c.take<bf16>((size_t)M * d.n_kv_heads * d.head_dim);
+  w.vblk = c.take<bf16>((size_t)M * d.n_kv_heads * d.head_dim);
+  w.o = c.take<bf16>((size_t)M * nqh);
+  w.hmid = c.take<bf16>((size_t)M * d.d_ff);
+  attn_plan(B, L, d.n_q_heads, d.n_kv_heads, t_cap, m.num_sms, &w.att_splits, &w.att_chunk);
+  w.o_part = c.take<float>((size_t)w.att_splits * M * nqh);
+  w.ml = c.take<float2>((size_t)w.att_splits * M * d.n_q_heads);
+  return w;
+}
+
+struct ArgmaxWs {
+  bf16* z;   // final-normed rows in class-sorted order
+  int *rows_sorted, *inv_sorted, *class_row_off, *n_items;
+  unsigned long long* packed;
+  int4* items;
+  int max_items, row_tile;
+};
+
+ArgmaxWs carve_argmax(const Model& m, Carver& c, int B, int L) {
+  ArgmaxWs w{};
+  const int n_rows = B * (L - 1);
+  w.row_tile = tc_lm_row_tile(n_rows);
+  w.z = c.take<bf16>((size_t)n_rows * m.d.d_model);
+  w.rows_sorted = c.take<int>(n_rows);
+  w.inv_sorted = c.take<int>(n_rows);
+  w.class_row_off = c.take<int>(FPD_MAX_CLASSES + 1);
+  w.n_items = c.take<int>(1);
+  w.packed = c.take<unsigned long long>(n_rows);
+  w.max_items = (ceil_div(m.d.vocab, kLmColTile) + 1 + FPD_MAX_RANGES) * (ceil_div(n_rows, w.row_tile) + FPD_MAX_CLASSES);
+  w.items = c.take<int4>(w.max_items);
+  return w;
+}
+
+struct PrepWs {
+  float* part;
+  bf16* ctx;
+  int chunk;
+};
+
+PrepWs carve_prep(const Model& m, Carver& c, int rows_max) {
+  PrepWs w{};
+  const auto& d = m.d;
+  w.chunk = std::max(1, std::min(kPrepChunk, rows_max));
+  const size_t a = part_floats_bound(m, w.chunk, d.d_model, d.n_feat * d.d_model);
+  const size_t b = part_floats_bound(m, w.chunk, 2 * d.n_kv_heads * d.head_dim, d.d_model);
+  w.part = c.take<float>(std::max(a, b));
+  w.ctx = c.take<bf16>((size_t)w.chunk * d.d_model);
+  return w;
+}
+
+size_t ws_draft_bytes(const Model& m, int B, int L, int t_cap) {
+  Carver c;
+  carve_draft(m, c, B, L, t_cap);
+  return c.off;
+}
+size_t ws_argmax_bytes(const Model& m, int B, int L) {
+  Carver c;
+  carve_argmax(m, c, B, L);
+  return c.off;
+}
+size_t ws_prep_bytes(const Model& m, int rows) {
+  Carver c;
+  carve_prep(m, c, rows);
+  return c.off;
+}
+
+fpd_status check_device(const Model& m) {
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != m.device) return fail(FPD_ERR_INVALID_ARG, "current device %d is not the model's device %d", cur, m.device);
+  return FPD_OK;
+}
+
+// ---- layout validation --------------------------------------------------------------------------------------
+fpd_status check_layout(const fpd_vocab_layout* lay, int V) {
+  if (!lay->class_off || !lay->class_ranges || !lay->pos_class)
+    return fail(FPD_ERR_INVALID_ARG, "layout: class_off, class_ranges and pos_class must be non-null");
+  if (lay->n_class < 1 || lay->n_class > FPD_MAX_CLASSES)
+    return fail(FPD_ERR_CAPACITY, "layout: n_class %d outside [1, %d]", lay->n_class, FPD_MAX_CLASSES);
+  if (lay->class_off[0] != 0) return fail(FPD_ERR_SHAPE, "layout: class_off[0] must be 0");
+  for (int c = 0; c < lay->n_class; c++) {
+    const int q0 = lay->class_off[c], q1 = lay->class_off[c + 1];
+    if (q1 <= q0) return fail(FPD_ERR_SHAPE, "layout: class %d has no id range", c);
+    if (q1 > FPD_MAX_RANGES) return fail(FPD_ERR_CAPACITY, "layout: more than %d id ranges", FPD_MAX_RANGES);
+    for (int q = q0; q < q1; q++) {
+      const int lo = lay->class_ranges[2 * q], hi = lay->class_ranges[2 * q + 1];
+      if (lo < 0 || hi > V || lo >= hi) return fail(FPD_ERR_SHAPE, "layout: range %d = [%d, %d) invalid for V = %d", q, lo, hi, V);
+      if (q > q0 && lo < lay->class_ranges[2 * q - 1])
+        return fail(FPD_ERR_SHAPE, "layout: ranges of class %d must be sorted and disjoint", c);
+    }
+  }
+  return FPD_OK;
+}
+
+}  // namespace
+
+// ============================================================================================================
+extern "C" {
+
+struct fpd_model : public Model {};
+
+const char* fpd_last_error(void) { return t_err.c_str(); }
+
+uint64_t fpd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+fpd_status fpd_device_status(void* stream, int32_t* code) {
+  if (!code) return fail(FPD_ERR_INVALID_ARG, "code must be non-null");
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t h = 0, zero = 0;
+  FPD_CUDA(cudaMemcpyFromSymbolAsync(&h, g_device_check, sizeof(h), 0, cudaMemcpyDeviceToHost, st), "read check word");
+  FPD_CUDA(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  FPD_CUDA(cudaMemcpyToSymbolAsync(g_device_check, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st), "clear check word");
+  FPD_CUDA(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  *code = h;
+  return h ? fail(FPD_ERR_DEVICE_CHECK, "device check %d", h) : FPD_OK;
+}
+
+fpd_status fpd_model_create(const fpd_model_desc* desc, const fpd_weights* w, fpd_model** out) {
+  if (!desc || !w || !out) return fail(FPD_ERR_INVALID_ARG, "desc, weights and out must be non-null");
+  *out = nullptr;
+  const fpd_model_desc& d = *desc;
+  if (d.n_layers < 1 || d.n_layers > FPD_MAX_LAYERS) return fail(FPD_ERR_UNSUPPORTED, "n_layers %d", d.n_layers);
+  if (d.head_dim != 64 && d.head_dim != 128) return fail(FPD_ERR_UNSUPPORTED, "head_dim %d (64 or 128)", d.head_dim);
+  if (d.d_model < 64 || d.d_model % 64 || d.d_ff < 64 || d.d_ff % 64)
+    return fail(FPD_ERR_UNSUPPORTED, "d_model %d / d_ff %d must be positive multiples of 64", d.d_model, d.d_ff);
+  if (d.n_kv_heads < 1 || d.n_q_heads < d.n_kv_heads || d.n_q_heads % d.n_kv_heads)
+    return fail(FPD_ERR_UNSUPPORTED, "n_q_heads %d must be a multiple of n_kv_heads %d", d.n_q_heads, d.n_kv_heads);
+  if ((d.n_q_heads * d.head_dim) % 64) return fail(FPD_ERR_UNSUPPORTED, "n_q_heads * head_dim must be a multiple of 64");
+  if (d.vocab < 2) return fail(FPD_ERR_SHAPE, "vocab %d", d.vocab);
+  if (d.n_feat < 1 || d.n_feat > 8) return fail(FPD_ERR_UNSUPPORTED, "n_feat %d (1..8)", d.n_feat);
+  if (d.max_pos < 2) return fail(FPD_ERR_SHAPE, "max_pos %d", d.max_pos);
+  if (!(d.rms_eps > 0.f) || !(d.rope_theta > 1.f)) return fail(FPD_ERR_SHAPE, "rms_eps must be > 0 and rope_theta > 1");
+  const void* glob[] = {w->embed, w->w_fc, w->hidden_norm, w->final_norm, w->lm_head};
+  for (const void* p : glob)
+    if (!p || !aligned16(p)) return fail(FPD_ERR_INVALID_ARG, "a global weight pointer is null or not 16-byte aligned");
+  for (int l = 0; l < d.n_layers; l++) {
+    const void* lp[] = {w->attn_norm[l], w->wqkv[l], w->q_norm[l], w->k_norm[l],
+                        w->wo[l],        w->mlp_norm[l], w->w_gate_up[l], w->w_down[l]};
+    for (const void* p : lp)
+      if (!p || !aligned16(p)) return fail(FPD_ERR_INVALID_ARG, "layer %d: a weight pointer is null or not 16-byte aligned", l);
+  }
+  {
+    static std::once_flag once;
+    static cudaError_t init_err = cudaSuccess;
+    std::call_once(once, [] {
+      init_err = tc_init_attributes();
+      if (init_err == cudaSuccess) init_err = attn_init_attributes();
+    });
+    if (init_err != cudaSuccess) return cuda_fail(init_err, "kernel attributes");
+  }
+  fpd_model* m = new fpd_model();
+  m->d = d;
+  m->w = *w;
+  cudaError_t e = cudaGetDevice(&m->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
+  if (e != cudaSuccess) {
+    delete m;
+    return cuda_fail(e, "device query");
+  }
+  // RoPE table: angle(pos, i) = pos * theta^(-2i/h), evaluated in double, stored as fp32 (cos, sin).
+  const int half = d.head_dim / 2;
+  std::vector<float2> tab((size_t)d.max_pos * half);
+  for (int i = 0; i < half; i++) {
+    const double f = std::pow((double)d.rope_theta, -2.0 * i / d.head_dim);
+    for (int p = 0; p < d.max_pos; p++) {
+      const double a = (double)p * f;
+      tab[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+  }
+  e = cudaMalloc(&m->rope, tab.size() * sizeof(float2));
+  if (e == cudaSuccess) e = cudaMemcpy(m->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    if (m->rope) cudaFree(m->rope);
+    delete m;
+    return cuda_fail(e, "RoPE table");
+  }
+  *out = m;
+  return FPD_OK;
+}
+
+void fpd_model_destroy(fpd_model* m) {
+  if (!m) return;
+  if (m->rope) cudaFree(m->rope);
+  delete m;
+}
+
+size_t fpd_kv_store_bytes(const fpd_model* m, int batch, int t_cap) {
+  if (!m || batch < 1 || t_cap < 1) return 0;
+  return (size_t)m->d.n_layers * batch * 2 * m->d.n_kv_heads * (size_t)t_cap * m->d.head_dim * sizeof(bf16);
+}
+
+size_t fpd_workspace_bytes(const fpd_model* m, int batch, int max_block_len, int t_cap) {
+  if (!m || batch < 1 || max_block_len < 2 || t_cap < 1) return 0;
+  // Calls may use any smaller batch and block length; the carve is not monotone in them (the attention
+  // split count grows as the batch shrinks), so take the maximum over all of them.
+  size_t a = 0, b = 0;
+  for (int bb = 1; bb <= batch; bb++)
+    for (int ll = 2; ll <= max_block_len; ll++) {
+      a = std::max(a, ws_draft_bytes(*m, bb, ll, t_cap));
+      b = std::max(b, ws_argmax_bytes(*m, bb, ll));
+    }
+  size_t c = ws_prep_bytes(*m, (int)std::min<long long>((long long)batch * t_cap, 1 << 30));
+  return std::max(a, std::max(b, c)) + 256;
+}
+
+// ---- a1 + a2 ------------------------------------------------------------------------------------------------
+fpd_status fpd_prepare_context(fpd_model* m, int batch, int total_rows, const int32_t* row_off,
+                               const int32_t* pos_start, const void* const* feats, void* kv_store, int t_cap,
+                               void* workspace, size_t ws_bytes, void* stream) {
+  if (!m) return fail(FPD_ERR_INVALID_ARG, "model is null");
+  const auto& d = m->d;
+  if (batch < 1 || total_rows < 0 || t_cap < 1) return fail(FPD_ERR_SHAPE, "batch %d, total_rows %d, t_cap %d", batch, total_rows, t_cap);
+  if (t_cap > d.max_pos) return fail(FPD_ERR_CAPACITY, "t_cap %d exceeds max_pos %d", t_cap, d.max_pos);
+  if ((long long)total_rows > (long long)batch * t_cap) return fail(FPD_ERR_CAPACITY, "total_rows %d exceeds batch * t_cap", total_rows);
+  if (!row_off || !feats || !kv_store || !workspace) return fail(FPD_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(kv_store) || !aligned16(workspace)) return fail(FPD_ERR_INVALID_ARG, "kv_store/workspace not 16-byte aligned");
+  for (int s = 0; s < d.n_feat && total_rows > 0; s++)
+    if (!feats[s] || !aligned16(feats[s])) return fail(FPD_ERR_INVALID_ARG, "feats[%d] null or not 16-byte aligned", s);
+  fpd_status ds = check_device(*m);
+  if (ds) return ds;
+  Carver c;
+  c.base = (char*)workspace;
+  PrepWs w = carve_prep(*m, c, total_rows);
+  if (c.off > ws_bytes) return fail(FPD_ERR_CAPACITY, "workspace %zu < %zu bytes", ws_bytes, c.off);
+  if (total_rows == 0) return FPD_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int h = d.head_dim, nkv = d.n_kv_heads;
+  for (int r0 = 0; r0 < total_rows; r0 += w.chunk) {
+    const int R = std::min(w.chunk, total_rows - r0);
+    GemmArgs g{};
+    for (int s = 0; s < d.n_feat; s++) g.a[s] = (const bf16*)feats[s] + (size_t)r0 * d.d_model;
+    g.seg_k = d.d_model;
+    g.lda = d.d_model;
+    g.b = (const bf16*)m->w.w_fc;
+    g.ldb = d.n_feat * d.d_model;
+    g.c = w.part;
+    g.ldc = d.d_model;
+    g.M = R;
+    g.N = d.d_model;
+    g.K = d.n_feat * d.d_model;
+    g.c_split_stride = (size_t)R * g.N;
+    const TcPlan pf = tc_plan_gemm(R, g.N, g.K, m->num_sms);
+    g.k_split = pf.k_split;
+    FPD_CUDA(launch_tc_gemm(g, pf, st), "fusion GEMM");
+    FPD_CUDA(launch_rmsnorm_partials(w.ctx, w.part, pf.splits, g.c_split_stride, (const bf16*)m->w.hidden_norm, R,
+                                     d.d_model, d.rms_eps, st),
+             "fusion RMSNorm");
+    for (int l = 0; l < d.n_layers; l++) {
+      GemmArgs k{};
+      k.a[0] = w.ctx;
+      k.seg_k = d.d_model;
+      k.lda = d.d_model;
+      k.b = (const bf16*)m->w.wqkv[l] + (size_t)d.n_q_heads * h * d.d_model;  // k rows then v rows
+      k.ldb = d.d_model;
+      k.c = w.part;
+      k.ldc = 2 * nkv * h;
+      k.M = R;
+      k.N = 2 * nkv * h;
+      k.K = d.d_model;
+      k.c_split_stride = (size_t)R * k.N;
+      const TcPlan pk = tc_plan_gemm(R, k.N, k.K, m->num_sms);
+      k.k_split = pk.k_split;
+      FPD_CUDA(launch_tc_gemm(k, pk, st), "context K/V GEMM");
+      FPD_CUDA(launch_kv_post((bf16*)kv_store, w.part, pk.splits, k.c_split_stride, (const bf16*)m->w.k_norm[l],
+                              m->rope, row_off, pos_start, batch, l, t_cap, r0, R, nkv, h, d.rms_eps, st),
+               "context K/V epilogue");
+    }
+  }
+  return FPD_OK;
+}
+
+// ---- a3..a7 -------------------------------------------------------------------------------------------------
+fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store, int t_cap, const int32_t* ctx_len,
+                           const int32_t* anchor, int32_t mask_id, void* hidden_out, void* layer_hidden,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  if (!m) return fail(FPD_ERR_INVALID_ARG, "model is null");
+  const auto& d = m->d;
+  if (batch < 1 || L < 2 || t_cap < 1) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d, t_cap %d", batch, L, t_cap);
+  if ((long long)t_cap + L > d.max_pos) return fail(FPD_ERR_CAPACITY, "t_cap + block_len %d exceeds max_pos %d", t_cap + L, d.max_pos);
+  if (mask_id < 0 || mask_id >= d.vocab) return fail(FPD_ERR_SHAPE, "mask_id %d outside [0, %d)", mask_id, d.vocab);
+  if (!kv_store || !ctx_len || !anchor || !hidden_out || !workspace) return fail(FPD_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(kv_store) || !aligned16(hidden_out) || !aligned16(workspace) || (layer_hidden && !aligned16(layer_hidden)))
+    return fail(FPD_ERR_INVALID_ARG, "kv_store/hidden_out/layer_hidden/workspace not 16-byte aligned");
+  fpd_status ds = check_device(*m);
+  if (ds) return ds;
+  Carver c;
+  c.base = (char*)workspace;
+  DraftWs w = carve_draft(*m, c, batch, L, t_cap);
+  if (c.off > ws_bytes) return fail(FPD_ERR_CAPACITY, "workspace %zu < %zu bytes", ws_bytes, c.off);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int M = batch * L, dm = d.d_model, h = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.d_ff;
+  const int nqkv = (nq + 2 * nkv) * h;
+  bf16* x = (bf16*)hidden_out;
+  FPD_CUDA(launch_embed(x, (const bf16*)m->w.embed, anchor, mask_id, batch, L, dm, d.vocab, st), "embed");
+  auto gemm = [&](const bf16* A, int K, const void* W, int N, const TcPlan& pl) {
+    GemmArgs g{};
+    g.a[0] = A;
+    g.seg_k = K;
+    g.lda = K;
+    g.b = (const bf16*)W;
+    g.ldb = K;
+    g.c = w.part;
+    g.ldc = N;
+    g.c_split_stride = (size_t)M * N;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.k_split = pl.k_split;
+    return launch_tc_gemm(g, pl, st);
+  };
+  for (int l = 0; l < d.n_layers; l++) {
+    FPD_CUDA(launch_rmsnorm(w.xn, x, (const bf16*)m->w.attn_norm[l], M, dm, d.rms_eps, 0, st), "attention norm");
+    FPD_CUDA(gemm(w.xn, dm, m->w.wqkv[l], nqkv, w.p_qkv), "QKV GEMM");
+    FPD_CUDA(launch_qkv_post(w.q, w.kblk, w.vblk, w.part, w.p_qkv.splits, (size_t)M * nqkv,
+                             (const bf16*)m->w.q_norm[l], (const bf16*)m->w.k_norm[l], m->rope, ctx_len, t_cap, batch,
+                             L, nq, nkv, h, d.rms_eps, st),
+             "q/k norm + RoPE");
+    AttnArgs a{};
+    a.q = w.q;
+    a.store = (const bf16*)kv_store;
+    a.kblk = w.kblk;
+    a.vblk = w.vblk;
+    a.ctx_len = ctx_len;
+    a.o_part = w.o_part;
+    a.ml = w.ml;
+    a.batch = batch;
+    a.L = L;
+    a.nq = nq;
+    a.nkv = nkv;
+    a.head_dim = h;
+    a.t_cap = t_cap;
+    a.layer = l;
+    a.rows = M;
+    a.splits = w.att_splits;
+    a.chunk = w.att_chunk;
+    FPD_CUDA(launch_attention(a, w.o, st), "attention");
+    FPD_CUDA(gemm(w.o, nq * h, m->w.wo[l], dm, w.p_o), "O GEMM");
+    FPD_CUDA(launch_residual_add(x, w.part, w.p_o.splits, (size_t)M * dm, (size_t)M * dm, st), "residual");
+    FPD_CUDA(launch_rmsnorm(w.xn, x, (const bf16*)m->w.mlp_norm[l], M, dm, d.rms_eps, 0, st), "MLP norm");
+    FPD_CUDA(gemm(w.xn, dm, m->w.w_gate_up[l], 2 * F, w.p_gu), "gate/up GEMM");
+    FPD_CUDA(launch_swiglu(w.hmid, w.part, w.p_gu.splits, (size_t)M * 2 * F, M, F, st), "SwiGLU");
+    FPD_CUDA(gemm(w.hmid, F, m->w.w_down[l], dm, w.p_down), "down GEMM");
+    FPD_CUDA(launch_residual_add(x, w.part, w.p_down.splits, (size_t)M * dm, (size_t)M * dm, st), "residual");
+    if (layer_hidden)
+      FPD_CUDA(cudaMemcpyAsync((bf16*)layer_hidden + (size_t)l * M * dm, x, (size_t)M * dm * sizeof(bf16),
+                               cudaMemcpyDeviceToDevice, st),
+               "layer_hidden copy");
+  }
+  return FPD_OK;
+}
+
+// ---- a8 -----------------------------------------------------------------------------------------------------
+fpd_status fpd_constrain_argmax(fpd_model* m, int batch, int L, const void* hidden, const fpd_vocab_layout* layout,
+                                int32_t* tokens_out, float* logits_out, void* workspace, size_t ws_bytes,
+                                void* stream) {
+  if (!m) return fail(FPD_ERR_INVALID_ARG, "model is null");
+  const auto& d = m->d;
+  if (batch < 1 || L < 2) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d", batch, L);
+  if (!hidden || !tokens_out || !workspace) return fail(FPD_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(hidden) || !aligned16(workspace)) return fail(FPD_ERR_INVALID_ARG, "hidden/workspace not 16-byte aligned");
+  if (layout) {
+    fpd_status s = check_layout(layout, d.vocab);
+    if (s) return s;
+  }
+  fpd_status ds = check_device(*m);
+  if (ds) return ds;
+  Carver c;
+  c.base = (char*)workspace;
+  ArgmaxWs w = carve_argmax(*m, c, batch, L);
+  if (c.off > ws_bytes) return fail(FPD_ERR_CAPACITY, "workspace %zu < %zu bytes", ws_bytes, c.off);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int n_rows = batch * (L - 1);
+  LmPlan p{};
+  p.n_rows = n_rows;
+  p.L = L;
+  p.ct = kLmColTile;
+  p.rt = w.row_tile;
+  if (layout) {
+    p.n_class = layout->n_class;
+    p.n_range = layout->class_off[layout->n_class];
+    for (int cl = 0; cl < layout->n_class; cl++)
+      for (int q = layout->class_off[cl]; q < layout->class_off[cl + 1]; q++) {
+        p.range_lo[q] = layout->class_ranges[2 * q];
+        p.range_hi[q] = layout->class_ranges[2 * q + 1];
+        p.range_class[q] = cl;
+      }
+  } else {
+    p.n_class = 1;
+    p.n_range = 1;
+    p.range_lo[0] = 0;
+    p.range_hi[0] = d.vocab;
+    p.range_class[0] = 0;
+  }
+  FPD_CUDA(launch_lm_plan(p, layout ? layout->pos_class : nullptr, w.rows_sorted, w.inv_sorted, w.class_row_off,
+                          w.items, w.n_items, w.packed, w.max_items, st),
+           "LM-head plan");
+  FPD_CUDA(launch_rmsnorm_gather(w.z, (const bf16*)hidden, (const bf16*)m->w.final_norm, w.rows_sorted, n_rows,
+                                 d.d_model, d.rms_eps, L, st),
+           "final norm");
+  FPD_CUDA(launch_tc_lmhead(p, w.z, n_rows, (const bf16*)m->w.lm_head, d.d_model, d.vocab, w.items, w.n_items,
+                            w.max_items, w.packed, w.rows_sorted, logits_out, m->num_sms, st),
+           "LM head + argmax");
+  FPD_CUDA(launch_lm_decode(tokens_out, w.packed, w.inv_sorted, n_rows, st), "argmax decode");
+  return FPD_OK;
+}
+
+// ---- a9 -----------------------------------------------------------------------------------------------------
+fpd_status fpd_verify(int mode, int batch, int L, const int32_t* draft, const int32_t* target,
+                      const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id, int32_t* accept_len,
+                      int32_t* committed, int32_t* valid_out, void* stream) {
+  if (mode != FPD_VERIFY_TEXT && mode != FPD_VERIFY_SCHEMA) return fail(FPD_ERR_INVALID_ARG, "mode %d", mode);
+  if (batch < 1 || L < 2) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d", batch, L);
+  if (!draft || !accept_len || !committed) return fail(FPD_ERR_INVALID_ARG, "null pointer argument");
+  VerifyTables tb{};
+  if (mode == FPD_VERIFY_TEXT) {
+    if (!target) return fail(FPD_ERR_INVALID_ARG, "text mode needs target");
+  } else {
+    if (!layout || !rule) return fail(FPD_ERR_INVALID_ARG, "schema mode needs layout and rule");
+    fpd_status s = check_layout(layout, INT32_MAX);
+    if (s) return s;
+    tb.n_class = layout->n_class;
+    for (int cl = 0; cl <= layout->n_class; cl++) tb.class_off[cl] = layout->class_off[cl];
+    for (int q = 0; q < layout->class_off[layout->n_class]; q++) {
+      tb.lo[q] = layout->class_ranges[2 * q];
+      tb.hi[q] = layout->class_ranges[2 * q + 1];
+    }
+  }
+  FPD_CUDA(launch_verify(mode, batch, L, draft, target, tb, layout ? layout->pos_class : nullptr, rule, pad_id,
+                         accept_len, committed, valid_out, (cudaStream_t)stream),
+           "verify");
+  return FPD_OK;
+}
+
+}  // extern "C"

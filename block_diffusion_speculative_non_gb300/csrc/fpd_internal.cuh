@@ -1,0 +1,69 @@
+// fpd_internal.cuh — shared internals of libfpd (kernels + C ABI).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "../../include/fpd.h"
+
+namespace fpd {
+
+using bf16 = __nv_bfloat16;
+
+// ---- device-side check word (bounded waits that ran out, ids out of range) --------------------------------
+// Kernels never trap: they record the first failure here and skip the offending access.
+enum DeviceCheck : int32_t {
+  kCheckOk = 0,
+  kCheckBadToken = 1,        // an id outside [0, V) reached the embedding gather
+  kCheckWaitTimeout = 2,     // an mbarrier / flag wait exceeded its limit
+  kCheckNoLegalId = 3,       // a position's class had no legal id (empty argmax)
+  kCheckBadClass = 4,        // pos_class outside [0, n_class)
+};
+extern __device__ int32_t g_device_check;
+
+__device__ __forceinline__ void record_check(int32_t code) { atomicCAS(&g_device_check, 0, code); }
+
+// ---- host-side bookkeeping ---------------------------------------------------------------------------------
+extern std::atomic<uint64_t> g_launches;
+inline void count_launch(uint64_t n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// ---- model -------------------------------------------------------------------------------------------------
+struct Model {
+  fpd_model_desc d;
+  fpd_weights w;
+  int device = 0;
+  int num_sms = 0;
+  float2* rope = nullptr;   // [max_pos][head_dim/2] (cos, sin), built in double on the host
+};
+
+// ---- small helpers -----------------------------------------------------------------------------------------
+__host__ __device__ constexpr inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr inline size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Orderable packing of (fp32 value, id) into 64 bits: a larger packed word means a larger value, and for
+// equal values the SMALLER id.  atomicMax over packed words is therefore an argmax with lowest-id ties,
+// independent of the order in which CTAs arrive.
+__device__ __forceinline__ unsigned long long pack_argmax(float v, int id) {
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
+}
+__device__ __forceinline__ int unpack_argmax_id(unsigned long long p) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(p & 0xFFFFFFFFull));
+}
+
+}  // namespace fpd

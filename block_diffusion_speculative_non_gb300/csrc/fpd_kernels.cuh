@@ -1,0 +1,104 @@
+// fpd_kernels.cuh — launch interfaces of the kernels behind the C ABI (internal).
+#pragma once
+
+#include <algorithm>
+
+#include "fpd_internal.cuh"
+
+namespace fpd {
+
+// ---- GEMM:  C[split][m][n] = sum_{k in split} A[m][k] * B[n][k]   (fp32 partials) ------------------------------
+struct GemmArgs {
+  const bf16* a[8];     // K-segments of A; segment s covers k in [s*seg_k, (s+1)*seg_k)
+  int seg_k;
+  int lda;              // row stride of every A segment (elements)
+  const bf16* b;        // B [N, K] row-major (weights, [out, in])
+  int ldb;
+  float* c;             // C [splits][M][ldc]
+  int ldc;
+  size_t c_split_stride;
+  int M, N, K;
+  int k_split;          // K elements per split (multiple of 64)
+};
+cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t st);
+
+// tcgen05 GEMM: the plan fixes operand placement, tile width, split-K and grid for a shape.
+struct TcPlan {
+  bool swap;      // weights on the 128-row MMA operand (few tokens)
+  int bn;         // width of the other operand's tile
+  int pt, qt;     // tiles along the 128-row and the bn-row operand
+  int splits, k_split;
+  int grid;       // persistent CTAs
+};
+TcPlan tc_plan_gemm(int M, int N, int K, int num_sms);
+TcPlan tc_plan_force(int M, int N, int K, int num_sms, int placement);   // placement 0: tokens on 128 rows, 1: weights
+cudaError_t launch_tc_gemm(const GemmArgs& g, const TcPlan& plan, cudaStream_t st);
+cudaError_t tc_init_attributes();     // once per process, before any stream capture
+cudaError_t attn_init_attributes();
+cudaError_t launch_sum_splits(float* out, const float* part, int splits, size_t n, cudaStream_t st);
+
+// ---- row ops -------------------------------------------------------------------------------------------------
+cudaError_t launch_embed(bf16* x, const bf16* embed, const int32_t* anchor, int32_t mask_id, int B, int L, int d,
+                         int V, cudaStream_t st);
+cudaError_t launch_rmsnorm(bf16* out, const bf16* in, const bf16* g, int rows, int d, float eps, int skip_L,
+                           cudaStream_t st);
+cudaError_t launch_rmsnorm_partials(bf16* out, const float* part, int nsplit, size_t split_stride, const bf16* g,
+                                    int rows, int d, float eps, cudaStream_t st);
+cudaError_t launch_qkv_post(bf16* q, bf16* kblk, bf16* vblk, const float* part, int nsplit, size_t split_stride,
+                            const bf16* q_norm, const bf16* k_norm, const float2* rope, const int32_t* ctx_len,
+                            int t_cap, int B, int L, int nq, int nkv, int h, float eps, cudaStream_t st);
+cudaError_t launch_kv_post(bf16* store, const float* part, int nsplit, size_t split_stride, const bf16* k_norm,
+                           const float2* rope, const int32_t* row_off, const int32_t* pos_start, int batch, int layer,
+                           int t_cap, int row0, int rows, int nkv, int h, float eps, cudaStream_t st);
+cudaError_t launch_residual_add(bf16* x, const float* part, int nsplit, size_t split_stride, size_t n,
+                                cudaStream_t st);
+cudaError_t launch_swiglu(bf16* hmid, const float* part, int nsplit, size_t split_stride, int rows, int F,
+                          cudaStream_t st);
+
+// ---- attention ---------------------------------------------------------------------------------------------
+struct AttnArgs {
+  const bf16* q;        // [B*L, nq, h]
+  const bf16* store;    // context KV store [layer][b][K|V][g][t_cap][h]
+  const bf16* kblk;     // [B, nkv, L, h]
+  const bf16* vblk;
+  const int32_t* ctx_len;
+  float* o_part;        // [splits][B*L][nq][h]
+  float2* ml;           // [splits][B*L][nq]  (running max, running sum)
+  int batch, L, nq, nkv, head_dim, t_cap, layer;
+  int rows;             // B*L
+  int splits, chunk;    // KV splits and keys per split
+};
+void attn_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* splits, int* chunk);
+cudaError_t launch_attention(const AttnArgs& a, bf16* out, cudaStream_t st);
+
+// ---- LM head + constrained argmax ------------------------------------------------------------------------------
+struct LmPlan {
+  int n_class, n_range, n_rows, L;
+  int ct, rt;           // column (id) tile and row (position) tile of one work item
+  int range_lo[FPD_MAX_RANGES], range_hi[FPD_MAX_RANGES], range_class[FPD_MAX_RANGES];
+};
+// rows_sorted: sorted slot -> original row (-1 past the last placed row); inv_sorted: original row -> slot.
+cudaError_t launch_lm_plan(const LmPlan& p, const int16_t* pos_class, int* rows_sorted, int* inv_sorted,
+                           int* class_row_off, int4* items, int* n_items, unsigned long long* packed, int max_items,
+                           cudaStream_t st);
+int tc_lm_row_tile(int n_rows);
+cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows, const bf16* W, int d, int V,
+                             const int4* items, const int* n_items, int max_items, unsigned long long* packed,
+                             const int* rows_sorted, float* logits, int num_sms, cudaStream_t st);
+cudaError_t launch_lm_decode(int32_t* tokens, const unsigned long long* packed, const int* inv_sorted, int n,
+                             cudaStream_t st);
+// RMSNorm of block rows into sorted order: out[i] = norm(hidden[map(rows_sorted[i])]), map drops anchors.
+cudaError_t launch_rmsnorm_gather(bf16* out, const bf16* in, const bf16* g, const int* rows_sorted, int rows, int d,
+                                  float eps, int L, cudaStream_t st);
+
+// ---- verify -----------------------------------------------------------------------------------------------------
+struct VerifyTables {
+  int n_class;
+  int class_off[FPD_MAX_CLASSES + 1];
+  int lo[FPD_MAX_RANGES], hi[FPD_MAX_RANGES];
+};
+cudaError_t launch_verify(int mode, int B, int L, const int32_t* draft, const int32_t* target, const VerifyTables& tb,
+                          const int16_t* pos_class, const int8_t* rule, int32_t pad_id, int32_t* accept,
+                          int32_t* committed, int32_t* valid, cudaStream_t st);
+
+}  // namespace fpd

@@ -1,0 +1,490 @@
+// k_gemm_tc.cu — persistent, warp-specialised tcgen05 GEMM for sm_103a, and the LM-head + argmax variant.
+//
+//   D[m][n] = sum_k X[m][k] * W[n][k]      X = activations [M, K] (K-major, bf16, may be K-segmented),
+//                                          W = weights     [N, K] (K-major, bf16, [out, in])
+//
+// Two operand placements share one kernel:
+//   SWAP  (few tokens, M <= 64): the 128-row MMA operand is a tile of W (output features) and the BN-row
+//          operand holds the tokens.  Weight streaming is the whole cost at batch 1, so every SM pulls weight
+//          tiles through a deep TMA ring; split-K over the grid supplies enough CTAs.
+//   !SWAP (many tokens): the 128-row operand is a token tile and the BN-row (128/256) operand a weight tile.
+//
+// Roles (6 warps): warp 0 issues TMA loads into a STAGES-deep shared-memory ring (128-byte swizzled K-major
+// tiles, one mbarrier pair per stage); warp 1 owns TMEM and one lane issues tcgen05.mma (M = 128, N = BN,
+// K = 16 per instruction, fp32 accumulators in TMEM, two accumulator buffers so the epilogue of one tile
+// overlaps the main loop of the next); warps 2-5 read the accumulators back with tcgen05.ld (each warp sees
+// its 32-lane quarter of TMEM) and run the epilogue.  Every wait is bounded (tc::mbar_wait).
+//
+// Epilogues:  EPI_STORE  — fp32 partial sums to C[split][M][ldc] (split-K partials are reduced by the
+//                          consumer row kernel, in fixed order).
+//             EPI_ARGMAX — LM head (VFlash paper (zh) §2.5: constraints act on computed logits): the MMA rows
+//                          are vocabulary ids of one legal range, the columns positions of that range's class;
+//                          per position the (logit, id) maximum is folded into a 64-bit word by atomicMax
+//                          (lowest id on ties, order independent).
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "fpd_kernels.cuh"
+#include "tc_primitives.cuh"
+
+namespace fpd {
+
+namespace {
+
+constexpr int BM = 128, BK = 64, UMMA_K = 16;
+constexpr int kThreads = 192;
+enum { EPI_STORE = 0, EPI_ARGMAX = 1 };
+
+struct TcParams {
+  CUtensorMap tm_x[8];   // activation K-segments (box rows: BN if swap else 128)
+  CUtensorMap tm_w;      // weights (box rows: 128 if swap else BN)
+  int n_seg, seg_k;
+  int M, N, K;
+  // EPI_STORE
+  float* c;
+  int ldc;
+  size_t c_split_stride;
+  int pt, qt, splits, k_split;   // tiles along the 128-row operand, the BN-row operand, and K splits
+  // EPI_ARGMAX
+  const int4* items;             // (range, first id, first sorted row, row count)
+  const int* n_items;
+  int hi_tab[FPD_MAX_RANGES];    // end (exclusive) of every legal id range
+  unsigned long long* packed;    // [sorted rows]
+  const int* rows_sorted;        // sorted row -> original row (logits only)
+  float* logits;                 // [n_rows, V] or null
+  int V;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // two accumulator buffers
+};
+
+struct Work {
+  int a_row0, b_row0;   // first row of the 128-row (A) and BN-row (B) operand tiles
+  int k0, nkb;          // first K element and number of BK blocks
+  int split;
+  int range;            // EPI_ARGMAX: range index; rows valid below `b_cnt`
+  int b_cnt;
+};
+
+template <bool SWAP, int BN, int EPI>
+__device__ __forceinline__ bool get_work(const TcParams& p, int t, int total, Work& w) {
+  if (t >= total) return false;
+  if (EPI == EPI_STORE) {
+    const int pi = t % p.pt, qi = (t / p.pt) % p.qt, s = t / (p.pt * p.qt);
+    w.a_row0 = pi * BM;
+    w.b_row0 = qi * BN;
+    w.split = s;
+    w.k0 = s * p.k_split;
+    const int k1 = min(p.K, w.k0 + p.k_split);
+    w.nkb = (k1 - w.k0) / BK;
+    w.range = 0;
+    w.b_cnt = BN;
+  } else {
+    const int4 it = p.items[t];
+    w.range = it.x;
+    w.a_row0 = it.y;
+    w.b_row0 = it.z;
+    w.b_cnt = it.w;
+    w.split = 0;
+    w.k0 = 0;
+    w.nkb = p.K / BK;
+  }
+  return true;
+}
+
+template <int BN, int STAGES, bool SWAP, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * STAGES, tfull0 = empty0 + 8 * STAGES,
+                 tempty0 = tfull0 + 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int total = (EPI == EPI_STORE) ? p.pt * p.qt * p.splits : *p.n_items;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; s++) {
+      tc::mbar_init(full0 + 8 * s, 1);
+      tc::mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; a++) {
+      tc::mbar_init(tfull0 + 8 * a, 1);
+      tc::mbar_init(tempty0 + 8 * a, 4);   // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch(&p.tm_w);
+    for (int s = 0; s < p.n_seg; s++) tc::tma_prefetch(&p.tm_x[s]);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      Work w;
+      for (int t = blockIdx.x; get_work<SWAP, BN, EPI>(p, t, total, w) && !*abort_flag; t += gridDim.x) {
+        for (int kb = 0; kb < w.nkb; kb++) {
+          if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1)) { *abort_flag = 1; break; }
+          const uint32_t fb = full0 + 8 * stage;
+          tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+          const int k = w.k0 + kb * BK;
+          const int seg = k / p.seg_k, kx = k - seg * p.seg_k;
+          if (SWAP) {
+            tc::tma_load_2d(sa, &p.tm_w, k, w.a_row0, fb);
+            tc::tma_load_2d(sb, &p.tm_x[seg], kx, w.b_row0, fb);
+          } else {
+            tc::tma_load_2d(sa, &p.tm_x[seg], kx, w.a_row0, fb);
+            tc::tma_load_2d(sb, &p.tm_w, k, w.b_row0, fb);
+          }
+          issued++;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA can exit (bounded)
+        for (int s = 0; s < STAGES && s < issued; s++) {
+          if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
+          tc::mbar_wait(full0 + 8 * stage, phase);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      Work w;
+      for (int t = blockIdx.x; get_work<SWAP, BN, EPI>(p, t, total, w); t += gridDim.x, it++) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        if (!*abort_flag && !tc::mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1)) *abort_flag = 1;
+        tc::tc_fence_after();
+        for (int kb = 0; kb < w.nkb && !*abort_flag; kb++) {
+          if (!tc::mbar_wait(full0 + 8 * stage, phase)) { *abort_flag = 1; break; }
+          tc::tc_fence_after();
+          const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; kk++) {
+            const uint64_t da = tc::sw128_kmajor_desc(sa + kk * UMMA_K * 2);
+            const uint64_t db = tc::sw128_kmajor_desc(sb + kk * UMMA_K * 2);
+            tc::umma_bf16(d_tmem, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::umma_commit(empty0 + 8 * stage);   // frees the stage once these MMAs have read it
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        tc::umma_commit(tfull0 + 8 * acc);       // accumulator ready (also on abort: never leave waiters)
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 ----------------
+    const int quarter = warp & 3;               // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int row_in_tile = quarter * 32 + lane;
+    int it = 0;
+    Work w;
+    for (int t = blockIdx.x; get_work<SWAP, BN, EPI>(p, t, total, w); t += gridDim.x, it++) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!tc::mbar_wait(tfull0 + 8 * acc, acc_phase)) *abort_flag = 1;
+      tc::tc_fence_after();
+      const uint32_t t_acc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      if (EPI == EPI_STORE) {
+        float* Cs = p.c + (size_t)w.split * p.c_split_stride;
+        const bool empty_k = w.nkb == 0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tc::tmem_ld16(t_acc + c0, v);
+          if (empty_k) {
+#pragma unroll
+            for (int j = 0; j < 16; j++) v[j] = 0.f;
+          }
+          if (SWAP) {
+            const int n = w.a_row0 + row_in_tile;
+            if (n < p.N) {
+#pragma unroll
+              for (int j = 0; j < 16; j++) {
+                const int m = w.b_row0 + c0 + j;
+                if (m < p.M) Cs[(size_t)m * p.ldc + n] = v[j];
+              }
+            }
+          } else {
+            const int m = w.a_row0 + row_in_tile;
+            const int n0 = w.b_row0 + c0;
+            if (m < p.M) {
+              float* dst = Cs + (size_t)m * p.ldc + n0;
+              if (n0 + 16 <= p.N && (p.ldc & 3) == 0) {
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                  *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++)
+                  if (n0 + j < p.N) dst[j] = v[j];
+              }
+            }
+          }
+        }
+      } else {
+        // LM head: rows = vocabulary ids, columns = sorted positions of one class
+        const int vid = w.a_row0 + row_in_tile;
+        const bool vok = vid < p.hi_tab[w.range];
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tc::tmem_ld16(t_acc + c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; j++) {
+            const int col = c0 + j;
+            const bool ok = vok && col < w.b_cnt;
+            unsigned long long best = ok ? pack_argmax(v[j], vid) : 0ull;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+            if (lane == 0 && best) atomicMax(p.packed + w.b_row0 + col, best);
+            if (p.logits && ok) p.logits[(size_t)p.rows_sorted[w.b_row0 + col] * p.V + vid] = v[j];
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---- host side ------------------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] with row stride ld (elements), boxes of 64 columns x box_rows rows,
+// 128-byte swizzle (matches sw128_kmajor_desc).  Out-of-range boxes read zeros.
+cudaError_t make_tmap(CUtensorMap* tm, const void* ptr, int rows, int cols, int ld, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return cudaErrorNotSupported;
+  if (((uintptr_t)ptr & 15) || (ld * 2) % 16 || rows < 1 || cols < BK) return cudaErrorInvalidValue;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BN, int STAGES>
+constexpr size_t smem_bytes() {
+  return (size_t)STAGES * Cfg<BN>::STAGE_BYTES + 1024 + 256;
+}
+
+template <int BN, int STAGES, bool SWAP, int EPI>
+cudaError_t set_attr() {
+  static_assert(smem_bytes<BN, STAGES>() <= 227 * 1024, "shared memory");
+  return cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, SWAP, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<BN, STAGES>());
+}
+
+template <int BN, int STAGES, bool SWAP, int EPI>
+cudaError_t launch_kernel(const TcParams& p, int grid, cudaStream_t st) {
+  tc_gemm_kernel<BN, STAGES, SWAP, EPI><<<grid, kThreads, smem_bytes<BN, STAGES>(), st>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Opt every instantiation into its shared-memory size once, outside any stream capture (fpd_model_create).
+cudaError_t tc_init_attributes() {
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = set_attr<16, 6, true, EPI_STORE>();
+  if (e == cudaSuccess) e = set_attr<32, 5, true, EPI_STORE>();
+  if (e == cudaSuccess) e = set_attr<64, 4, true, EPI_STORE>();
+  if (e == cudaSuccess) e = set_attr<128, 6, false, EPI_STORE>();
+  if (e == cudaSuccess) e = set_attr<256, 4, false, EPI_STORE>();
+  if (e == cudaSuccess) e = set_attr<16, 6, true, EPI_ARGMAX>();
+  if (e == cudaSuccess) e = set_attr<32, 5, true, EPI_ARGMAX>();
+  if (e == cudaSuccess) e = set_attr<64, 4, true, EPI_ARGMAX>();
+  return e;
+}
+
+TcPlan tc_plan_gemm(int M, int N, int K, int num_sms) {
+  TcPlan pl{};
+  const int nkb = K / BK;
+  int ctas_per_sm;
+  if (M <= 64) {
+    pl.swap = true;
+    pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    pl.pt = ceil_div(N, BM);
+    pl.qt = ceil_div(M, pl.bn);
+    ctas_per_sm = 2;
+  } else {
+    pl.swap = false;
+    pl.bn = N >= 1024 ? 256 : 128;
+    pl.pt = ceil_div(M, BM);
+    pl.qt = ceil_div(N, pl.bn);
+    ctas_per_sm = 1;
+  }
+  const int tiles = pl.pt * pl.qt;
+  const int slots = num_sms * ctas_per_sm;
+  int splits = 1;
+  if (tiles < slots) splits = std::max(1, std::min(slots / tiles, nkb / 4));
+  const int kb_per = ceil_div(nkb, splits);
+  pl.k_split = kb_per * BK;
+  pl.splits = ceil_div(nkb, kb_per);
+  pl.grid = std::min(tiles * pl.splits, slots);
+  return pl;
+}
+
+TcPlan tc_plan_force(int M, int N, int K, int num_sms, int placement) {
+  TcPlan pl = tc_plan_gemm(M, N, K, num_sms);
+  if (placement < 0 || (placement == 1) == pl.swap) return pl;
+  const int nkb = K / BK;
+  pl.swap = placement == 1;
+  if (pl.swap) {
+    pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    pl.pt = ceil_div(N, BM);
+    pl.qt = ceil_div(M, pl.bn);
+  } else {
+    pl.bn = N >= 1024 ? 256 : 128;
+    pl.pt = ceil_div(M, BM);
+    pl.qt = ceil_div(N, pl.bn);
+  }
+  const int slots = num_sms * (pl.swap ? 2 : 1);
+  const int tiles = pl.pt * pl.qt;
+  int splits = 1;
+  if (tiles < slots) splits = std::max(1, std::min(slots / tiles, nkb / 4));
+  const int kb_per = ceil_div(nkb, splits);
+  pl.k_split = kb_per * BK;
+  pl.splits = ceil_div(nkb, kb_per);
+  pl.grid = std::min(tiles * pl.splits, slots);
+  return pl;
+}
+
+namespace {
+__global__ void sum_splits_kernel(float* __restrict__ out, const float* __restrict__ part, int splits, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    float a = 0.f;
+    for (int s = 0; s < splits; s++) a += part[s * n + i];
+    out[i] = a;
+  }
+}
+}  // namespace
+
+cudaError_t launch_sum_splits(float* out, const float* part, int splits, size_t n, cudaStream_t st) {
+  sum_splits_kernel<<<(int)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(out, part, splits, n);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(const GemmArgs& g, const TcPlan& pl, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  if (g.K % BK || g.seg_k % BK || g.k_split != pl.k_split) return cudaErrorInvalidValue;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  const int x_box = pl.swap ? pl.bn : BM, w_box = pl.swap ? BM : pl.bn;
+  p.n_seg = g.K / g.seg_k;
+  if (p.n_seg < 1 || p.n_seg > 8) return cudaErrorInvalidValue;
+  for (int s = 0; s < p.n_seg; s++) {
+    cudaError_t e = make_tmap(&p.tm_x[s], g.a[s], g.M, g.seg_k, g.lda, x_box);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = make_tmap(&p.tm_w, g.b, g.N, g.K, g.ldb, w_box);
+  if (e != cudaSuccess) return e;
+  p.seg_k = g.seg_k;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.c = g.c;
+  p.ldc = g.ldc;
+  p.c_split_stride = g.c_split_stride;
+  p.pt = pl.pt;
+  p.qt = pl.qt;
+  p.splits = pl.splits;
+  p.k_split = pl.k_split;
+  if (pl.swap) {
+    if (pl.bn == 16) return launch_kernel<16, 6, true, EPI_STORE>(p, pl.grid, st);
+    if (pl.bn == 32) return launch_kernel<32, 5, true, EPI_STORE>(p, pl.grid, st);
+    return launch_kernel<64, 4, true, EPI_STORE>(p, pl.grid, st);
+  }
+  if (pl.bn == 128) return launch_kernel<128, 6, false, EPI_STORE>(p, pl.grid, st);
+  return launch_kernel<256, 4, false, EPI_STORE>(p, pl.grid, st);
+}
+
+int tc_lm_row_tile(int n_rows) { return n_rows <= 16 ? 16 : (n_rows <= 32 ? 32 : 64); }
+
+cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows, const bf16* W, int d, int V,
+                             const int4* items, const int* n_items, int max_items, unsigned long long* packed,
+                             const int* rows_sorted, float* logits, int num_sms, cudaStream_t st) {
+  if (d % BK) return cudaErrorInvalidValue;
+  const int bn = lp.rt;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  cudaError_t e = make_tmap(&p.tm_x[0], z_sorted, n_rows, d, d, bn);
+  if (e != cudaSuccess) return e;
+  e = make_tmap(&p.tm_w, W, V, d, d, BM);
+  if (e != cudaSuccess) return e;
+  p.n_seg = 1;
+  p.seg_k = d;
+  p.M = n_rows;
+  p.N = V;
+  p.K = d;
+  p.items = items;
+  p.n_items = n_items;
+  for (int q = 0; q < lp.n_range; q++) p.hi_tab[q] = lp.range_hi[q];
+  p.packed = packed;
+  p.rows_sorted = rows_sorted;
+  p.logits = logits;
+  p.V = V;
+  const int grid = std::max(1, std::min(max_items, 2 * num_sms));
+  if (bn == 16) return launch_kernel<16, 6, true, EPI_ARGMAX>(p, grid, st);
+  if (bn == 32) return launch_kernel<32, 5, true, EPI_ARGMAX>(p, grid, st);
+  return launch_kernel<64, 4, true, EPI_ARGMAX>(p, grid, st);
+}
+
+}  // namespace fpd

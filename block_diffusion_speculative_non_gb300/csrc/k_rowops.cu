@@ -1,0 +1,296 @@
+// k_rowops.cu — row-wise kernels of the drafter pass: embedding gather, RMSNorm, the q/k RMSNorm + RoPE
+// epilogue of the QKV projection, the context K/V epilogue, residual add and SwiGLU.
+//
+// Method: VFlash paper (zh) §2.1-§2.2 (one anchor + L-1 mask tokens through a bidirectional layer stack
+// conditioned on per-layer context K/V); layer form = pre-norm transformer layer with per-head q/k RMSNorm
+// and rotate-half RoPE, SwiGLU MLP (the reading of the five-layer non-causal drafter of the VFlash blog,
+// "Key claims").  All of these are HBM/latency-bound (a few MB per call): one thread block or one warp per
+// row or head, 16-byte vector loads, fp32 arithmetic, bf16 stores at the storage points.
+#include "fpd_kernels.cuh"
+
+namespace fpd {
+
+__device__ int32_t g_device_check = 0;
+
+// ---- a3: x[b*L + j] = E[anchor[b]] (j == 0) or E[mask_id] (j >= 1) ---------------------------------------------
+__global__ void embed_kernel(bf16* __restrict__ x, const bf16* __restrict__ embed, const int32_t* __restrict__ anchor,
+                             int32_t mask_id, int L, int d, int V) {
+  const int r = blockIdx.x, b = r / L, j = r % L;
+  int id = j == 0 ? anchor[b] : mask_id;
+  uint4* dst = reinterpret_cast<uint4*>(x + (size_t)r * d);
+  if (id < 0 || id >= V) {
+    if (threadIdx.x == 0) record_check(kCheckBadToken);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(embed + (size_t)id * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+}
+
+cudaError_t launch_embed(bf16* x, const bf16* embed, const int32_t* anchor, int32_t mask_id, int B, int L, int d,
+                         int V, cudaStream_t st) {
+  embed_kernel<<<B * L, 128, 0, st>>>(x, embed, anchor, mask_id, L, d, V);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ---- block reduction helper ------------------------------------------------------------------------------------
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = l < nw ? red[l] : 0.f;
+  return warp_sum(t);
+}
+
+// ---- RMSNorm of bf16 rows -> bf16 rows ---------------------------------------------------------------------------
+// out[r] = bf16(x / sqrt(mean(x^2) + eps) * g).  skip_L > 0 maps output row r to input row
+// (r / (skip_L-1)) * skip_L + r % (skip_L-1) + 1, i.e. it drops the anchor row of every block (final norm).
+__global__ void rmsnorm_kernel(bf16* __restrict__ out, const bf16* __restrict__ in, const bf16* __restrict__ g, int d,
+                               float eps, int skip_L) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const int rin = skip_L > 0 ? (r / (skip_L - 1)) * skip_L + r % (skip_L - 1) + 1 : r;
+  const uint4* src = reinterpret_cast<const uint4*>(in + (size_t)rin * d);
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+    uint4 u = src[i];
+    const bf16* e = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      float f = __bfloat162float(e[k]);
+      ss += f * f;
+    }
+  }
+  const float inv = rsqrtf(block_sum(ss, red) / (float)d + eps);
+  const uint4* gs = reinterpret_cast<const uint4*>(g);
+  uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+    uint4 u = src[i], gu = gs[i], o;
+    const bf16* e = reinterpret_cast<const bf16*>(&u);
+    const bf16* ge = reinterpret_cast<const bf16*>(&gu);
+    bf16* oe = reinterpret_cast<bf16*>(&o);
+#pragma unroll
+    for (int k = 0; k < 8; k++) oe[k] = __float2bfloat16_rn(__bfloat162float(e[k]) * inv * __bfloat162float(ge[k]));
+    dst[i] = o;
+  }
+}
+
+cudaError_t launch_rmsnorm(bf16* out, const bf16* in, const bf16* g, int rows, int d, float eps, int skip_L,
+                           cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  rmsnorm_kernel<<<rows, 256, 0, st>>>(out, in, g, d, eps, skip_L);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ---- RMSNorm of fp32 split-K partial sums -> bf16 (fused context) -------------------------------------------------
+__global__ void rmsnorm_partials_kernel(bf16* __restrict__ out, const float* __restrict__ part, int nsplit,
+                                        size_t split_stride, const bf16* __restrict__ g, int d, float eps) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = 0.f;
+    for (int s = 0; s < nsplit; s++) v += part[s * split_stride + (size_t)r * d + i];
+    ss += v * v;
+  }
+  const float inv = rsqrtf(block_sum(ss, red) / (float)d + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = 0.f;
+    for (int s = 0; s < nsplit; s++) v += part[s * split_stride + (size_t)r * d + i];
+    out[(size_t)r * d + i] = __float2bfloat16_rn(v * inv * __bfloat162float(g[i]));
+  }
+}
+
+cudaError_t launch_rmsnorm_partials(bf16* out, const float* part, int nsplit, size_t split_stride, const bf16* g,
+                                    int rows, int d, float eps, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  rmsnorm_partials_kernel<<<rows, 256, 0, st>>>(out, part, nsplit, split_stride, g, d, eps);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ---- per-head RMSNorm + rotate-half RoPE on a warp's head ----------------------------------------------------------
+// Lane `lane` holds elements e = lane + 32k (k < H/32) of one head (H = head_dim).  The RoPE pair of element i
+// (< H/2) is i + H/2, held by the same lane.  rope[pos * H/2 + i] = (cos, sin) of angle pos * theta^(-2i/H).
+template <int H>
+__device__ __forceinline__ void head_norm_rope(float (&v)[H / 32], const bf16* __restrict__ gain, float eps,
+                                               const float2* __restrict__ rope_row, bool do_norm, bool do_rope) {
+  constexpr int NV = H / 32;
+  const int lane = threadIdx.x & 31;
+  if (do_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; k++) ss += v[k] * v[k];
+    const float inv = rsqrtf(warp_sum(ss) / (float)H + eps);
+#pragma unroll
+    for (int k = 0; k < NV; k++) v[k] = v[k] * inv * __bfloat162float(gain[lane + 32 * k]);
+  }
+  if (do_rope) {
+#pragma unroll
+    for (int k = 0; k < NV / 2; k++) {
+      const float2 cs = rope_row[lane + 32 * k];
+      const float x1 = v[k], x2 = v[k + NV / 2];
+      v[k] = x1 * cs.x - x2 * cs.y;
+      v[k + NV / 2] = x2 * cs.x + x1 * cs.y;
+    }
+  }
+}
+
+// ---- a4 epilogue: sum split-K partials of [q | k | v], q/k RMSNorm + RoPE at pos = ctx_len[b] + j ------------------
+// grid (B*L, Hq + 2 Hkv), one warp per (row, head).
+template <int H>
+__global__ void qkv_post_kernel(bf16* __restrict__ q_out, bf16* __restrict__ kblk, bf16* __restrict__ vblk,
+                                const float* __restrict__ part, int nsplit, size_t split_stride,
+                                const bf16* __restrict__ q_norm, const bf16* __restrict__ k_norm,
+                                const float2* __restrict__ rope, const int32_t* __restrict__ ctx_len, int t_cap,
+                                int L, int nq, int nkv, float eps) {
+  constexpr int NV = H / 32;
+  const int r = blockIdx.x, hd = blockIdx.y, lane = threadIdx.x;
+  const int b = r / L, j = r % L;
+  const int ncol = (nq + 2 * nkv) * H;
+  float v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; k++) {
+    float a = 0.f;
+    for (int s = 0; s < nsplit; s++) a += part[s * split_stride + (size_t)r * ncol + hd * H + lane + 32 * k];
+    v[k] = a;
+  }
+  int cl = ctx_len[b];
+  cl = cl < 0 ? 0 : (cl > t_cap ? t_cap : cl);
+  const float2* rope_row = rope + (size_t)(cl + j) * (H / 2);
+  bf16* dst;
+  if (hd < nq) {
+    head_norm_rope<H>(v, q_norm, eps, rope_row, true, true);
+    dst = q_out + ((size_t)r * nq + hd) * H;
+  } else if (hd < nq + nkv) {
+    head_norm_rope<H>(v, k_norm, eps, rope_row, true, true);
+    dst = kblk + (((size_t)b * nkv + (hd - nq)) * L + j) * H;
+  } else {
+    dst = vblk + (((size_t)b * nkv + (hd - nq - nkv)) * L + j) * H;
+  }
+#pragma unroll
+  for (int k = 0; k < NV; k++) dst[lane + 32 * k] = __float2bfloat16_rn(v[k]);
+}
+
+cudaError_t launch_qkv_post(bf16* q, bf16* kblk, bf16* vblk, const float* part, int nsplit, size_t split_stride,
+                            const bf16* q_norm, const bf16* k_norm, const float2* rope, const int32_t* ctx_len,
+                            int t_cap, int B, int L, int nq, int nkv, int h, float eps, cudaStream_t st) {
+  dim3 grid(B * L, nq + 2 * nkv);
+  if (h == 128)
+    qkv_post_kernel<128><<<grid, 32, 0, st>>>(q, kblk, vblk, part, nsplit, split_stride, q_norm, k_norm, rope,
+                                              ctx_len, t_cap, L, nq, nkv, eps);
+  else
+    qkv_post_kernel<64><<<grid, 32, 0, st>>>(q, kblk, vblk, part, nsplit, split_stride, q_norm, k_norm, rope,
+                                             ctx_len, t_cap, L, nq, nkv, eps);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ---- a2 epilogue: context K (k-norm + RoPE at its context position) and V into the KV store -----------------------
+// part: [rows, 2*nkv*H] fp32 = ctx . [Wk; Wv]^T for `rows` packed rows starting at global row row0.
+// Store layout [layer][b][K|V][g][t_cap][H].
+template <int H>
+__global__ void kv_post_kernel(bf16* __restrict__ store, const float* __restrict__ part, int nsplit,
+                               size_t split_stride, const bf16* __restrict__ k_norm, const float2* __restrict__ rope,
+                               const int32_t* __restrict__ row_off, const int32_t* __restrict__ pos_start, int batch,
+                               int layer, int t_cap, int row0, int nkv, float eps) {
+  constexpr int NV = H / 32;
+  const int r = blockIdx.x, hd = blockIdx.y, lane = threadIdx.x;
+  const int grow = row0 + r;
+  int lo = 0, hi = batch;                       // request b with row_off[b] <= grow < row_off[b+1]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (row_off[mid] <= grow) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int pos = (pos_start ? pos_start[b] : 0) + grow - row_off[b];
+  if (pos < 0 || pos >= t_cap) return;          // caller contract violated: skip the store
+  const int ncol = 2 * nkv * H;
+  float v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; k++) {
+    float a = 0.f;
+    for (int s = 0; s < nsplit; s++) a += part[s * split_stride + (size_t)r * ncol + hd * H + lane + 32 * k];
+    v[k] = a;
+  }
+  const int is_v = hd >= nkv, g = is_v ? hd - nkv : hd;
+  if (!is_v) head_norm_rope<H>(v, k_norm, eps, rope + (size_t)pos * (H / 2), true, true);
+  bf16* dst = store + (((((size_t)layer * batch + b) * 2 + is_v) * nkv + g) * (size_t)t_cap + pos) * H;
+#pragma unroll
+  for (int k = 0; k < NV; k++) dst[lane + 32 * k] = __float2bfloat16_rn(v[k]);
+}
+
+cudaError_t launch_kv_post(bf16* store, const float* part, int nsplit, size_t split_stride, const bf16* k_norm,
+                           const float2* rope, const int32_t* row_off, const int32_t* pos_start, int batch, int layer,
+                           int t_cap, int row0, int rows, int nkv, int h, float eps, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  dim3 grid(rows, 2 * nkv);
+  if (h == 128)
+    kv_post_kernel<128><<<grid, 32, 0, st>>>(store, part, nsplit, split_stride, k_norm, rope, row_off, pos_start,
+                                             batch, layer, t_cap, row0, nkv, eps);
+  else
+    kv_post_kernel<64><<<grid, 32, 0, st>>>(store, part, nsplit, split_stride, k_norm, rope, row_off, pos_start,
+                                            batch, layer, t_cap, row0, nkv, eps);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ---- a6/a7 epilogue: x = bf16(x + sum_s part[s]) ------------------------------------------------------------------
+__global__ void residual_add_kernel(bf16* __restrict__ x, const float* __restrict__ part, int nsplit,
+                                    size_t split_stride, size_t n8) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    uint4 u = reinterpret_cast<uint4*>(x)[i];
+    bf16* e = reinterpret_cast<bf16*>(&u);
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) acc[k] = 0.f;
+    for (int s = 0; s < nsplit; s++) {
+      const float4* p = reinterpret_cast<const float4*>(part + s * split_stride) + 2 * i;
+      float4 a = p[0], c = p[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += c.x; acc[5] += c.y; acc[6] += c.z; acc[7] += c.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; k++) e[k] = __float2bfloat16_rn(__bfloat162float(e[k]) + acc[k]);
+    reinterpret_cast<uint4*>(x)[i] = u;
+  }
+}
+
+cudaError_t launch_residual_add(bf16* x, const float* part, int nsplit, size_t split_stride, size_t n,
+                                cudaStream_t st) {
+  size_t n8 = n / 8;
+  int grid = (int)std::min<size_t>((n8 + 255) / 256, 4096);
+  residual_add_kernel<<<grid, 256, 0, st>>>(x, part, nsplit, split_stride, n8);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ---- a7 middle: hmid = bf16(silu(g) * u), g/u = columns f and F+f of the gate/up projection ------------------------
+__global__ void swiglu_kernel(bf16* __restrict__ hmid, const float* __restrict__ part, int nsplit, size_t split_stride,
+                              int F, size_t total) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / F, f = i % F;
+    float g = 0.f, u = 0.f;
+    for (int s = 0; s < nsplit; s++) {
+      g += part[s * split_stride + r * 2 * F + f];
+      u += part[s * split_stride + r * 2 * F + F + f];
+    }
+    const float sg = g / (1.0f + expf(-g));
+    hmid[i] = __float2bfloat16_rn(sg * u);
+  }
+}
+
+cudaError_t launch_swiglu(bf16* hmid, const float* part, int nsplit, size_t split_stride, int rows, int F,
+                          cudaStream_t st) {
+  size_t total = (size_t)rows * F;
+  int grid = (int)std::min<size_t>((total + 255) / 256, 8192);
+  swiglu_kernel<<<grid, 256, 0, st>>>(hmid, part, nsplit, split_stride, F, total);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace fpd

@@ -1,0 +1,75 @@
+"""Helpers shared by the GPU parity tests: transfers and the comparison rules.
+
+Tolerances: hidden states, K/V and logits agree with the oracle within a max relative error of 2e-2 per row
+(max_i |gpu_i - ref_i| / max_i |ref_i|; bf16 storage, fp32 accumulation on the GPU).  Token ids are bit-exact
+except where the oracle's top-2 fp32 logit margin is below 1e-2.  Acceptance lengths and committed tokens are
+bit-exact given the ids.
+"""
+import numpy as np
+import torch
+
+import synth
+
+REL_TOL = 2e-2
+MARGIN_EXEMPT = 1e-2
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def f64(bits: np.ndarray) -> np.ndarray:
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def dev_i32(a, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def row_rel_err(gpu: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """Per-row max relative error of two [rows, n] float arrays (rows of all-zero reference count as 0)."""
+    gpu = gpu.reshape(gpu.shape[0], -1).astype(np.float64)
+    ref = ref.reshape(ref.shape[0], -1).astype(np.float64)
+    den = np.max(np.abs(ref), axis=1)
+    num = np.max(np.abs(gpu - ref), axis=1)
+    out = np.zeros_like(den)
+    nz = den > 0
+    out[nz] = num[nz] / den[nz]
+    out[~nz] = num[~nz]
+    return out
+
+
+def assert_rows_close(gpu_bits: np.ndarray, ref_bits: np.ndarray, what: str, tol: float = REL_TOL):
+    e = row_rel_err(f64(gpu_bits), f64(ref_bits))
+    assert e.max() <= tol, f"{what}: max row rel err {e.max():.3e} at row {int(e.argmax())}"
+    return e.max()
+
+
+def assert_tokens(gpu: np.ndarray, ref: np.ndarray, margin: np.ndarray, what: str = "tokens"):
+    gpu = np.asarray(gpu).reshape(-1)
+    ref = np.asarray(ref).reshape(-1)
+    bad = (gpu != ref) & (np.asarray(margin).reshape(-1) >= MARGIN_EXEMPT)
+    assert not bad.any(), f"{what}: {int(bad.sum())} ids differ at non-exempt positions {np.nonzero(bad)[0][:10]}"
+    return int((gpu != ref).sum())
+
+
+def assert_logits(gpu: np.ndarray, ref: np.ndarray, what: str = "logits", few: int = 64):
+    """gpu [rows, V] fp32 (only legal columns written), ref [rows, V] f64 with NaN on illegal columns.
+    A row is scaled by its own largest |logit| when it has at least `few` legal ids; a row with fewer legal
+    ids (a delimiter slot admits one id, whose logit may be near zero) is scaled by the largest |logit| of
+    the whole block instead, since a one-column row's own maximum is the value being checked."""
+    legal = ~np.isnan(ref)
+    block_scale = np.nanmax(np.abs(ref))
+    worst, where = 0.0, None
+    for r in range(ref.shape[0]):
+        cols = legal[r]
+        n = int(cols.sum())
+        if n == 0:
+            continue
+        g, t = gpu[r, cols].astype(np.float64), ref[r, cols]
+        den = np.max(np.abs(t)) if n >= few else block_scale
+        e = np.max(np.abs(g - t)) / den
+        if e > worst:
+            worst, where = e, (r, n, float(np.max(np.abs(g - t))), float(den))
+    assert worst <= REL_TOL, f"{what}: max row rel err {worst:.3e} (row, legal ids, abs err, scale) = {where}"
+    return worst
