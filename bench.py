@@ -90,6 +90,22 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(elapsed_ms, world, device):
+    """The timed region's length as the slowest rank saw it (all ranks get the same number)."""
+    if world == 1:
+        return float(elapsed_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, tokens_per_step, steps, elapsed_ms):
+    """Whole-job draft tokens/s: every replica drafts `tokens_per_step` per step; time = slowest rank."""
+    return world * tokens_per_step * steps / (elapsed_ms / 1e3)
+
+
 def run_oracle_block(om, wl, kv, target, layout):
     import oracle
     t0 = time.perf_counter()
@@ -129,7 +145,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
+    if world > 1 and args.impl == "ours":
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         if torch.cuda.is_available():
@@ -281,13 +297,9 @@ def main():
     elapsed_ms = t0e.elapsed_time(t1e)
     lm_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_lm]))
     assert pkg.fpd_device_status(stream) == 0, "device-side check failed"
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = world * draft_tokens_per_step * args.steps / (elapsed_ms / 1e3)
+    value = replica_throughput(world, draft_tokens_per_step, args.steps, elapsed_ms)
 
     # ---- end to end through the C ABI with host buffers: H2D of the step's inputs, D2H of its results --------
     a_h = torch.from_numpy(wl.anchor.copy()).pin_memory()

@@ -99,6 +99,8 @@ def _ptr(t) -> int | None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError("device tensors passed to libfpd must be contiguous (row-major)")
     return t.data_ptr()
 
 

@@ -80,7 +80,7 @@ struct DraftWs {
   float* o_part;
   float2* ml;
   int att_splits, att_chunk;
-  TcPlan p_qkv, p_o, p_gu, p_down;
+  TcPlan p_qkv, p_o, p_sw, p_down;
 };
 
 DraftWs carve_draft(const Model& m, Carver& c, int B, int L, int t_cap) {
@@ -90,12 +90,11 @@ DraftWs carve_draft(const Model& m, Carver& c, int B, int L, int t_cap) {
   const int nqkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim, nqh = d.n_q_heads * d.head_dim;
   w.p_qkv = tc_plan_gemm(M, nqkv, d.d_model, m.num_sms);
   w.p_o = tc_plan_gemm(M, d.d_model, nqh, m.num_sms);
-  w.p_gu = tc_plan_gemm(M, 2 * d.d_ff, d.d_model, m.num_sms);
+  w.p_sw = tc_plan_swiglu(M, d.d_ff, d.d_model, m.num_sms);
   w.p_down = tc_plan_gemm(M, d.d_model, d.d_ff, m.num_sms);
   size_t part = 0;
   part = std::max(part, (size_t)w.p_qkv.splits * M * nqkv);
   part = std::max(part, (size_t)w.p_o.splits * M * d.d_model);
-  part = std::max(part, (size_t)w.p_gu.splits * M * 2 * d.d_ff);
   part = std::max(part, (size_t)w.p_down.splits * M * d.d_model);
   w.xn = c.take<bf16>((size_t)M * d.d_model);
   w.part = c.take<float>(part);
@@ -394,7 +393,9 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
   const int M = batch * L, dm = d.d_model, h = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.d_ff;
   const int nqkv = (nq + 2 * nkv) * h;
   bf16* x = (bf16*)hidden_out;
-  FPD_CUDA(launch_embed(x, (const bf16*)m->w.embed, anchor, mask_id, batch, L, dm, d.vocab, st), "embed");
+  FPD_CUDA(launch_embed_norm(x, w.xn, (const bf16*)m->w.embed, anchor, mask_id, (const bf16*)m->w.attn_norm[0], batch,
+                             L, dm, d.vocab, d.rms_eps, st),
+           "embed + attention norm");
   auto gemm = [&](const bf16* A, int K, const void* W, int N, const TcPlan& pl) {
     GemmArgs g{};
     g.a[0] = A;
@@ -412,7 +413,7 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
     return launch_tc_gemm(g, pl, st);
   };
   for (int l = 0; l < d.n_layers; l++) {
-    FPD_CUDA(launch_rmsnorm(w.xn, x, (const bf16*)m->w.attn_norm[l], M, dm, d.rms_eps, 0, st), "attention norm");
+    // xn holds RMSNorm_attn(x) here (from the embedding or the previous layer's last residual kernel)
     FPD_CUDA(gemm(w.xn, dm, m->w.wqkv[l], nqkv, w.p_qkv), "QKV GEMM");
     FPD_CUDA(launch_qkv_post(w.q, w.kblk, w.vblk, w.part, w.p_qkv.splits, (size_t)M * nqkv,
                              (const bf16*)m->w.q_norm[l], (const bf16*)m->w.k_norm[l], m->rope, ctx_len, t_cap, batch,
@@ -438,12 +439,14 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
     a.chunk = w.att_chunk;
     FPD_CUDA(launch_attention(a, w.o, st), "attention");
     FPD_CUDA(gemm(w.o, nq * h, m->w.wo[l], dm, w.p_o), "O GEMM");
-    FPD_CUDA(launch_residual_add(x, w.part, w.p_o.splits, (size_t)M * dm, (size_t)M * dm, st), "residual");
-    FPD_CUDA(launch_rmsnorm(w.xn, x, (const bf16*)m->w.mlp_norm[l], M, dm, d.rms_eps, 0, st), "MLP norm");
-    FPD_CUDA(gemm(w.xn, dm, m->w.w_gate_up[l], 2 * F, w.p_gu), "gate/up GEMM");
-    FPD_CUDA(launch_swiglu(w.hmid, w.part, w.p_gu.splits, (size_t)M * 2 * F, M, F, st), "SwiGLU");
+    FPD_CUDA(launch_residual_norm(x, w.xn, w.part, w.p_o.splits, (size_t)M * dm, (const bf16*)m->w.mlp_norm[l], M, dm,
+                                  d.rms_eps, st),
+             "residual + MLP norm");
+    FPD_CUDA(launch_tc_swiglu(w.xn, M, dm, (const bf16*)m->w.w_gate_up[l], F, w.hmid, w.p_sw, st), "gate/up + SwiGLU");
     FPD_CUDA(gemm(w.hmid, F, m->w.w_down[l], dm, w.p_down), "down GEMM");
-    FPD_CUDA(launch_residual_add(x, w.part, w.p_down.splits, (size_t)M * dm, (size_t)M * dm, st), "residual");
+    const bf16* next_norm = l + 1 < d.n_layers ? (const bf16*)m->w.attn_norm[l + 1] : nullptr;
+    FPD_CUDA(launch_residual_norm(x, w.xn, w.part, w.p_down.splits, (size_t)M * dm, next_norm, M, dm, d.rms_eps, st),
+             "residual + next attention norm");
     if (layer_hidden)
       FPD_CUDA(cudaMemcpyAsync((bf16*)layer_hidden + (size_t)l * M * dm, x, (size_t)M * dm * sizeof(bf16),
                                cudaMemcpyDeviceToDevice, st),

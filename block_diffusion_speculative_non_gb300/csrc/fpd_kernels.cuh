@@ -33,15 +33,15 @@ struct TcPlan {
 TcPlan tc_plan_gemm(int M, int N, int K, int num_sms);
 TcPlan tc_plan_force(int M, int N, int K, int num_sms, int placement);   // placement 0: tokens on 128 rows, 1: weights
 cudaError_t launch_tc_gemm(const GemmArgs& g, const TcPlan& plan, cudaStream_t st);
+TcPlan tc_plan_swiglu(int M, int F, int K, int num_sms);
+// hmid[M][F] = bf16(silu(x . Wg^T) * (x . Wu^T)) with W = [Wg; Wu] ([2F, K]), one tcgen05 pass
+cudaError_t launch_tc_swiglu(const bf16* x, int M, int K, const bf16* w_gate_up, int F, bf16* hmid, const TcPlan& pl,
+                             cudaStream_t st);
 cudaError_t tc_init_attributes();     // once per process, before any stream capture
 cudaError_t attn_init_attributes();
 cudaError_t launch_sum_splits(float* out, const float* part, int splits, size_t n, cudaStream_t st);
 
 // ---- row ops -------------------------------------------------------------------------------------------------
-cudaError_t launch_embed(bf16* x, const bf16* embed, const int32_t* anchor, int32_t mask_id, int B, int L, int d,
-                         int V, cudaStream_t st);
-cudaError_t launch_rmsnorm(bf16* out, const bf16* in, const bf16* g, int rows, int d, float eps, int skip_L,
-                           cudaStream_t st);
 cudaError_t launch_rmsnorm_partials(bf16* out, const float* part, int nsplit, size_t split_stride, const bf16* g,
                                     int rows, int d, float eps, cudaStream_t st);
 cudaError_t launch_qkv_post(bf16* q, bf16* kblk, bf16* vblk, const float* part, int nsplit, size_t split_stride,
@@ -50,10 +50,10 @@ cudaError_t launch_qkv_post(bf16* q, bf16* kblk, bf16* vblk, const float* part, 
 cudaError_t launch_kv_post(bf16* store, const float* part, int nsplit, size_t split_stride, const bf16* k_norm,
                            const float2* rope, const int32_t* row_off, const int32_t* pos_start, int batch, int layer,
                            int t_cap, int row0, int rows, int nkv, int h, float eps, cudaStream_t st);
-cudaError_t launch_residual_add(bf16* x, const float* part, int nsplit, size_t split_stride, size_t n,
-                                cudaStream_t st);
-cudaError_t launch_swiglu(bf16* hmid, const float* part, int nsplit, size_t split_stride, int rows, int F,
-                          cudaStream_t st);
+cudaError_t launch_residual_norm(bf16* x, bf16* xn, const float* part, int nsplit, size_t split_stride, const bf16* g,
+                                 int rows, int d, float eps, cudaStream_t st);
+cudaError_t launch_embed_norm(bf16* x, bf16* xn, const bf16* embed, const int32_t* anchor, int32_t mask_id,
+                              const bf16* g, int B, int L, int d, int V, float eps, cudaStream_t st);
 
 // ---- attention ---------------------------------------------------------------------------------------------
 struct AttnArgs {

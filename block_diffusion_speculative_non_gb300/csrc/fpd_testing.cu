@@ -61,4 +61,17 @@ fpd_status fpd_test_gemm(int impl, int placement, int M, int N, int K, const voi
   return launch_sum_splits(C, (const float*)workspace, pl.splits, (size_t)M * N, st) == cudaSuccess ? FPD_OK : FPD_ERR_CUDA;
 }
 
+fpd_status fpd_test_swiglu(int M, int F, int K, const void* X, const void* W, void* hmid, void* stream) {
+  if (M < 1 || F < 1 || K < 64 || K % 64) return FPD_ERR_SHAPE;
+  if (!X || !W || !hmid) return FPD_ERR_INVALID_ARG;
+  const int sms = current_sms();
+  if (!sms) return FPD_ERR_CUDA;
+  static cudaError_t init_err = tc_init_attributes();
+  if (init_err != cudaSuccess) return FPD_ERR_CUDA;
+  const TcPlan pl = tc_plan_swiglu(M, F, K, sms);
+  return launch_tc_swiglu((const bf16*)X, M, K, (const bf16*)W, F, (bf16*)hmid, pl, (cudaStream_t)stream) == cudaSuccess
+             ? FPD_OK
+             : FPD_ERR_CUDA;
+}
+
 }  // extern "C"

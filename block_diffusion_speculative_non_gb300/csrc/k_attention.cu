@@ -7,29 +7,76 @@
 //
 // Work split: (query tile of 64 rows of one kv-head group) x (request, kv head) x (KV split).  The rows of a
 // tile are the L positions x H_q/H_kv q heads that share one kv head, so every K/V row loaded is used by the
-// whole group.  Each CTA runs an online softmax over its key range and writes an unnormalised partial
-// (o, m, l); a merge kernel combines the splits in fixed order (deterministic, no atomics).
+// whole group.  Four warps each own 16 query rows; Q stays in registers as mma fragments; K/V tiles of 64
+// keys are staged in shared memory with cp.async (double buffered, 16-byte chunks XOR-swizzled so ldmatrix
+// is conflict free); S = Q K^T and O += P V run on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+// accumulate; P is rounded to bf16 as the second product's operand); the online softmax works in base 2 on
+// the fp32 accumulators.  With one split the CTA writes the normalised bf16 output; with several it writes
+// an unnormalised partial (o, m, l) and a merge kernel combines the splits in fixed order (deterministic,
+// no atomics).
 #include "fpd_kernels.cuh"
 
 namespace fpd {
 
 namespace {
-constexpr int QT = 64, KT = 64;
+constexpr int QT = 64, KT = 64, NWARP = 4;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;   // 0 source bytes: the 16 destination bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Tile of rows x H bf16 in shared memory; 16-byte chunk c of row r lives at chunk c ^ (r & 7).
+template <int H>
+__device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
+  return base + (uint32_t)(r * H * 2 + ((c ^ (r & 7)) << 4));
+}
 
 template <int H>
-struct AttnSmem {
-  float q[QT][H];
-  float k[KT][H + 1];
-  float v[KT][H];
-  float s[QT][KT + 1];
-  float corr[QT];
+struct Smem {
+  bf16 q[QT * H];
+  bf16 k[2][KT * H];
+  bf16 v[2][KT * H];
 };
 
 template <int H>
-__global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  AttnSmem<H>& sm = *reinterpret_cast<AttnSmem<H>*>(smem_raw);
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(NWARP * 32) attn_mma_kernel(AttnArgs a, bf16* __restrict__ out) {
+  constexpr int CH = H / 8;     // 16-byte chunks per row
+  constexpr int NKS = H / 16;   // k-steps over the head dimension
+  constexpr int NOT = H / 8;    // 8-wide n-tiles of O
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem<H>& sm = *reinterpret_cast<Smem<H>*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qt = blockIdx.x, bg = blockIdx.y, split = blockIdx.z;
   const int b = bg / a.nkv, g = bg % a.nkv;
   const int grp = a.nq / a.nkv, nrows = a.L * grp;
@@ -37,114 +84,186 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
   T = T < 0 ? 0 : (T > a.t_cap ? a.t_cap : T);
   const int n_keys = T + a.L;
   const int k_begin = split * a.chunk, k_end = min(n_keys, k_begin + a.chunk);
-  const float scale = rsqrtf((float)H);
-
-  // query rows of this tile
-  for (int idx = tid; idx < QT * H; idx += blockDim.x) {
-    const int rr = idx / H, e = idx % H, qi = qt * QT + rr;
-    float v = 0.f;
-    if (qi < nrows) {
-      const int j = qi / grp, i = g * grp + qi % grp;
-      v = __bfloat162float(a.q[(((size_t)b * a.L + j) * a.nq + i) * H + e]) * scale;
-    }
-    sm.q[rr][e] = v;
-  }
-  const int orow = tid >> 2, oc0 = (tid & 3) * (H / 4);
-  float o[H / 4];
-#pragma unroll
-  for (int c = 0; c < H / 4; c++) o[c] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;   // valid in threads tid < QT (row tid)
+  const float sl2 = rsqrtf((float)H) * 1.4426950408889634f;   // 1/sqrt(h) * log2(e): softmax in base 2
 
   const bf16* kctx = a.store + ((((size_t)a.layer * a.batch + b) * 2 + 0) * a.nkv + g) * (size_t)a.t_cap * H;
   const bf16* vctx = a.store + ((((size_t)a.layer * a.batch + b) * 2 + 1) * a.nkv + g) * (size_t)a.t_cap * H;
-  const bf16* kb = a.kblk + ((size_t)b * a.nkv + g) * a.L * H;
-  const bf16* vb = a.vblk + ((size_t)b * a.nkv + g) * a.L * H;
+  const bf16* kbk = a.kblk + ((size_t)b * a.nkv + g) * a.L * H;
+  const bf16* vbk = a.vblk + ((size_t)b * a.nkv + g) * a.L * H;
 
-  for (int k0 = k_begin; k0 < k_end; k0 += KT) {
-    __syncthreads();
-    for (int idx = tid; idx < KT * H; idx += blockDim.x) {
-      const int kk = idx / H, e = idx % H, t = k0 + kk;
-      float kv = 0.f, vv = 0.f;
-      if (t < k_end) {
+  const uint32_t q_s = smem_addr(sm.q);
+  for (int idx = tid; idx < QT * CH; idx += NWARP * 32) {
+    const int r = idx / CH, c = idx % CH, qi = qt * QT + r;
+    const bool ok = qi < nrows;
+    const bf16* src = a.q;
+    if (ok) {
+      const int j = qi / grp, i = g * grp + qi % grp;
+      src = a.q + (((size_t)b * a.L + j) * a.nq + i) * H + c * 8;
+    }
+    cp_async16(swz<H>(q_s, r, c), src, ok);
+  }
+  cp_async_commit();
+
+  auto load_kv = [&](int buf, int k0) {
+    const uint32_t ks = smem_addr(sm.k[buf]), vs = smem_addr(sm.v[buf]);
+    for (int idx = tid; idx < KT * CH; idx += NWARP * 32) {
+      const int r = idx / CH, c = idx % CH, t = k0 + r;
+      const bool ok = t < k_end;
+      const bf16 *ksrc = kctx, *vsrc = vctx;
+      if (ok) {
         if (t < T) {
-          kv = __bfloat162float(kctx[(size_t)t * H + e]);
-          vv = __bfloat162float(vctx[(size_t)t * H + e]);
+          ksrc = kctx + (size_t)t * H + c * 8;
+          vsrc = vctx + (size_t)t * H + c * 8;
         } else {
-          kv = __bfloat162float(kb[(size_t)(t - T) * H + e]);
-          vv = __bfloat162float(vb[(size_t)(t - T) * H + e]);
+          ksrc = kbk + (size_t)(t - T) * H + c * 8;
+          vsrc = vbk + (size_t)(t - T) * H + c * 8;
         }
       }
-      sm.k[kk][e] = kv;
-      sm.v[kk][e] = vv;
+      cp_async16(swz<H>(ks, r, c), ksrc, ok);
+      cp_async16(swz<H>(vs, r, c), vsrc, ok);
     }
-    __syncthreads();
-    {
-      const int ty = tid >> 4, tx = tid & 15;
-      float acc[4][4] = {};
-      for (int e = 0; e < H; e++) {
-        float qa[4], kbv[4];
+    cp_async_commit();
+  };
+
+  const int n_tiles = k_end > k_begin ? (k_end - k_begin + KT - 1) / KT : 0;
+  if (n_tiles > 0) load_kv(0, k_begin);
+
+  float o[NOT][4];
 #pragma unroll
-        for (int i = 0; i < 4; i++) qa[i] = sm.q[ty * 4 + i][e];
+  for (int n = 0; n < NOT; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows lane/4 and lane/4 + 8 of the warp
+  uint32_t qf[NKS][4];
+
+  if (n_tiles > 0)
+    cp_async_wait<1>();   // Q has landed; the first K/V tile may still be in flight
+  else
+    cp_async_wait<0>();
+  __syncthreads();
+  {
+    const int r = warp * 16 + (lane & 15);
 #pragma unroll
-        for (int j = 0; j < 4; j++) kbv[j] = sm.k[tx * 4 + j][e];
-#pragma unroll
-        for (int i = 0; i < 4; i++)
-#pragma unroll
-          for (int j = 0; j < 4; j++) acc[i][j] = fmaf(qa[i], kbv[j], acc[i][j]);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; i++)
-#pragma unroll
-        for (int j = 0; j < 4; j++) sm.s[ty * 4 + i][tx * 4 + j] = (k0 + tx * 4 + j < k_end) ? acc[i][j] : -INFINITY;
-    }
-    __syncthreads();
-    if (tid < QT) {
-      float mx = -INFINITY;
-      for (int kk = 0; kk < KT; kk++) mx = fmaxf(mx, sm.s[tid][kk]);
-      const float m_new = fmaxf(m_run, mx);
-      const float corr = m_run == -INFINITY ? 0.f : expf(m_run - m_new);
-      float sum = 0.f;
-      for (int kk = 0; kk < KT; kk++) {
-        const float sv = sm.s[tid][kk];
-        const float pv = sv == -INFINITY ? 0.f : expf(sv - m_new);
-        sm.s[tid][kk] = pv;
-        sum += pv;
-      }
-      l_run = l_run * corr + sum;
-      m_run = m_new;
-      sm.corr[tid] = corr;
-    }
-    __syncthreads();
-    {
-      const float corr = sm.corr[orow];
-#pragma unroll
-      for (int c = 0; c < H / 4; c++) o[c] *= corr;
-      for (int kk = 0; kk < KT; kk++) {
-        const float pv = sm.s[orow][kk];
-#pragma unroll
-        for (int c = 0; c < H / 4; c++) o[c] = fmaf(pv, sm.v[kk][oc0 + c], o[c]);
-      }
-    }
+    for (int kk = 0; kk < NKS; kk++) ldsm_x4(swz<H>(q_s, r, kk * 2 + (lane >> 4)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
   }
-  // partial outputs
-  const int qi = qt * QT + orow;
-  if (qi < nrows) {
+
+  for (int it = 0; it < n_tiles; it++) {
+    const int buf = it & 1, k0 = k_begin + it * KT;
+    if (it + 1 < n_tiles) {
+      load_kv(buf ^ 1, k0 + KT);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t ks = smem_addr(sm.k[buf]), vs = smem_addr(sm.v[buf]);
+    // ---- S = Q K^T: 16 rows x 64 keys per warp ----
+    float s[KT / 8][4];
+#pragma unroll
+    for (int n = 0; n < KT / 8; n++) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+    for (int kp = 0; kp < KT / 16; kp++) {
+#pragma unroll
+      for (int kk = 0; kk < NKS; kk++) {
+        // 8x8 matrices: (keys +0..7, dims lo), (keys +0..7, dims hi), (keys +8..15, dims lo), (keys +8..15, dims hi)
+        const int key = kp * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int c = kk * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(swz<H>(ks, key, c), b0, b1, b2, b3);
+        mma_bf16(s[2 * kp], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+        mma_bf16(s[2 * kp + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+      }
+    }
+    // ---- online softmax (base 2) ----
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < KT / 8; n++) {
+      const int key = k0 + n * 8 + (lane & 3) * 2;
+      const bool v0 = key < k_end, v1 = key + 1 < k_end;
+      s[n][0] = v0 ? s[n][0] * sl2 : -INFINITY;
+      s[n][1] = v1 ? s[n][1] * sl2 : -INFINITY;
+      s[n][2] = v0 ? s[n][2] * sl2 : -INFINITY;
+      s[n][3] = v1 ? s[n][3] * sl2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: every tile holds at least one valid key
+    const float c0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mn0);
+    const float c1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < KT / 8; n++) {
+      s[n][0] = exp2f(s[n][0] - mn0);
+      s[n][1] = exp2f(s[n][1] - mn0);
+      s[n][2] = exp2f(s[n][2] - mn1);
+      s[n][3] = exp2f(s[n][3] - mn1);
+      ps0 += s[n][0] + s[n][1];
+      ps1 += s[n][2] + s[n][3];
+    }
+    l0 = l0 * c0 + ps0;
+    l1 = l1 * c1 + ps1;
+#pragma unroll
+    for (int n = 0; n < NOT; n++) {
+      o[n][0] *= c0;
+      o[n][1] *= c0;
+      o[n][2] *= c1;
+      o[n][3] *= c1;
+    }
+    // ---- O += P V ----
+#pragma unroll
+    for (int kk = 0; kk < KT / 16; kk++) {
+      const uint32_t a0 = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+      const uint32_t a1 = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+      const uint32_t a2 = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      const uint32_t a3 = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+      for (int np = 0; np < NOT / 2; np++) {
+        // transposed 8x8 matrices: (keys +0..7, dims lo), (keys +8..15, dims lo), (keys +0..7, dims hi), (keys +8..15, dims hi)
+        const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int c = np * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(swz<H>(vs, key, c), b0, b1, b2, b3);
+        mma_bf16(o[2 * np], a0, a1, a2, a3, b0, b1);
+        mma_bf16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    __syncthreads();   // this buffer is refilled by the next iteration's prefetch
+  }
+
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const int rlo = qt * QT + warp * 16 + (lane >> 2);
+#pragma unroll
+  for (int half = 0; half < 2; half++) {
+    const int qi = rlo + half * 8;
+    if (qi >= nrows) continue;
     const int j = qi / grp, i = g * grp + qi % grp;
     const size_t row = (size_t)b * a.L + j;
-    float* dst = a.o_part + (((size_t)split * a.rows + row) * a.nq + i) * H + oc0;
+    const float m = half ? m1 : m0, l = half ? l1 : l0;
+    if (a.splits == 1) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      bf16* dst = out + (row * a.nq + i) * H + (lane & 3) * 2;
 #pragma unroll
-    for (int c = 0; c < H / 4; c++) dst[c] = o[c];
-  }
-  if (tid < QT) {
-    const int qi2 = qt * QT + tid;
-    if (qi2 < nrows) {
-      const int j = qi2 / grp, i = g * grp + qi2 % grp;
-      const size_t row = (size_t)b * a.L + j;
-      a.ml[((size_t)split * a.rows + row) * a.nq + i] = make_float2(m_run, l_run);
+      for (int n = 0; n < NOT; n++)
+        *reinterpret_cast<__nv_bfloat162*>(dst + n * 8) =
+            __floats2bfloat162_rn(o[n][half * 2] * inv, o[n][half * 2 + 1] * inv);
+    } else {
+      float* dst = a.o_part + (((size_t)split * a.rows + row) * a.nq + i) * H + (lane & 3) * 2;
+#pragma unroll
+      for (int n = 0; n < NOT; n++)
+        *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][half * 2], o[n][half * 2 + 1]);
+      if ((lane & 3) == 0) a.ml[((size_t)split * a.rows + row) * a.nq + i] = make_float2(m, l);
     }
   }
 }
 
+// Combines the splits of one (row, q head); running maxima are in base-2 units.
 template <int H>
 __global__ void attn_merge_kernel(bf16* __restrict__ out, const float* __restrict__ o_part,
                                   const float2* __restrict__ ml, int nsplit, int rows, int nq) {
@@ -158,7 +277,7 @@ __global__ void attn_merge_kernel(bf16* __restrict__ out, const float* __restric
   for (int s = 0; s < nsplit; s++) {
     const float2 v = ml[((size_t)s * rows + r) * nq + i];
     if (v.y > 0.f) {
-      const float w = expf(v.x - M);
+      const float w = exp2f(v.x - M);
       den += v.y * w;
       num += o_part[(((size_t)s * rows + r) * nq + i) * H + e] * w;
     }
@@ -175,17 +294,16 @@ void attn_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* s
   const int max_splits = ceil_div(max_keys, KT);
   int s = ceil_div(2 * num_sms, base);
   s = s < 1 ? 1 : (s > max_splits ? max_splits : s);
-  int ch = ceil_div(ceil_div(max_keys, s), KT) * KT;
+  const int ch = ceil_div(ceil_div(max_keys, s), KT) * KT;
   *chunk = ch;
   *splits = ceil_div(max_keys, ch);
 }
 
 cudaError_t attn_init_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)sizeof(AttnSmem<128>));
+  cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(Smem<128>));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_simt_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(AttnSmem<64>));
+    e = cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem<64>));
   return e;
 }
 
@@ -194,16 +312,14 @@ cudaError_t launch_attention(const AttnArgs& a, bf16* out, cudaStream_t st) {
   dim3 grid(ceil_div(a.L * grp, QT), a.batch * a.nkv, a.splits);
   cudaError_t err;
   if (a.head_dim == 128) {
-    const size_t smem = sizeof(AttnSmem<128>);
-    attn_simt_kernel<128><<<grid, 256, smem, st>>>(a);
+    attn_mma_kernel<128><<<grid, NWARP * 32, sizeof(Smem<128>), st>>>(a, out);
     count_launch();
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = cudaGetLastError()) != cudaSuccess || a.splits == 1) return err;
     attn_merge_kernel<128><<<dim3(a.rows, a.nq), 128, 0, st>>>(out, a.o_part, a.ml, a.splits, a.rows, a.nq);
   } else {
-    const size_t smem = sizeof(AttnSmem<64>);
-    attn_simt_kernel<64><<<grid, 256, smem, st>>>(a);
+    attn_mma_kernel<64><<<grid, NWARP * 32, sizeof(Smem<64>), st>>>(a, out);
     count_launch();
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = cudaGetLastError()) != cudaSuccess || a.splits == 1) return err;
     attn_merge_kernel<64><<<dim3(a.rows, a.nq), 64, 0, st>>>(out, a.o_part, a.ml, a.splits, a.rows, a.nq);
   }
   count_launch();

@@ -35,7 +35,7 @@ namespace {
 
 constexpr int BM = 128, BK = 64, UMMA_K = 16;
 constexpr int kThreads = 192;
-enum { EPI_STORE = 0, EPI_ARGMAX = 1 };
+enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_SWIGLU = 2 };
 
 struct TcParams {
   CUtensorMap tm_x[8];   // activation K-segments (box rows: BN if swap else 128)
@@ -55,6 +55,9 @@ struct TcParams {
   const int* rows_sorted;        // sorted row -> original row (logits only)
   float* logits;                 // [n_rows, V] or null
   int V;
+  // EPI_SWIGLU: W = [gate; up] rows [2F, K]; output hmid[M][F] = bf16(silu(gate) * up)
+  bf16* hmid;
+  int F;
 };
 
 template <int BN>
@@ -64,6 +67,12 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // two accumulator buffers
 };
+// shared memory the SwiGLU epilogue uses to hand the up-projection values from the warps holding TMEM lanes
+// 64..127 to the warps holding the gate values of the same features (lanes 0..63), weight-tile placement only
+template <int BN, bool SWAP, int EPI>
+constexpr int xch_bytes() {
+  return (EPI == EPI_SWIGLU && SWAP) ? 64 * BN * 4 : 0;
+}
 
 struct Work {
   int a_row0, b_row0;   // first row of the 128-row (A) and BN-row (B) operand tiles
@@ -76,10 +85,10 @@ struct Work {
 template <bool SWAP, int BN, int EPI>
 __device__ __forceinline__ bool get_work(const TcParams& p, int t, int total, Work& w) {
   if (t >= total) return false;
-  if (EPI == EPI_STORE) {
+  if (EPI != EPI_ARGMAX) {
     const int pi = t % p.pt, qi = (t / p.pt) % p.qt, s = t / (p.pt * p.qt);
-    w.a_row0 = pi * BM;
-    w.b_row0 = qi * BN;
+    w.a_row0 = pi * ((EPI == EPI_SWIGLU && SWAP) ? BM / 2 : BM);    // SwiGLU: first feature of the tile
+    w.b_row0 = qi * ((EPI == EPI_SWIGLU && !SWAP) ? BN / 2 : BN);
     w.split = s;
     w.k0 = s * p.k_split;
     const int k1 = min(p.K, w.k0 + p.k_split);
@@ -104,7 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   using C = Cfg<BN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  float* xch = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + xch_bytes<BN, SWAP, EPI>());
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -112,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                  tempty0 = tfull0 + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int total = (EPI == EPI_STORE) ? p.pt * p.qt * p.splits : *p.n_items;
+  const int total = (EPI != EPI_ARGMAX) ? p.pt * p.qt * p.splits : *p.n_items;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; s++) {
@@ -155,7 +165,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           const uint32_t sb = sa + C::A_BYTES;
           const int k = w.k0 + kb * BK;
           const int seg = k / p.seg_k, kx = k - seg * p.seg_k;
-          if (SWAP) {
+          if (EPI == EPI_SWIGLU) {
+            // weight tile = [gate rows f0.. ; up rows F+f0..], two boxes of half the tile each
+            if (SWAP) {
+              tc::tma_load_2d(sa, &p.tm_w, k, w.a_row0, fb);
+              tc::tma_load_2d(sa + C::A_BYTES / 2, &p.tm_w, k, p.F + w.a_row0, fb);
+              tc::tma_load_2d(sb, &p.tm_x[seg], kx, w.b_row0, fb);
+            } else {
+              tc::tma_load_2d(sa, &p.tm_x[seg], kx, w.a_row0, fb);
+              tc::tma_load_2d(sb, &p.tm_w, k, w.b_row0, fb);
+              tc::tma_load_2d(sb + C::B_BYTES / 2, &p.tm_w, k, p.F + w.b_row0, fb);
+            }
+          } else if (SWAP) {
             tc::tma_load_2d(sa, &p.tm_w, k, w.a_row0, fb);
             tc::tma_load_2d(sb, &p.tm_x[seg], kx, w.b_row0, fb);
           } else {
@@ -254,6 +275,59 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             }
           }
         }
+      } else if (EPI == EPI_SWIGLU) {
+        if (SWAP) {
+          // lanes 0..63: gate of feature f0 + lane; lanes 64..127: up of feature f0 + lane - 64
+          const bool up_half = row_in_tile >= 64;
+          const int fr = up_half ? row_in_tile - 64 : row_in_tile;
+          const int f = w.a_row0 + fr;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float v[16];
+            tc::tmem_ld16(t_acc + c0, v);
+            if (up_half) {
+#pragma unroll
+              for (int j = 0; j < 16; j++) xch[fr * BN + c0 + j] = v[j];
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (!up_half && f < p.F) {
+#pragma unroll
+              for (int j = 0; j < 16; j++) {
+                const int m = w.b_row0 + c0 + j;
+                if (m < p.M) {
+                  const float gv = v[j], uv = xch[fr * BN + c0 + j];
+                  p.hmid[(size_t)m * p.F + f] = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+                }
+              }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+          }
+        } else {
+          // columns 0..BN/2-1: gate of features f0.., columns BN/2..BN-1: up of the same features
+          const int m = w.a_row0 + row_in_tile;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+            float gv[16], uv[16];
+            tc::tmem_ld16(t_acc + c0, gv);
+            tc::tmem_ld16(t_acc + BN / 2 + c0, uv);
+            const int f0 = w.b_row0 + c0;
+            if (m < p.M) {
+              bf16* dst = p.hmid + (size_t)m * p.F + f0;
+              if (f0 + 16 <= p.F && (p.F & 7) == 0) {
+                uint4 pk[2];
+                bf16* pe = reinterpret_cast<bf16*>(pk);
+#pragma unroll
+                for (int j = 0; j < 16; j++) pe[j] = __float2bfloat16_rn(gv[j] / (1.0f + expf(-gv[j])) * uv[j]);
+                reinterpret_cast<uint4*>(dst)[0] = pk[0];
+                reinterpret_cast<uint4*>(dst)[1] = pk[1];
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++)
+                  if (f0 + j < p.F) dst[j] = __float2bfloat16_rn(gv[j] / (1.0f + expf(-gv[j])) * uv[j]);
+              }
+            }
+          }
+        }
       } else {
         // LM head: rows = vocabulary ids, columns = sorted positions of one class
         const int vid = w.a_row0 + row_in_tile;
@@ -318,21 +392,21 @@ cudaError_t make_tmap(CUtensorMap* tm, const void* ptr, int rows, int cols, int 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool SWAP, int EPI>
 constexpr size_t smem_bytes() {
-  return (size_t)STAGES * Cfg<BN>::STAGE_BYTES + 1024 + 256;
+  return (size_t)STAGES * Cfg<BN>::STAGE_BYTES + xch_bytes<BN, SWAP, EPI>() + 1024 + 256;
 }
 
 template <int BN, int STAGES, bool SWAP, int EPI>
 cudaError_t set_attr() {
-  static_assert(smem_bytes<BN, STAGES>() <= 227 * 1024, "shared memory");
+  static_assert(smem_bytes<BN, STAGES, SWAP, EPI>() <= 227 * 1024, "shared memory");
   return cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, SWAP, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes<BN, STAGES>());
+                              (int)smem_bytes<BN, STAGES, SWAP, EPI>());
 }
 
 template <int BN, int STAGES, bool SWAP, int EPI>
 cudaError_t launch_kernel(const TcParams& p, int grid, cudaStream_t st) {
-  tc_gemm_kernel<BN, STAGES, SWAP, EPI><<<grid, kThreads, smem_bytes<BN, STAGES>(), st>>>(p);
+  tc_gemm_kernel<BN, STAGES, SWAP, EPI><<<grid, kThreads, smem_bytes<BN, STAGES, SWAP, EPI>(), st>>>(p);
   count_launch();
   return cudaGetLastError();
 }
@@ -350,6 +424,10 @@ cudaError_t tc_init_attributes() {
   if (e == cudaSuccess) e = set_attr<16, 6, true, EPI_ARGMAX>();
   if (e == cudaSuccess) e = set_attr<32, 5, true, EPI_ARGMAX>();
   if (e == cudaSuccess) e = set_attr<64, 4, true, EPI_ARGMAX>();
+  if (e == cudaSuccess) e = set_attr<16, 10, true, EPI_SWIGLU>();
+  if (e == cudaSuccess) e = set_attr<32, 8, true, EPI_SWIGLU>();
+  if (e == cudaSuccess) e = set_attr<64, 6, true, EPI_SWIGLU>();
+  if (e == cudaSuccess) e = set_attr<256, 4, false, EPI_SWIGLU>();
   return e;
 }
 
@@ -454,6 +532,57 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, const TcPlan& pl, cudaStream_t st)
   }
   if (pl.bn == 128) return launch_kernel<128, 6, false, EPI_STORE>(p, pl.grid, st);
   return launch_kernel<256, 4, false, EPI_STORE>(p, pl.grid, st);
+}
+
+// Gate/up projection with the SwiGLU epilogue: one pass over [gate; up] (no split-K: the nonlinearity needs
+// complete sums), tiles of 64 features (weight-tile placement) or 128 features (token-tile placement).
+TcPlan tc_plan_swiglu(int M, int F, int K, int num_sms) {
+  TcPlan pl{};
+  pl.splits = 1;
+  pl.k_split = K;
+  if (M <= 64) {
+    pl.swap = true;
+    pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    pl.pt = ceil_div(F, BM / 2);
+    pl.qt = ceil_div(M, pl.bn);
+  } else {
+    pl.swap = false;
+    pl.bn = 256;
+    pl.pt = ceil_div(M, BM);
+    pl.qt = ceil_div(F, 128);
+  }
+  pl.grid = std::min(pl.pt * pl.qt, num_sms);
+  return pl;
+}
+
+cudaError_t launch_tc_swiglu(const bf16* x, int M, int K, const bf16* w_gate_up, int F, bf16* hmid, const TcPlan& pl,
+                             cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  if (K % BK) return cudaErrorInvalidValue;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  const int x_box = pl.swap ? pl.bn : BM, w_box = pl.swap ? BM / 2 : pl.bn / 2;
+  cudaError_t e = make_tmap(&p.tm_x[0], x, M, K, K, x_box);
+  if (e != cudaSuccess) return e;
+  e = make_tmap(&p.tm_w, w_gate_up, 2 * F, K, K, w_box);
+  if (e != cudaSuccess) return e;
+  p.n_seg = 1;
+  p.seg_k = K;
+  p.M = M;
+  p.N = 2 * F;
+  p.K = K;
+  p.pt = pl.pt;
+  p.qt = pl.qt;
+  p.splits = 1;
+  p.k_split = K;
+  p.hmid = hmid;
+  p.F = F;
+  if (pl.swap) {
+    if (pl.bn == 16) return launch_kernel<16, 10, true, EPI_SWIGLU>(p, pl.grid, st);
+    if (pl.bn == 32) return launch_kernel<32, 8, true, EPI_SWIGLU>(p, pl.grid, st);
+    return launch_kernel<64, 6, true, EPI_SWIGLU>(p, pl.grid, st);
+  }
+  return launch_kernel<256, 4, false, EPI_SWIGLU>(p, pl.grid, st);
 }
 
 int tc_lm_row_tile(int n_rows) { return n_rows <= 16 ? 16 : (n_rows <= 32 ? 32 : 64); }

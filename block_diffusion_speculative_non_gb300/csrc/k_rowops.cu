@@ -1,5 +1,6 @@
-// k_rowops.cu — row-wise kernels of the drafter pass: embedding gather, RMSNorm, the q/k RMSNorm + RoPE
-// epilogue of the QKV projection, the context K/V epilogue, residual add and SwiGLU.
+// k_rowops.cu — row-wise kernels of the drafter pass: embedding gather + RMSNorm, residual add + RMSNorm (which
+// also reduces the split-K partial sums), the q/k RMSNorm + RoPE epilogue of the QKV projection, and the context
+// K/V epilogue.  (SwiGLU runs in the gate/up GEMM epilogue, k_gemm_tc.cu.)
 //
 // Method: VFlash paper (zh) §2.1-§2.2 (one anchor + L-1 mask tokens through a bidirectional layer stack
 // conditioned on per-layer context K/V); layer form = pre-norm transformer layer with per-head q/k RMSNorm
@@ -12,28 +13,6 @@ namespace fpd {
 
 __device__ int32_t g_device_check = 0;
 
-// ---- a3: x[b*L + j] = E[anchor[b]] (j == 0) or E[mask_id] (j >= 1) ---------------------------------------------
-__global__ void embed_kernel(bf16* __restrict__ x, const bf16* __restrict__ embed, const int32_t* __restrict__ anchor,
-                             int32_t mask_id, int L, int d, int V) {
-  const int r = blockIdx.x, b = r / L, j = r % L;
-  int id = j == 0 ? anchor[b] : mask_id;
-  uint4* dst = reinterpret_cast<uint4*>(x + (size_t)r * d);
-  if (id < 0 || id >= V) {
-    if (threadIdx.x == 0) record_check(kCheckBadToken);
-    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
-    return;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(embed + (size_t)id * d);
-  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
-}
-
-cudaError_t launch_embed(bf16* x, const bf16* embed, const int32_t* anchor, int32_t mask_id, int B, int L, int d,
-                         int V, cudaStream_t st) {
-  embed_kernel<<<B * L, 128, 0, st>>>(x, embed, anchor, mask_id, L, d, V);
-  count_launch();
-  return cudaGetLastError();
-}
-
 // ---- block reduction helper ------------------------------------------------------------------------------------
 __device__ __forceinline__ float block_sum(float v, float* red) {
   v = warp_sum(v);
@@ -43,47 +22,6 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   __syncthreads();
   float t = l < nw ? red[l] : 0.f;
   return warp_sum(t);
-}
-
-// ---- RMSNorm of bf16 rows -> bf16 rows ---------------------------------------------------------------------------
-// out[r] = bf16(x / sqrt(mean(x^2) + eps) * g).  skip_L > 0 maps output row r to input row
-// (r / (skip_L-1)) * skip_L + r % (skip_L-1) + 1, i.e. it drops the anchor row of every block (final norm).
-__global__ void rmsnorm_kernel(bf16* __restrict__ out, const bf16* __restrict__ in, const bf16* __restrict__ g, int d,
-                               float eps, int skip_L) {
-  __shared__ float red[32];
-  const int r = blockIdx.x;
-  const int rin = skip_L > 0 ? (r / (skip_L - 1)) * skip_L + r % (skip_L - 1) + 1 : r;
-  const uint4* src = reinterpret_cast<const uint4*>(in + (size_t)rin * d);
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
-    uint4 u = src[i];
-    const bf16* e = reinterpret_cast<const bf16*>(&u);
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-      float f = __bfloat162float(e[k]);
-      ss += f * f;
-    }
-  }
-  const float inv = rsqrtf(block_sum(ss, red) / (float)d + eps);
-  const uint4* gs = reinterpret_cast<const uint4*>(g);
-  uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * d);
-  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
-    uint4 u = src[i], gu = gs[i], o;
-    const bf16* e = reinterpret_cast<const bf16*>(&u);
-    const bf16* ge = reinterpret_cast<const bf16*>(&gu);
-    bf16* oe = reinterpret_cast<bf16*>(&o);
-#pragma unroll
-    for (int k = 0; k < 8; k++) oe[k] = __float2bfloat16_rn(__bfloat162float(e[k]) * inv * __bfloat162float(ge[k]));
-    dst[i] = o;
-  }
-}
-
-cudaError_t launch_rmsnorm(bf16* out, const bf16* in, const bf16* g, int rows, int d, float eps, int skip_L,
-                           cudaStream_t st) {
-  if (rows <= 0) return cudaSuccess;
-  rmsnorm_kernel<<<rows, 256, 0, st>>>(out, in, g, d, eps, skip_L);
-  count_launch();
-  return cudaGetLastError();
 }
 
 // ---- RMSNorm of fp32 split-K partial sums -> bf16 (fused context) -------------------------------------------------
@@ -239,56 +177,95 @@ cudaError_t launch_kv_post(bf16* store, const float* part, int nsplit, size_t sp
   return cudaGetLastError();
 }
 
-// ---- a6/a7 epilogue: x = bf16(x + sum_s part[s]) ------------------------------------------------------------------
-__global__ void residual_add_kernel(bf16* __restrict__ x, const float* __restrict__ part, int nsplit,
-                                    size_t split_stride, size_t n8) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    uint4 u = reinterpret_cast<uint4*>(x)[i];
-    bf16* e = reinterpret_cast<bf16*>(&u);
-    float acc[8];
+// ---- residual add fused with the next RMSNorm: one block per row ------------------------------------------------
+// x = bf16(x + sum_s part[s]);  xn = bf16(x / sqrt(mean(x^2) + eps) * g)   (g == nullptr: residual only).
+// The norm reads the bf16-rounded x, exactly what an unfused norm kernel would read back.
+template <int VPT>
+__global__ void residual_norm_kernel(bf16* __restrict__ x, bf16* __restrict__ xn, const float* __restrict__ part,
+                                     int nsplit, size_t split_stride, const bf16* __restrict__ g, int d, float eps) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  bf16* xr = x + (size_t)r * d;
+  float v[VPT];
+  float ss = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; k++) acc[k] = 0.f;
-    for (int s = 0; s < nsplit; s++) {
-      const float4* p = reinterpret_cast<const float4*>(part + s * split_stride) + 2 * i;
-      float4 a = p[0], c = p[1];
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += c.x; acc[5] += c.y; acc[6] += c.z; acc[7] += c.w;
+  for (int k = 0; k < VPT; k++) {
+    const int i = threadIdx.x + k * blockDim.x;
+    v[k] = 0.f;
+    if (i < d) {
+      float a = __bfloat162float(xr[i]);
+      float acc = 0.f;
+      for (int s = 0; s < nsplit; s++) acc += part[s * split_stride + (size_t)r * d + i];
+      const bf16 nb = __float2bfloat16_rn(a + acc);
+      xr[i] = nb;
+      v[k] = __bfloat162float(nb);
+      ss += v[k] * v[k];
     }
+  }
+  if (!g) return;
+  const float inv = rsqrtf(block_sum(ss, red) / (float)d + eps);
 #pragma unroll
-    for (int k = 0; k < 8; k++) e[k] = __float2bfloat16_rn(__bfloat162float(e[k]) + acc[k]);
-    reinterpret_cast<uint4*>(x)[i] = u;
+  for (int k = 0; k < VPT; k++) {
+    const int i = threadIdx.x + k * blockDim.x;
+    if (i < d) xn[(size_t)r * d + i] = __float2bfloat16_rn(v[k] * inv * __bfloat162float(g[i]));
   }
 }
 
-cudaError_t launch_residual_add(bf16* x, const float* part, int nsplit, size_t split_stride, size_t n,
-                                cudaStream_t st) {
-  size_t n8 = n / 8;
-  int grid = (int)std::min<size_t>((n8 + 255) / 256, 4096);
-  residual_add_kernel<<<grid, 256, 0, st>>>(x, part, nsplit, split_stride, n8);
+cudaError_t launch_residual_norm(bf16* x, bf16* xn, const float* part, int nsplit, size_t split_stride, const bf16* g,
+                                 int rows, int d, float eps, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (d <= 256 * 4)
+    residual_norm_kernel<4><<<rows, 256, 0, st>>>(x, xn, part, nsplit, split_stride, g, d, eps);
+  else if (d <= 512 * 8)
+    residual_norm_kernel<8><<<rows, 512, 0, st>>>(x, xn, part, nsplit, split_stride, g, d, eps);
+  else
+    residual_norm_kernel<16><<<rows, 1024, 0, st>>>(x, xn, part, nsplit, split_stride, g, d, eps);
   count_launch();
   return cudaGetLastError();
 }
 
-// ---- a7 middle: hmid = bf16(silu(g) * u), g/u = columns f and F+f of the gate/up projection ------------------------
-__global__ void swiglu_kernel(bf16* __restrict__ hmid, const float* __restrict__ part, int nsplit, size_t split_stride,
-                              int F, size_t total) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t r = i / F, f = i % F;
-    float g = 0.f, u = 0.f;
-    for (int s = 0; s < nsplit; s++) {
-      g += part[s * split_stride + r * 2 * F + f];
-      u += part[s * split_stride + r * 2 * F + F + f];
+// ---- embedding gather fused with the first RMSNorm ----------------------------------------------------------------
+__global__ void embed_norm_kernel(bf16* __restrict__ x, bf16* __restrict__ xn, const bf16* __restrict__ embed,
+                                  const int32_t* __restrict__ anchor, int32_t mask_id, const bf16* __restrict__ g,
+                                  int L, int d, int V, float eps) {
+  __shared__ float red[32];
+  const int r = blockIdx.x, b = r / L, j = r % L;
+  int id = j == 0 ? anchor[b] : mask_id;
+  const bool bad = id < 0 || id >= V;
+  if (bad) {
+    if (threadIdx.x == 0) record_check(kCheckBadToken);
+    id = 0;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(embed + (size_t)id * d);
+  uint4* dx = reinterpret_cast<uint4*>(x + (size_t)r * d);
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+    uint4 u = bad ? make_uint4(0, 0, 0, 0) : src[i];
+    dx[i] = u;
+    const bf16* e = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      const float f = __bfloat162float(e[k]);
+      ss += f * f;
     }
-    const float sg = g / (1.0f + expf(-g));
-    hmid[i] = __float2bfloat16_rn(sg * u);
+  }
+  const float inv = rsqrtf(block_sum(ss, red) / (float)d + eps);
+  const uint4* gs = reinterpret_cast<const uint4*>(g);
+  uint4* dn = reinterpret_cast<uint4*>(xn + (size_t)r * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+    uint4 u = bad ? make_uint4(0, 0, 0, 0) : src[i], gu = gs[i], o;
+    const bf16* e = reinterpret_cast<const bf16*>(&u);
+    const bf16* ge = reinterpret_cast<const bf16*>(&gu);
+    bf16* oe = reinterpret_cast<bf16*>(&o);
+#pragma unroll
+    for (int k = 0; k < 8; k++) oe[k] = __float2bfloat16_rn(__bfloat162float(e[k]) * inv * __bfloat162float(ge[k]));
+    dn[i] = o;
   }
 }
 
-cudaError_t launch_swiglu(bf16* hmid, const float* part, int nsplit, size_t split_stride, int rows, int F,
-                          cudaStream_t st) {
-  size_t total = (size_t)rows * F;
-  int grid = (int)std::min<size_t>((total + 255) / 256, 8192);
-  swiglu_kernel<<<grid, 256, 0, st>>>(hmid, part, nsplit, split_stride, F, total);
+cudaError_t launch_embed_norm(bf16* x, bf16* xn, const bf16* embed, const int32_t* anchor, int32_t mask_id,
+                              const bf16* g, int B, int L, int d, int V, float eps, cudaStream_t st) {
+  embed_norm_kernel<<<B * L, 256, 0, st>>>(x, xn, embed, anchor, mask_id, g, L, d, V, eps);
   count_launch();
   return cudaGetLastError();
 }

@@ -98,7 +98,7 @@ class Drafter:
         pc = np.asarray(layout_np["pos_class"], dtype=np.int16)
         if pc.ndim == 1:
             pc = np.broadcast_to(pc, (batch, block_len))
-        pc_d = torch.from_numpy(np.ascontiguousarray(pc)).to(device)
+        pc_d = torch.from_numpy(np.array(pc, dtype=np.int16, order="C", copy=True)).to(device)
         lay = make_layout(layout_np["class_off"], layout_np["class_ranges"], pc_d)
         rule = layout_np.get("rule")
         rule_d = None
@@ -106,7 +106,7 @@ class Drafter:
             r = np.asarray(rule, dtype=np.int8)
             if r.ndim == 1:
                 r = np.broadcast_to(r, (batch, block_len))
-            rule_d = torch.from_numpy(np.ascontiguousarray(r)).to(device)
+            rule_d = torch.from_numpy(np.array(r, dtype=np.int8, order="C", copy=True)).to(device)
         return lay, rule_d
 
     def verify_text(self, batch, block_len, draft, target, accept=None, committed=None, valid=None, stream=None):

@@ -21,6 +21,11 @@ fpd_status fpd_test_gemm(int impl, int placement, int M, int N, int K, const voi
                          void* workspace, size_t workspace_bytes, void* stream);
 size_t fpd_test_gemm_workspace_bytes(int M, int N, int K);
 
+/* hmid[M, F] (bf16) = silu(X . Wg^T) * (X . Wu^T) for X [M, K] and W = [Wg; Wu] ([2F, K]) bf16 row-major device
+ * matrices, with the gate/up tcgen05 kernel and its SwiGLU epilogue (weight-tile placement for M <= 64, token
+ * tiles above).  Asynchronous on stream. */
+fpd_status fpd_test_swiglu(int M, int F, int K, const void* X, const void* W, void* hmid, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

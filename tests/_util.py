@@ -2,8 +2,12 @@
 
 Tolerances: hidden states, K/V and logits agree with the oracle within a max relative error of 2e-2 per row
 (max_i |gpu_i - ref_i| / max_i |ref_i|; bf16 storage, fp32 accumulation on the GPU).  Token ids are bit-exact
-except where the oracle's top-2 fp32 logit margin is below 1e-2.  Acceptance lengths and committed tokens are
-bit-exact given the ids.
+except where the oracle's top-2 fp32 logit margin is below 1e-2 when the LM head + argmax stage is given the
+oracle's hidden states (assert_tokens).  Through the whole chain the bf16 storage points make the two sides'
+hidden states differ by about one bf16 ulp in most elements after five layers (the same happens between the
+fp64 oracle and an fp32-accumulating copy of it), so there a differing id is accepted only where the logit
+errors of the two competing ids explain it (assert_tokens_chain), and the GPU id must be the argmax of the
+GPU's own logits.  Acceptance lengths and committed tokens are bit-exact given the ids.
 """
 import numpy as np
 import torch
@@ -73,3 +77,25 @@ def assert_logits(gpu: np.ndarray, ref: np.ndarray, what: str = "logits", few: i
             worst, where = e, (r, n, float(np.max(np.abs(g - t))), float(den))
     assert worst <= REL_TOL, f"{what}: max row rel err {worst:.3e} (row, legal ids, abs err, scale) = {where}"
     return worst
+
+
+def assert_tokens_chain(gpu_tok, ref_tok, margin, gpu_logits, ref_logits, what="tokens"):
+    """End-to-end id check: every GPU id is the lowest-id argmax of the GPU's own legal logits; an id that
+    differs from the oracle's is accepted only at margin < 1e-2 or where the oracle margin is below twice
+    the larger logit error of the two ids involved."""
+    gpu_tok = np.asarray(gpu_tok).reshape(-1)
+    ref_tok = np.asarray(ref_tok).reshape(-1)
+    margin = np.asarray(margin).reshape(-1)
+    legal = ~np.isnan(ref_logits)
+    for r in range(len(gpu_tok)):
+        ids = np.nonzero(legal[r])[0]
+        gl = gpu_logits[r, ids].astype(np.float32)
+        assert gpu_tok[r] == ids[int(np.argmax(gl))], f"{what}: row {r} id is not the argmax of the GPU logits"
+    bad = []
+    for r in np.nonzero(gpu_tok != ref_tok)[0]:
+        a, b = gpu_tok[r], ref_tok[r]
+        err = max(abs(float(gpu_logits[r, a]) - ref_logits[r, a]), abs(float(gpu_logits[r, b]) - ref_logits[r, b]))
+        if not (margin[r] < MARGIN_EXEMPT or margin[r] < 2 * err):
+            bad.append((int(r), float(margin[r]), err))
+    assert not bad, f"{what}: ids differ beyond the logit error: {bad[:5]}"
+    return int((gpu_tok != ref_tok).sum())

@@ -19,6 +19,9 @@ def lib():
     l.fpd_test_gemm.restype = ctypes.c_int
     l.fpd_test_gemm_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
     l.fpd_test_gemm_workspace_bytes.restype = ctypes.c_size_t
+    l.fpd_test_swiglu.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_void_p, ctypes.c_void_p]
+    l.fpd_test_swiglu.restype = ctypes.c_int
     return l
 
 
@@ -63,3 +66,21 @@ def test_tc_gemm_forced_placement(lib, M, N, K, placement):
 @pytest.mark.parametrize("M,N,K", [(15, 300, 256), (130, 70, 128)])
 def test_simt_gemm(lib, M, N, K):
     assert run(lib, 1, -1, M, N, K, seed=2) < 1e-5
+
+
+@pytest.mark.parametrize("M,F,K", [(1, 256, 128), (15, 9728, 2560), (32, 320, 256), (64, 1536, 512),
+                                   (65, 1536, 512), (385, 1000, 640)])
+def test_tc_swiglu(lib, M, F, K):
+    """Gate/up projection with the SwiGLU epilogue against silu(x Wg^T) * (x Wu^T) in fp32; the result is
+    stored in bf16, so it must agree within a bf16 rounding step of the fp32 reference."""
+    g = torch.Generator(device="cuda").manual_seed(M + F)
+    X = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    W = (0.05 * torch.randn(2 * F, K, device="cuda", generator=g)).to(torch.bfloat16)
+    H = torch.full((M, F), float("nan"), device="cuda", dtype=torch.bfloat16)
+    st = lib.fpd_test_swiglu(M, F, K, X.data_ptr(), W.data_ptr(), H.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    gu = X.float() @ W.float().T
+    ref = torch.nn.functional.silu(gu[:, :F]) * gu[:, F:]
+    err = ((H.float() - ref).abs() / (ref.abs() + 1e-3 * ref.abs().max())).max().item()
+    assert err < 1e-2, err

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import synth
-from _util import (assert_logits, assert_rows_close, assert_tokens, bits_of, dev_i32, f64)
+from _util import (assert_logits, assert_rows_close, assert_tokens, assert_tokens_chain, bits_of, dev_i32, f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -84,8 +84,19 @@ def _draft_and_compare(pkg, orc, dr, om, kv_ref, t_cap, ctx_len, anchor, mask_id
             pc = np.asarray(layout["pos_class"])
             lay_b["pos_class"] = pc if pc.ndim == 1 else pc[b]
         o_tok, o_margin, o_log = orc.constrain_argmax(om, o_hid, 1, L, layout=lay_b, want_logits=True)
-        assert_logits(g_log[b * (L - 1):(b + 1) * (L - 1)], o_log, f"request {b} logits")
-        assert_tokens(g_tok[b], o_tok[0], o_margin, f"request {b} tokens")
+        g_log_b = g_log[b * (L - 1):(b + 1) * (L - 1)]
+        assert_logits(g_log_b, o_log, f"request {b} logits")
+        assert_tokens_chain(g_tok[b], o_tok[0], o_margin, g_log_b, o_log, f"request {b} tokens")
+        # the LM head + argmax stage alone, given the oracle's hidden states: the strict id rule
+        hid_o = torch.from_numpy(o_hid.view(np.int16)).to(DEV).view(torch.bfloat16)
+        lay_1 = None
+        if layout is not None:
+            lay_1, _ = pkg.Drafter.layout(lay_b, 1, L, DEV)
+        lg1 = torch.full((L - 1, s.vocab), float("nan"), dtype=torch.float32, device=DEV)
+        t1 = dr.constrain_argmax(1, L, hid_o, layout=lay_1, logits_out=lg1)
+        torch.cuda.synchronize()
+        assert_logits(lg1.cpu().numpy(), o_log, f"request {b} logits from oracle hidden")
+        assert_tokens(t1.cpu().numpy()[0], o_tok[0], o_margin, f"request {b} tokens from oracle hidden")
     return g_tok, hid
 
 
