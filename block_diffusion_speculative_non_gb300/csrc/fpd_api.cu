@@ -504,7 +504,7 @@ fpd_status fpd_constrain_argmax(fpd_model* m, int batch, int L, const void* hidd
                                  d.d_model, d.rms_eps, L, st),
            "final norm");
   FPD_CUDA(launch_tc_lmhead(p, w.z, n_rows, (const bf16*)m->w.lm_head, d.d_model, d.vocab, w.items, w.n_items,
-                            w.max_items, w.packed, w.rows_sorted, logits_out, m->num_sms, st),
+                            w.max_items, w.packed, w.rows_sorted, logits_out, m->num_sms, layout == nullptr, st),
            "LM head + argmax");
   FPD_CUDA(launch_lm_decode(tokens_out, w.packed, w.inv_sorted, n_rows, st), "argmax decode");
   return FPD_OK;

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 #include "../../include/fpd.h"
 
@@ -29,6 +30,32 @@ __device__ __forceinline__ void record_check(int32_t code) { atomicCAS(&g_device
 // ---- host-side bookkeeping ---------------------------------------------------------------------------------
 extern std::atomic<uint64_t> g_launches;
 inline void count_launch(uint64_t n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// ---- programmatic dependent launch ---------------------------------------------------------------------------
+// Every kernel of the library is launched with programmatic stream serialisation: it may start while its
+// predecessor in the stream is still running.  pdl_trigger() lets the next kernel launch; pdl_wait() blocks
+// until every predecessor grid has completed and its memory is visible.  A kernel touches no buffer another
+// kernel writes or reads before pdl_wait() (the GEMM producer only prefetches weight tiles, which nothing
+// writes, into its own shared memory).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---- model -------------------------------------------------------------------------------------------------
 struct Model {

@@ -38,6 +38,7 @@ TcPlan tc_plan_swiglu(int M, int F, int K, int num_sms);
 cudaError_t launch_tc_swiglu(const bf16* x, int M, int K, const bf16* w_gate_up, int F, bf16* hmid, const TcPlan& pl,
                              cudaStream_t st);
 cudaError_t tc_init_attributes();     // once per process, before any stream capture
+void tc_set_swap_variant(int v);      // tuning sweeps only (fpd_test_set_variant)
 cudaError_t attn_init_attributes();
 cudaError_t launch_sum_splits(float* out, const float* part, int splits, size_t n, cudaStream_t st);
 
@@ -84,7 +85,7 @@ cudaError_t launch_lm_plan(const LmPlan& p, const int16_t* pos_class, int* rows_
 int tc_lm_row_tile(int n_rows);
 cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows, const bf16* W, int d, int V,
                              const int4* items, const int* n_items, int max_items, unsigned long long* packed,
-                             const int* rows_sorted, float* logits, int num_sms, cudaStream_t st);
+                             const int* rows_sorted, float* logits, int num_sms, bool unconstrained, cudaStream_t st);
 cudaError_t launch_lm_decode(int32_t* tokens, const unsigned long long* packed, const int* inv_sorted, int n,
                              cudaStream_t st);
 // RMSNorm of block rows into sorted order: out[i] = norm(hidden[map(rows_sorted[i])]), map drops anchors.

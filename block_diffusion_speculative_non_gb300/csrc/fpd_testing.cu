@@ -74,4 +74,6 @@ fpd_status fpd_test_swiglu(int M, int F, int K, const void* X, const void* W, vo
              : FPD_ERR_CUDA;
 }
 
+void fpd_test_set_variant(int variant) { tc_set_swap_variant(variant); }
+
 }  // extern "C"

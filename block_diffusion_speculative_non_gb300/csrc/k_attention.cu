@@ -71,6 +71,8 @@ struct Smem {
 
 template <int H>
 __global__ void __launch_bounds__(NWARP * 32) attn_mma_kernel(AttnArgs a, bf16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int CH = H / 8;     // 16-byte chunks per row
   constexpr int NKS = H / 16;   // k-steps over the head dimension
   constexpr int NOT = H / 8;    // 8-wide n-tiles of O
@@ -263,25 +265,47 @@ __global__ void __launch_bounds__(NWARP * 32) attn_mma_kernel(AttnArgs a, bf16* 
   }
 }
 
-// Combines the splits of one (row, q head); running maxima are in base-2 units.
+// Combines the splits of one (row, q head); running maxima are in base-2 units.  The (m, l) pairs of all splits
+// are staged in shared memory first, then every thread sums its column over the splits in split order.
 template <int H>
 __global__ void attn_merge_kernel(bf16* __restrict__ out, const float* __restrict__ o_part,
                                   const float2* __restrict__ ml, int nsplit, int rows, int nq) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float w_s[128];
+  __shared__ float den_s;
   const int r = blockIdx.x, i = blockIdx.y, e = threadIdx.x;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; s++) {
-    const float2 v = ml[((size_t)s * rows + r) * nq + i];
-    if (v.y > 0.f) M = fmaxf(M, v.x);
+  const int ns = nsplit < 128 ? nsplit : 128;   // attn_plan never makes more than 128 splits
+  for (int s = e; s < ns; s += blockDim.x) {
+    const float2 v = __ldcg(ml + ((size_t)s * rows + r) * nq + i);
+    w_s[s] = v.y > 0.f ? v.x : -INFINITY;       // running max of split s (empty splits excluded)
   }
-  float den = 0.f, num = 0.f;
-  for (int s = 0; s < nsplit; s++) {
-    const float2 v = ml[((size_t)s * rows + r) * nq + i];
-    if (v.y > 0.f) {
-      const float w = exp2f(v.x - M);
-      den += v.y * w;
-      num += o_part[(((size_t)s * rows + r) * nq + i) * H + e] * w;
+  __syncthreads();
+  if (e == 0) {
+    float M = -INFINITY;
+    for (int s = 0; s < ns; s++) M = fmaxf(M, w_s[s]);
+    float den = 0.f;
+    for (int s = 0; s < ns; s++) {
+      const float2 v = __ldcg(ml + ((size_t)s * rows + r) * nq + i);
+      const float wgt = w_s[s] == -INFINITY ? 0.f : exp2f(w_s[s] - M);
+      den += v.y * wgt;
+      w_s[s] = wgt;
     }
+    den_s = den;
   }
+  __syncthreads();
+  const float* op = o_part + ((size_t)r * nq + i) * H + e;
+  const size_t sstride = (size_t)rows * nq * H;
+  float num = 0.f;
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float t[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) t[u] = (s0 + u < ns && w_s[s0 + u] != 0.f) ? __ldcg(op + (size_t)(s0 + u) * sstride) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; u++)
+      if (s0 + u < ns) num += t[u] * w_s[s0 + u];
+  }
+  const float den = den_s;
   out[((size_t)r * nq + i) * H + e] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
 }
 }  // namespace
@@ -294,6 +318,7 @@ void attn_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* s
   const int max_splits = ceil_div(max_keys, KT);
   int s = ceil_div(2 * num_sms, base);
   s = s < 1 ? 1 : (s > max_splits ? max_splits : s);
+  s = s > 128 ? 128 : s;   // the merge kernel stages at most 128 splits' weights
   const int ch = ceil_div(ceil_div(max_keys, s), KT) * KT;
   *chunk = ch;
   *splits = ceil_div(max_keys, ch);
@@ -312,18 +337,15 @@ cudaError_t launch_attention(const AttnArgs& a, bf16* out, cudaStream_t st) {
   dim3 grid(ceil_div(a.L * grp, QT), a.batch * a.nkv, a.splits);
   cudaError_t err;
   if (a.head_dim == 128) {
-    attn_mma_kernel<128><<<grid, NWARP * 32, sizeof(Smem<128>), st>>>(a, out);
-    count_launch();
-    if ((err = cudaGetLastError()) != cudaSuccess || a.splits == 1) return err;
-    attn_merge_kernel<128><<<dim3(a.rows, a.nq), 128, 0, st>>>(out, a.o_part, a.ml, a.splits, a.rows, a.nq);
-  } else {
-    attn_mma_kernel<64><<<grid, NWARP * 32, sizeof(Smem<64>), st>>>(a, out);
-    count_launch();
-    if ((err = cudaGetLastError()) != cudaSuccess || a.splits == 1) return err;
-    attn_merge_kernel<64><<<dim3(a.rows, a.nq), 64, 0, st>>>(out, a.o_part, a.ml, a.splits, a.rows, a.nq);
+    err = launch_k(attn_mma_kernel<128>, grid, NWARP * 32, sizeof(Smem<128>), st, a, out);
+    if (err != cudaSuccess || a.splits == 1) return err;
+    return launch_k(attn_merge_kernel<128>, dim3(a.rows, a.nq), 128, 0, st, out, (const float*)a.o_part,
+                    (const float2*)a.ml, a.splits, a.rows, a.nq);
   }
-  count_launch();
-  return cudaGetLastError();
+  err = launch_k(attn_mma_kernel<64>, grid, NWARP * 32, sizeof(Smem<64>), st, a, out);
+  if (err != cudaSuccess || a.splits == 1) return err;
+  return launch_k(attn_merge_kernel<64>, dim3(a.rows, a.nq), 64, 0, st, out, (const float*)a.o_part,
+                  (const float2*)a.ml, a.splits, a.rows, a.nq);
 }
 
 }  // namespace fpd

@@ -12,6 +12,8 @@ namespace {
 constexpr int TM = 64, TN = 64, TK = 32;
 
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -71,9 +73,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
 cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
   dim3 grid(ceil_div(g.N, TN), ceil_div(g.M, TM), ceil_div(g.K, g.k_split));
-  gemm_simt_kernel<<<grid, 256, 0, st>>>(g);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(gemm_simt_kernel, grid, 256, 0, st, g);
 }
 
 }  // namespace fpd

@@ -50,6 +50,8 @@ struct TcParams {
   // EPI_ARGMAX
   const int4* items;             // (range, first id, first sorted row, row count)
   const int* n_items;
+  int implicit_rowtiles;         // > 0: unconstrained vocabulary, item t = (id tile t / rowtiles, row tile t % rowtiles)
+  int implicit_total;
   int hi_tab[FPD_MAX_RANGES];    // end (exclusive) of every legal id range
   unsigned long long* packed;    // [sorted rows]
   const int* rows_sorted;        // sorted row -> original row (logits only)
@@ -60,11 +62,14 @@ struct TcParams {
   int F;
 };
 
-template <int BN>
+// A pipeline stage holds KS consecutive 64-element K atoms of both operands: [A atoms][B atoms].  Several
+// atoms per stage make the TMA unit request KS adjacent 128-byte pieces of every weight row back to back.
+template <int BN, int KS>
 struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int A_ATOM = BM * BK * 2;   // 128 rows x 128 B
+  static constexpr int B_ATOM = BN * BK * 2;
+  static constexpr int A_BYTES = KS * A_ATOM;
+  static constexpr int STAGE_BYTES = KS * (A_ATOM + B_ATOM);
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;   // two accumulator buffers
 };
 // shared memory the SwiGLU epilogue uses to hand the up-projection values from the warps holding TMEM lanes
@@ -76,13 +81,13 @@ constexpr int xch_bytes() {
 
 struct Work {
   int a_row0, b_row0;   // first row of the 128-row (A) and BN-row (B) operand tiles
-  int k0, nkb;          // first K element and number of BK blocks
+  int k0, k1, nkb;      // K range [k0, k1) and number of pipeline stages it takes
   int split;
   int range;            // EPI_ARGMAX: range index; rows valid below `b_cnt`
   int b_cnt;
 };
 
-template <bool SWAP, int BN, int EPI>
+template <bool SWAP, int BN, int EPI, int KS>
 __device__ __forceinline__ bool get_work(const TcParams& p, int t, int total, Work& w) {
   if (t >= total) return false;
   if (EPI != EPI_ARGMAX) {
@@ -91,26 +96,35 @@ __device__ __forceinline__ bool get_work(const TcParams& p, int t, int total, Wo
     w.b_row0 = qi * ((EPI == EPI_SWIGLU && !SWAP) ? BN / 2 : BN);
     w.split = s;
     w.k0 = s * p.k_split;
-    const int k1 = min(p.K, w.k0 + p.k_split);
-    w.nkb = (k1 - w.k0) / BK;
+    w.k1 = min(p.K, w.k0 + p.k_split);
+    w.nkb = (w.k1 - w.k0 + KS * BK - 1) / (KS * BK);
     w.range = 0;
     w.b_cnt = BN;
   } else {
-    const int4 it = p.items[t];
-    w.range = it.x;
-    w.a_row0 = it.y;
-    w.b_row0 = it.z;
-    w.b_cnt = it.w;
+    if (p.implicit_rowtiles > 0) {
+      const int ct = t / p.implicit_rowtiles, rt = t % p.implicit_rowtiles;
+      w.range = 0;
+      w.a_row0 = ct * BM;
+      w.b_row0 = rt * BN;
+      w.b_cnt = min(BN, p.M - rt * BN);
+    } else {
+      const int4 it = p.items[t];
+      w.range = it.x;
+      w.a_row0 = it.y;
+      w.b_row0 = it.z;
+      w.b_cnt = it.w;
+    }
     w.split = 0;
     w.k0 = 0;
-    w.nkb = p.K / BK;
+    w.k1 = p.K;
+    w.nkb = (p.K + KS * BK - 1) / (KS * BK);
   }
   return true;
 }
 
-template <int BN, int STAGES, bool SWAP, int EPI>
+template <int BN, int STAGES, bool SWAP, int EPI, int KS>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, KS>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xch = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
@@ -122,7 +136,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                  tempty0 = tfull0 + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int total = (EPI != EPI_ARGMAX) ? p.pt * p.qt * p.splits : *p.n_items;
+  pdl_trigger();
+  // weight tiles never depend on earlier kernels, so the producer may fetch the first ring of them before
+  // waiting for the predecessor grid; everything else (activations, item lists, outputs) comes after pdl_wait
+  const bool explicit_items = EPI == EPI_ARGMAX && p.implicit_rowtiles == 0;
+  if (explicit_items) pdl_wait();
+  const int total = EPI != EPI_ARGMAX ? p.pt * p.qt * p.splits : (explicit_items ? *p.n_items : p.implicit_total);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; s++) {
@@ -152,40 +171,67 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      // weight / activation atoms of one stage; the stage's bytes are expected on its full barrier first
+      auto load_w = [&](uint32_t sa, const Work& w, int k, int natoms, uint32_t fb) {
+        for (int a = 0; a < natoms; a++) {
+          const int ka = k + a * BK;
+          if (EPI == EPI_SWIGLU) {   // weight atom = [gate rows f0.. ; up rows F+f0..], two half boxes
+            const uint32_t dst = SWAP ? sa + a * C::A_ATOM : sa + C::A_BYTES + a * C::B_ATOM;
+            const int half = SWAP ? C::A_ATOM / 2 : C::B_ATOM / 2;
+            const int f0 = SWAP ? w.a_row0 : w.b_row0;
+            tc::tma_load_2d(dst, &p.tm_w, ka, f0, fb);
+            tc::tma_load_2d(dst + half, &p.tm_w, ka, p.F + f0, fb);
+          } else if (SWAP) {
+            tc::tma_load_2d(sa + a * C::A_ATOM, &p.tm_w, ka, w.a_row0, fb);
+          } else {
+            tc::tma_load_2d(sa + C::A_BYTES + a * C::B_ATOM, &p.tm_w, ka, w.b_row0, fb);
+          }
+        }
+      };
+      auto load_x = [&](uint32_t sa, const Work& w, int k, int natoms, uint32_t fb) {
+        for (int a = 0; a < natoms; a++) {
+          const int ka = k + a * BK;
+          const int seg = ka / p.seg_k, kx = ka - seg * p.seg_k;
+          if (SWAP)
+            tc::tma_load_2d(sa + C::A_BYTES + a * C::B_ATOM, &p.tm_x[seg], kx, w.b_row0, fb);
+          else
+            tc::tma_load_2d(sa + a * C::A_ATOM, &p.tm_x[seg], kx, w.a_row0, fb);
+        }
+      };
+      auto atoms = [&](const Work& w, int kb) { return min(KS, (w.k1 - (w.k0 + kb * KS * BK)) / BK); };
+      int pre = 0;
+      Work w0;
+      if (!explicit_items && get_work<SWAP, BN, EPI, KS>(p, blockIdx.x, total, w0)) {
+        pre = min(STAGES, w0.nkb);
+        for (int kb = 0; kb < pre; kb++) {   // fresh ring: the empty barriers need no wait
+          const uint32_t fb = full0 + 8 * kb;
+          const int na = atoms(w0, kb);
+          tc::mbar_arrive_expect_tx(fb, na * (C::A_ATOM + C::B_ATOM));
+          load_w(tc::smem_u32(smem + kb * C::STAGE_BYTES), w0, w0.k0 + kb * KS * BK, na, fb);
+        }
+      }
+      if (!explicit_items) pdl_wait();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
+      bool first = true;
       Work w;
-      for (int t = blockIdx.x; get_work<SWAP, BN, EPI>(p, t, total, w) && !*abort_flag; t += gridDim.x) {
+      for (int t = blockIdx.x; get_work<SWAP, BN, EPI, KS>(p, t, total, w) && !*abort_flag; t += gridDim.x) {
         for (int kb = 0; kb < w.nkb; kb++) {
-          if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1)) { *abort_flag = 1; break; }
           const uint32_t fb = full0 + 8 * stage;
-          tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint32_t sb = sa + C::A_BYTES;
-          const int k = w.k0 + kb * BK;
-          const int seg = k / p.seg_k, kx = k - seg * p.seg_k;
-          if (EPI == EPI_SWIGLU) {
-            // weight tile = [gate rows f0.. ; up rows F+f0..], two boxes of half the tile each
-            if (SWAP) {
-              tc::tma_load_2d(sa, &p.tm_w, k, w.a_row0, fb);
-              tc::tma_load_2d(sa + C::A_BYTES / 2, &p.tm_w, k, p.F + w.a_row0, fb);
-              tc::tma_load_2d(sb, &p.tm_x[seg], kx, w.b_row0, fb);
-            } else {
-              tc::tma_load_2d(sa, &p.tm_x[seg], kx, w.a_row0, fb);
-              tc::tma_load_2d(sb, &p.tm_w, k, w.b_row0, fb);
-              tc::tma_load_2d(sb + C::B_BYTES / 2, &p.tm_w, k, p.F + w.b_row0, fb);
-            }
-          } else if (SWAP) {
-            tc::tma_load_2d(sa, &p.tm_w, k, w.a_row0, fb);
-            tc::tma_load_2d(sb, &p.tm_x[seg], kx, w.b_row0, fb);
-          } else {
-            tc::tma_load_2d(sa, &p.tm_x[seg], kx, w.a_row0, fb);
-            tc::tma_load_2d(sb, &p.tm_w, k, w.b_row0, fb);
+          const int k = w.k0 + kb * KS * BK;
+          const int na = atoms(w, kb);
+          if (!(first && kb < pre)) {
+            if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1)) { *abort_flag = 1; break; }
+            tc::mbar_arrive_expect_tx(fb, na * (C::A_ATOM + C::B_ATOM));
+            load_w(sa, w, k, na, fb);
           }
+          load_x(sa, w, k, na, fb);
           issued++;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
+        first = false;
       }
       if (*abort_flag) {
         // let the copies already issued land before the CTA can exit (bounded)
@@ -203,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       uint32_t phase = 0;
       int it = 0;
       Work w;
-      for (int t = blockIdx.x; get_work<SWAP, BN, EPI>(p, t, total, w); t += gridDim.x, it++) {
+      for (int t = blockIdx.x; get_work<SWAP, BN, EPI, KS>(p, t, total, w); t += gridDim.x, it++) {
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -214,11 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
+          const int na = min(KS, (w.k1 - (w.k0 + kb * KS * BK)) / BK);
+          for (int a = 0; a < na; a++) {
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; kk++) {
-            const uint64_t da = tc::sw128_kmajor_desc(sa + kk * UMMA_K * 2);
-            const uint64_t db = tc::sw128_kmajor_desc(sb + kk * UMMA_K * 2);
-            tc::umma_bf16(d_tmem, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / UMMA_K; kk++) {
+              const uint64_t da = tc::sw128_kmajor_desc(sa + a * C::A_ATOM + kk * UMMA_K * 2);
+              const uint64_t db = tc::sw128_kmajor_desc(sb + a * C::B_ATOM + kk * UMMA_K * 2);
+              tc::umma_bf16(d_tmem, da, db, idesc, (kb > 0 || a > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           tc::umma_commit(empty0 + 8 * stage);   // frees the stage once these MMAs have read it
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -228,11 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
   } else {
     // ---------------- epilogue: warps 2..5 ----------------
+    if (!explicit_items) pdl_wait();            // outputs may still be read by the predecessor until it completes
     const int quarter = warp & 3;               // TMEM lanes [32*quarter, 32*quarter + 32)
     const int row_in_tile = quarter * 32 + lane;
     int it = 0;
     Work w;
-    for (int t = blockIdx.x; get_work<SWAP, BN, EPI>(p, t, total, w); t += gridDim.x, it++) {
+    for (int t = blockIdx.x; get_work<SWAP, BN, EPI, KS>(p, t, total, w); t += gridDim.x, it++) {
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if (!tc::mbar_wait(tfull0 + 8 * acc, acc_phase)) *abort_flag = 1;
@@ -392,31 +442,58 @@ cudaError_t make_tmap(CUtensorMap* tm, const void* ptr, int rows, int cols, int 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int BN, int STAGES, bool SWAP, int EPI>
+template <int BN, int STAGES, bool SWAP, int EPI, int KS>
 constexpr size_t smem_bytes() {
-  return (size_t)STAGES * Cfg<BN>::STAGE_BYTES + xch_bytes<BN, SWAP, EPI>() + 1024 + 256;
+  return (size_t)STAGES * Cfg<BN, KS>::STAGE_BYTES + xch_bytes<BN, SWAP, EPI>() + 1024 + 256;
 }
 
-template <int BN, int STAGES, bool SWAP, int EPI>
+template <int BN, int STAGES, bool SWAP, int EPI, int KS = 1>
 cudaError_t set_attr() {
-  static_assert(smem_bytes<BN, STAGES, SWAP, EPI>() <= 227 * 1024, "shared memory");
-  return cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, SWAP, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes<BN, STAGES, SWAP, EPI>());
+  static_assert(smem_bytes<BN, STAGES, SWAP, EPI, KS>() <= 227 * 1024, "shared memory");
+  return cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, SWAP, EPI, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<BN, STAGES, SWAP, EPI, KS>());
 }
 
-template <int BN, int STAGES, bool SWAP, int EPI>
+template <int BN, int STAGES, bool SWAP, int EPI, int KS = 1>
 cudaError_t launch_kernel(const TcParams& p, int grid, cudaStream_t st) {
-  tc_gemm_kernel<BN, STAGES, SWAP, EPI><<<grid, kThreads, smem_bytes<BN, STAGES, SWAP, EPI>(), st>>>(p);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(tc_gemm_kernel<BN, STAGES, SWAP, EPI, KS>, grid, kThreads, smem_bytes<BN, STAGES, SWAP, EPI, KS>(),
+                  st, p);
 }
 
+// Pipeline shapes of the few-token (weight-tile) kernels with 16-token tiles: (atoms per stage, stages,
+// CTAs per SM).  Entry 0 is the production choice; the others exist for tuning sweeps (fpd_test_set_variant).
+struct SwapVariant {
+  int ks, stages, ctas_per_sm;
+};
+constexpr SwapVariant kSwapVariants[] = {{1, 6, 2}, {2, 6, 1}, {4, 3, 1}, {2, 3, 2}, {1, 12, 1}};
+int g_swap_variant = 0;
+
+template <int EPI>
+cudaError_t launch_swap16(const TcParams& p, int grid, cudaStream_t st) {
+  switch (g_swap_variant) {
+    case 1: return launch_kernel<16, 6, true, EPI, 2>(p, grid, st);
+    case 2: return launch_kernel<16, 3, true, EPI, 4>(p, grid, st);
+    case 3: return launch_kernel<16, 3, true, EPI, 2>(p, grid, st);
+    case 4: return launch_kernel<16, 12, true, EPI, 1>(p, grid, st);
+    default: return launch_kernel<16, 6, true, EPI, 1>(p, grid, st);
+  }
+}
 }  // namespace
+
+void tc_set_swap_variant(int v) { g_swap_variant = (v >= 0 && v < 5) ? v : 0; }
 
 // Opt every instantiation into its shared-memory size once, outside any stream capture (fpd_model_create).
 cudaError_t tc_init_attributes() {
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = set_attr<16, 6, true, EPI_STORE>();
+  if (e == cudaSuccess) e = set_attr<16, 6, true, EPI_STORE, 2>();
+  if (e == cudaSuccess) e = set_attr<16, 3, true, EPI_STORE, 4>();
+  if (e == cudaSuccess) e = set_attr<16, 3, true, EPI_STORE, 2>();
+  if (e == cudaSuccess) e = set_attr<16, 12, true, EPI_STORE, 1>();
+  if (e == cudaSuccess) e = set_attr<16, 6, true, EPI_ARGMAX, 2>();
+  if (e == cudaSuccess) e = set_attr<16, 3, true, EPI_ARGMAX, 4>();
+  if (e == cudaSuccess) e = set_attr<16, 3, true, EPI_ARGMAX, 2>();
+  if (e == cudaSuccess) e = set_attr<16, 12, true, EPI_ARGMAX, 1>();
   if (e == cudaSuccess) e = set_attr<32, 5, true, EPI_STORE>();
   if (e == cudaSuccess) e = set_attr<64, 4, true, EPI_STORE>();
   if (e == cudaSuccess) e = set_attr<128, 6, false, EPI_STORE>();
@@ -440,7 +517,7 @@ TcPlan tc_plan_gemm(int M, int N, int K, int num_sms) {
     pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     pl.pt = ceil_div(N, BM);
     pl.qt = ceil_div(M, pl.bn);
-    ctas_per_sm = 2;
+    ctas_per_sm = pl.bn == 16 ? kSwapVariants[g_swap_variant].ctas_per_sm : 2;
   } else {
     pl.swap = false;
     pl.bn = N >= 1024 ? 256 : 128;
@@ -473,7 +550,7 @@ TcPlan tc_plan_force(int M, int N, int K, int num_sms, int placement) {
     pl.pt = ceil_div(M, BM);
     pl.qt = ceil_div(N, pl.bn);
   }
-  const int slots = num_sms * (pl.swap ? 2 : 1);
+  const int slots = num_sms * (pl.swap ? (pl.bn == 16 ? kSwapVariants[g_swap_variant].ctas_per_sm : 2) : 1);
   const int tiles = pl.pt * pl.qt;
   int splits = 1;
   if (tiles < slots) splits = std::max(1, std::min(slots / tiles, nkb / 4));
@@ -486,6 +563,8 @@ TcPlan tc_plan_force(int M, int N, int K, int num_sms, int placement) {
 
 namespace {
 __global__ void sum_splits_kernel(float* __restrict__ out, const float* __restrict__ part, int splits, size_t n) {
+  pdl_trigger();
+  pdl_wait();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
     float a = 0.f;
     for (int s = 0; s < splits; s++) a += part[s * n + i];
@@ -495,9 +574,7 @@ __global__ void sum_splits_kernel(float* __restrict__ out, const float* __restri
 }  // namespace
 
 cudaError_t launch_sum_splits(float* out, const float* part, int splits, size_t n, cudaStream_t st) {
-  sum_splits_kernel<<<(int)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st>>>(out, part, splits, n);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(sum_splits_kernel, (int)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st, out, part, splits, n);
 }
 
 cudaError_t launch_tc_gemm(const GemmArgs& g, const TcPlan& pl, cudaStream_t st) {
@@ -526,7 +603,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, const TcPlan& pl, cudaStream_t st)
   p.splits = pl.splits;
   p.k_split = pl.k_split;
   if (pl.swap) {
-    if (pl.bn == 16) return launch_kernel<16, 6, true, EPI_STORE>(p, pl.grid, st);
+    if (pl.bn == 16) return launch_swap16<EPI_STORE>(p, pl.grid, st);
     if (pl.bn == 32) return launch_kernel<32, 5, true, EPI_STORE>(p, pl.grid, st);
     return launch_kernel<64, 4, true, EPI_STORE>(p, pl.grid, st);
   }
@@ -589,7 +666,7 @@ int tc_lm_row_tile(int n_rows) { return n_rows <= 16 ? 16 : (n_rows <= 32 ? 32 :
 
 cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows, const bf16* W, int d, int V,
                              const int4* items, const int* n_items, int max_items, unsigned long long* packed,
-                             const int* rows_sorted, float* logits, int num_sms, cudaStream_t st) {
+                             const int* rows_sorted, float* logits, int num_sms, bool unconstrained, cudaStream_t st) {
   if (d % BK) return cudaErrorInvalidValue;
   const int bn = lp.rt;
   TcParams p;
@@ -605,13 +682,19 @@ cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows,
   p.K = d;
   p.items = items;
   p.n_items = n_items;
+  if (lp.n_class == 1 && lp.n_range == 1 && lp.range_lo[0] == 0 && lp.range_hi[0] == V && unconstrained) {
+    p.implicit_rowtiles = ceil_div(n_rows, bn);
+    p.implicit_total = p.implicit_rowtiles * ceil_div(V, BM);
+  }
   for (int q = 0; q < lp.n_range; q++) p.hi_tab[q] = lp.range_hi[q];
   p.packed = packed;
   p.rows_sorted = rows_sorted;
   p.logits = logits;
   p.V = V;
-  const int grid = std::max(1, std::min(max_items, 2 * num_sms));
-  if (bn == 16) return launch_kernel<16, 6, true, EPI_ARGMAX>(p, grid, st);
+  const int n_work = p.implicit_rowtiles > 0 ? p.implicit_total : max_items;
+  const int per_sm = bn == 16 ? kSwapVariants[g_swap_variant].ctas_per_sm : 2;
+  const int grid = std::max(1, std::min(n_work, per_sm * num_sms));
+  if (bn == 16) return launch_swap16<EPI_ARGMAX>(p, grid, st);
   if (bn == 32) return launch_kernel<32, 5, true, EPI_ARGMAX>(p, grid, st);
   return launch_kernel<64, 4, true, EPI_ARGMAX>(p, grid, st);
 }

@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(1024) lm_plan_kernel(LmPlan p, const int16_t* 
                                                         int* __restrict__ class_row_off, int4* __restrict__ items,
                                                         int* __restrict__ n_items,
                                                         unsigned long long* __restrict__ packed, int max_items) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int warp_tot[32];
   __shared__ int s_total;
   __shared__ int s_off[FPD_MAX_CLASSES + 1];
@@ -114,15 +116,15 @@ __global__ void __launch_bounds__(1024) lm_plan_kernel(LmPlan p, const int16_t* 
 cudaError_t launch_lm_plan(const LmPlan& p, const int16_t* pos_class, int* rows_sorted, int* inv_sorted,
                            int* class_row_off, int4* items, int* n_items, unsigned long long* packed, int max_items,
                            cudaStream_t st) {
-  lm_plan_kernel<<<1, 1024, 0, st>>>(p, pos_class, rows_sorted, inv_sorted, class_row_off, items, n_items, packed,
-                                     max_items);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(lm_plan_kernel, 1, 1024, 0, st, p, pos_class, rows_sorted, inv_sorted, class_row_off, items, n_items,
+                  packed, max_items);
 }
 
 // ---- final RMSNorm into sorted order -------------------------------------------------------------------------------
 __global__ void rmsnorm_gather_kernel(bf16* __restrict__ out, const bf16* __restrict__ in, const bf16* __restrict__ g,
                                       const int* __restrict__ rows_sorted, int d, float eps, int L) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int i = blockIdx.x;
   const int r = rows_sorted[i];
@@ -164,14 +166,14 @@ __global__ void rmsnorm_gather_kernel(bf16* __restrict__ out, const bf16* __rest
 cudaError_t launch_rmsnorm_gather(bf16* out, const bf16* in, const bf16* g, const int* rows_sorted, int rows, int d,
                                   float eps, int L, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  rmsnorm_gather_kernel<<<rows, 256, 0, st>>>(out, in, g, rows_sorted, d, eps, L);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(rmsnorm_gather_kernel, rows, 256, 0, st, out, in, g, rows_sorted, d, eps, L);
 }
 
 // ---- decode the packed argmax words into ids ---------------------------------------------------------------------
 __global__ void lm_decode_kernel(int32_t* __restrict__ tokens, const unsigned long long* __restrict__ packed,
                                  const int* __restrict__ inv_sorted, int n) {
+  pdl_trigger();
+  pdl_wait();
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) {
     const int i = inv_sorted[r];
     const unsigned long long p = i >= 0 ? packed[i] : 0ull;
@@ -183,9 +185,7 @@ __global__ void lm_decode_kernel(int32_t* __restrict__ tokens, const unsigned lo
 cudaError_t launch_lm_decode(int32_t* tokens, const unsigned long long* packed, const int* inv_sorted, int n,
                              cudaStream_t st) {
   const int grid = std::min(ceil_div(n, 256), 1024);
-  lm_decode_kernel<<<grid, 256, 0, st>>>(tokens, packed, inv_sorted, n);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(lm_decode_kernel, grid, 256, 0, st, tokens, packed, inv_sorted, n);
 }
 
 }  // namespace fpd

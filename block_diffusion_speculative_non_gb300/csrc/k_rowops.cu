@@ -27,6 +27,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // ---- RMSNorm of fp32 split-K partial sums -> bf16 (fused context) -------------------------------------------------
 __global__ void rmsnorm_partials_kernel(bf16* __restrict__ out, const float* __restrict__ part, int nsplit,
                                         size_t split_stride, const bf16* __restrict__ g, int d, float eps) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int r = blockIdx.x;
   float ss = 0.f;
@@ -46,9 +48,7 @@ __global__ void rmsnorm_partials_kernel(bf16* __restrict__ out, const float* __r
 cudaError_t launch_rmsnorm_partials(bf16* out, const float* part, int nsplit, size_t split_stride, const bf16* g,
                                     int rows, int d, float eps, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  rmsnorm_partials_kernel<<<rows, 256, 0, st>>>(out, part, nsplit, split_stride, g, d, eps);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(rmsnorm_partials_kernel, rows, 256, 0, st, out, part, nsplit, split_stride, g, d, eps);
 }
 
 // ---- per-head RMSNorm + rotate-half RoPE on a warp's head ----------------------------------------------------------
@@ -86,16 +86,26 @@ __global__ void qkv_post_kernel(bf16* __restrict__ q_out, bf16* __restrict__ kbl
                                 const bf16* __restrict__ q_norm, const bf16* __restrict__ k_norm,
                                 const float2* __restrict__ rope, const int32_t* __restrict__ ctx_len, int t_cap,
                                 int L, int nq, int nkv, float eps) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int NV = H / 32;
   const int r = blockIdx.x, hd = blockIdx.y, lane = threadIdx.x;
   const int b = r / L, j = r % L;
   const int ncol = (nq + 2 * nkv) * H;
   float v[NV];
 #pragma unroll
-  for (int k = 0; k < NV; k++) {
-    float a = 0.f;
-    for (int s = 0; s < nsplit; s++) a += part[s * split_stride + (size_t)r * ncol + hd * H + lane + 32 * k];
-    v[k] = a;
+  for (int k = 0; k < NV; k++) v[k] = 0.f;
+  const float* pr = part + (size_t)r * ncol + hd * H + lane;
+  for (int s0 = 0; s0 < nsplit; s0 += 4) {
+    float t[4][NV];
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int k = 0; k < NV; k++) t[u][k] = s0 + u < nsplit ? __ldcg(pr + (size_t)(s0 + u) * split_stride + 32 * k) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int k = 0; k < NV; k++) v[k] += t[u][k];
   }
   int cl = ctx_len[b];
   cl = cl < 0 ? 0 : (cl > t_cap ? t_cap : cl);
@@ -119,13 +129,10 @@ cudaError_t launch_qkv_post(bf16* q, bf16* kblk, bf16* vblk, const float* part, 
                             int t_cap, int B, int L, int nq, int nkv, int h, float eps, cudaStream_t st) {
   dim3 grid(B * L, nq + 2 * nkv);
   if (h == 128)
-    qkv_post_kernel<128><<<grid, 32, 0, st>>>(q, kblk, vblk, part, nsplit, split_stride, q_norm, k_norm, rope,
-                                              ctx_len, t_cap, L, nq, nkv, eps);
-  else
-    qkv_post_kernel<64><<<grid, 32, 0, st>>>(q, kblk, vblk, part, nsplit, split_stride, q_norm, k_norm, rope,
-                                             ctx_len, t_cap, L, nq, nkv, eps);
-  count_launch();
-  return cudaGetLastError();
+    return launch_k(qkv_post_kernel<128>, grid, 32, 0, st, q, kblk, vblk, part, nsplit, split_stride, q_norm, k_norm,
+                    rope, ctx_len, t_cap, L, nq, nkv, eps);
+  return launch_k(qkv_post_kernel<64>, grid, 32, 0, st, q, kblk, vblk, part, nsplit, split_stride, q_norm, k_norm,
+                  rope, ctx_len, t_cap, L, nq, nkv, eps);
 }
 
 // ---- a2 epilogue: context K (k-norm + RoPE at its context position) and V into the KV store -----------------------
@@ -136,6 +143,8 @@ __global__ void kv_post_kernel(bf16* __restrict__ store, const float* __restrict
                                size_t split_stride, const bf16* __restrict__ k_norm, const float2* __restrict__ rope,
                                const int32_t* __restrict__ row_off, const int32_t* __restrict__ pos_start, int batch,
                                int layer, int t_cap, int row0, int nkv, float eps) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int NV = H / 32;
   const int r = blockIdx.x, hd = blockIdx.y, lane = threadIdx.x;
   const int grow = row0 + r;
@@ -168,13 +177,10 @@ cudaError_t launch_kv_post(bf16* store, const float* part, int nsplit, size_t sp
   if (rows <= 0) return cudaSuccess;
   dim3 grid(rows, 2 * nkv);
   if (h == 128)
-    kv_post_kernel<128><<<grid, 32, 0, st>>>(store, part, nsplit, split_stride, k_norm, rope, row_off, pos_start,
-                                             batch, layer, t_cap, row0, nkv, eps);
-  else
-    kv_post_kernel<64><<<grid, 32, 0, st>>>(store, part, nsplit, split_stride, k_norm, rope, row_off, pos_start,
-                                            batch, layer, t_cap, row0, nkv, eps);
-  count_launch();
-  return cudaGetLastError();
+    return launch_k(kv_post_kernel<128>, grid, 32, 0, st, store, part, nsplit, split_stride, k_norm, rope, row_off,
+                    pos_start, batch, layer, t_cap, row0, nkv, eps);
+  return launch_k(kv_post_kernel<64>, grid, 32, 0, st, store, part, nsplit, split_stride, k_norm, rope, row_off,
+                  pos_start, batch, layer, t_cap, row0, nkv, eps);
 }
 
 // ---- residual add fused with the next RMSNorm: one block per row ------------------------------------------------
@@ -183,9 +189,30 @@ cudaError_t launch_kv_post(bf16* store, const float* part, int nsplit, size_t sp
 template <int VPT>
 __global__ void residual_norm_kernel(bf16* __restrict__ x, bf16* __restrict__ xn, const float* __restrict__ part,
                                      int nsplit, size_t split_stride, const bf16* __restrict__ g, int d, float eps) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int r = blockIdx.x;
   bf16* xr = x + (size_t)r * d;
+  const float* pr = part + (size_t)r * d;
+  float acc[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; k++) acc[k] = 0.f;
+  // split-K partials: four splits' loads in flight at once, summed in split order (bit-reproducible)
+  for (int s0 = 0; s0 < nsplit; s0 += 4) {
+    float t[4][VPT];
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int k = 0; k < VPT; k++) {
+        const int i = threadIdx.x + k * blockDim.x;
+        t[u][k] = (s0 + u < nsplit && i < d) ? __ldcg(pr + (size_t)(s0 + u) * split_stride + i) : 0.f;
+      }
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int k = 0; k < VPT; k++) acc[k] += t[u][k];
+  }
   float v[VPT];
   float ss = 0.f;
 #pragma unroll
@@ -193,10 +220,7 @@ __global__ void residual_norm_kernel(bf16* __restrict__ x, bf16* __restrict__ xn
     const int i = threadIdx.x + k * blockDim.x;
     v[k] = 0.f;
     if (i < d) {
-      float a = __bfloat162float(xr[i]);
-      float acc = 0.f;
-      for (int s = 0; s < nsplit; s++) acc += part[s * split_stride + (size_t)r * d + i];
-      const bf16 nb = __float2bfloat16_rn(a + acc);
+      const bf16 nb = __float2bfloat16_rn(__bfloat162float(xr[i]) + acc[k]);
       xr[i] = nb;
       v[k] = __bfloat162float(nb);
       ss += v[k] * v[k];
@@ -214,20 +238,17 @@ __global__ void residual_norm_kernel(bf16* __restrict__ x, bf16* __restrict__ xn
 cudaError_t launch_residual_norm(bf16* x, bf16* xn, const float* part, int nsplit, size_t split_stride, const bf16* g,
                                  int rows, int d, float eps, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  if (d <= 256 * 4)
-    residual_norm_kernel<4><<<rows, 256, 0, st>>>(x, xn, part, nsplit, split_stride, g, d, eps);
-  else if (d <= 512 * 8)
-    residual_norm_kernel<8><<<rows, 512, 0, st>>>(x, xn, part, nsplit, split_stride, g, d, eps);
-  else
-    residual_norm_kernel<16><<<rows, 1024, 0, st>>>(x, xn, part, nsplit, split_stride, g, d, eps);
-  count_launch();
-  return cudaGetLastError();
+  if (d <= 256 * 4) return launch_k(residual_norm_kernel<4>, rows, 256, 0, st, x, xn, part, nsplit, split_stride, g, d, eps);
+  if (d <= 512 * 8) return launch_k(residual_norm_kernel<8>, rows, 512, 0, st, x, xn, part, nsplit, split_stride, g, d, eps);
+  return launch_k(residual_norm_kernel<16>, rows, 1024, 0, st, x, xn, part, nsplit, split_stride, g, d, eps);
 }
 
 // ---- embedding gather fused with the first RMSNorm ----------------------------------------------------------------
 __global__ void embed_norm_kernel(bf16* __restrict__ x, bf16* __restrict__ xn, const bf16* __restrict__ embed,
                                   const int32_t* __restrict__ anchor, int32_t mask_id, const bf16* __restrict__ g,
                                   int L, int d, int V, float eps) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int r = blockIdx.x, b = r / L, j = r % L;
   int id = j == 0 ? anchor[b] : mask_id;
@@ -265,9 +286,7 @@ __global__ void embed_norm_kernel(bf16* __restrict__ x, bf16* __restrict__ xn, c
 
 cudaError_t launch_embed_norm(bf16* x, bf16* xn, const bf16* embed, const int32_t* anchor, int32_t mask_id,
                               const bf16* g, int B, int L, int d, int V, float eps, cudaStream_t st) {
-  embed_norm_kernel<<<B * L, 256, 0, st>>>(x, xn, embed, anchor, mask_id, g, L, d, V, eps);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(embed_norm_kernel, B * L, 256, 0, st, x, xn, embed, anchor, mask_id, g, L, d, V, eps);
 }
 
 }  // namespace fpd

@@ -21,6 +21,8 @@ __global__ void verify_kernel(int mode, int B, int L, const int32_t* __restrict_
                               const int16_t* __restrict__ pos_class, const int8_t* __restrict__ rule, int32_t pad_id,
                               int32_t* __restrict__ accept, int32_t* __restrict__ committed,
                               int32_t* __restrict__ valid) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -78,10 +80,8 @@ __global__ void verify_kernel(int mode, int B, int L, const int32_t* __restrict_
 cudaError_t launch_verify(int mode, int B, int L, const int32_t* draft, const int32_t* target, const VerifyTables& tb,
                           const int16_t* pos_class, const int8_t* rule, int32_t pad_id, int32_t* accept,
                           int32_t* committed, int32_t* valid, cudaStream_t st) {
-  verify_kernel<<<ceil_div(B, 4), 128, 0, st>>>(mode, B, L, draft, target, tb, pos_class, rule, pad_id, accept,
-                                                committed, valid);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(verify_kernel, ceil_div(B, 4), 128, 0, st, mode, B, L, draft, target, tb, pos_class, rule, pad_id,
+                  accept, committed, valid);
 }
 
 }  // namespace fpd

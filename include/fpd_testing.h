@@ -26,6 +26,12 @@ size_t fpd_test_gemm_workspace_bytes(int M, int N, int K);
  * tiles above).  Asynchronous on stream. */
 fpd_status fpd_test_swiglu(int M, int F, int K, const void* X, const void* W, void* hmid, void* stream);
 
+/* Selects the pipeline shape of the 16-token weight-tile GEMM kernels for tuning sweeps: 0 (default) = one
+ * 64-element K atom per stage, 6 stages, 2 CTAs per SM; 1 = 2 atoms x 6 stages, 1 CTA/SM; 2 = 4 atoms x 3 stages,
+ * 1 CTA/SM; 3 = 2 atoms x 3 stages, 2 CTAs/SM; 4 = 1 atom x 12 stages, 1 CTA/SM.  Affects plans (and so
+ * workspace sizes) made afterwards: set it before fpd_workspace_bytes. */
+void fpd_test_set_variant(int variant);
+
 #ifdef __cplusplus
 }
 #endif

@@ -84,3 +84,16 @@ def test_tc_swiglu(lib, M, F, K):
     ref = torch.nn.functional.silu(gu[:, :F]) * gu[:, F:]
     err = ((H.float() - ref).abs() / (ref.abs() + 1e-3 * ref.abs().max())).max().item()
     assert err < 1e-2, err
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
+@pytest.mark.parametrize("M,N,K", [(15, 6144, 2560), (16, 300, 320), (9, 1000, 704)])
+def test_tc_gemm_pipeline_variants(lib, variant, M, N, K):
+    """The other pipeline shapes of the 16-token weight-tile kernel (several K atoms per stage, tail stages
+    with fewer atoms, 1 or 2 CTAs per SM) give the same products."""
+    lib.fpd_test_set_variant.argtypes = [ctypes.c_int]
+    lib.fpd_test_set_variant(variant)
+    try:
+        assert run(lib, 0, -1, M, N, K, seed=3) < 1e-5
+    finally:
+        lib.fpd_test_set_variant(0)
