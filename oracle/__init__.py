@@ -12,6 +12,7 @@ exhaustive enumeration, brute force on tiny inputs, numpy's library routines, de
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -54,32 +55,49 @@ class _OracleModel(ctypes.Structure):
 _lib = None
 
 
+def _configure(l):
+    """Declare the ctypes signatures of one build of the oracle."""
+    l.oracle_round_bf16.restype = ctypes.c_uint16
+    l.oracle_round_bf16.argtypes = [ctypes.c_double]
+    l.oracle_bf16_to_double.restype = ctypes.c_double
+    l.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    l.oracle_silu.restype = ctypes.c_double
+    l.oracle_silu.argtypes = [ctypes.c_double]
+    l.oracle_num_threads.restype = ctypes.c_int
+    l.oracle_rmsnorm.argtypes = [ctypes.c_int, _f64p, _u16p, ctypes.c_double, _f64p]
+    l.oracle_rope.argtypes = [ctypes.c_int, _f64p, ctypes.c_double, ctypes.c_double]
+    l.oracle_linear.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64p, _u16p, _f64p]
+    l.oracle_attention.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int, _u16p, _u16p,
+                                   ctypes.c_int, _f64p, _f64p, ctypes.c_double, _f64p]
+    l.oracle_prepare_context.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _i32p,
+                                         _i32p, ctypes.POINTER(_u16p), _u16p, ctypes.c_int]
+    l.oracle_draft_block.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
+                                     ctypes.c_int, _i32p, _i32p, ctypes.c_int32, _u16p, _u16p]
+    l.oracle_constrain_argmax.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
+                                          ctypes.c_int, _i32p, _i32p, _i16p, _i32p, _f64p, _f64p]
+    l.oracle_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _i32p, ctypes.c_int, _i32p,
+                                _i32p, _i16p, _i8p, ctypes.c_int32, _i32p, _i32p, _i32p]
+    return l
+
+
 def lib():
     global _lib
     if _lib is None:
-        l = ctypes.CDLL(build())
-        l.oracle_round_bf16.restype = ctypes.c_uint16
-        l.oracle_round_bf16.argtypes = [ctypes.c_double]
-        l.oracle_bf16_to_double.restype = ctypes.c_double
-        l.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
-        l.oracle_silu.restype = ctypes.c_double
-        l.oracle_silu.argtypes = [ctypes.c_double]
-        l.oracle_num_threads.restype = ctypes.c_int
-        l.oracle_rmsnorm.argtypes = [ctypes.c_int, _f64p, _u16p, ctypes.c_double, _f64p]
-        l.oracle_rope.argtypes = [ctypes.c_int, _f64p, ctypes.c_double, ctypes.c_double]
-        l.oracle_linear.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64p, _u16p, _f64p]
-        l.oracle_attention.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int, _u16p, _u16p,
-                                       ctypes.c_int, _f64p, _f64p, ctypes.c_double, _f64p]
-        l.oracle_prepare_context.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _i32p,
-                                             _i32p, ctypes.POINTER(_u16p), _u16p, ctypes.c_int]
-        l.oracle_draft_block.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
-                                         ctypes.c_int, _i32p, _i32p, ctypes.c_int32, _u16p, _u16p]
-        l.oracle_constrain_argmax.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
-                                              ctypes.c_int, _i32p, _i32p, _i16p, _i32p, _f64p, _f64p]
-        l.oracle_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _i32p, ctypes.c_int, _i32p,
-                                    _i32p, _i16p, _i8p, ctypes.c_int32, _i32p, _i32p, _i32p]
-        _lib = l
+        _lib = _configure(ctypes.CDLL(build()))
     return _lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Route every oracle call through another build of the oracle source (the pin tests use this to run a
+    copy with a deliberately planted mistake and check that the pins reject it), then restore the default."""
+    global _lib
+    saved = lib()
+    _lib = _configure(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        _lib = saved
 
 
 def num_threads() -> int:
