@@ -51,7 +51,8 @@ class VocabLayout(ctypes.Structure):
 
 _lib = None
 _EXPORTS = ["fpd_model_create", "fpd_model_destroy", "fpd_kv_store_bytes", "fpd_workspace_bytes",
-            "fpd_prepare_context", "fpd_draft_block", "fpd_constrain_argmax", "fpd_verify", "fpd_last_error",
+            "fpd_prepare_context", "fpd_draft_block", "fpd_constrain_argmax", "fpd_constrain_argmax_noalloc",
+            "fpd_verify", "fpd_last_error",
             "fpd_kernel_launches", "fpd_device_status"]
 
 
@@ -76,13 +77,15 @@ def lib():
                                       sz, vp]
         l.fpd_constrain_argmax.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.POINTER(VocabLayout), vp, vp,
                                            vp, sz, vp]
+        l.fpd_constrain_argmax_noalloc.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.POINTER(VocabLayout),
+                                                   vp, vp, vp]
         l.fpd_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, ctypes.POINTER(VocabLayout), vp,
                                  i32, vp, vp, vp, vp]
         l.fpd_last_error.restype = ctypes.c_char_p
         l.fpd_kernel_launches.restype = ctypes.c_uint64
         l.fpd_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         for f in ("fpd_model_create", "fpd_prepare_context", "fpd_draft_block", "fpd_constrain_argmax",
-                  "fpd_verify", "fpd_device_status"):
+                  "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_device_status"):
             getattr(l, f).restype = ctypes.c_int
         _lib = l
     return _lib
@@ -164,6 +167,14 @@ def fpd_constrain_argmax(model, batch, block_len, hidden, layout, tokens_out, lo
                                       ctypes.byref(layout) if layout is not None else None, _ptr(tokens_out),
                                       _ptr(logits_out), _ptr(workspace), workspace_bytes, _stream(stream)),
            "fpd_constrain_argmax")
+
+
+def fpd_constrain_argmax_noalloc(model, batch, block_len, hidden, layout, tokens_out, logits_out, stream=None):
+    """fpd_constrain_argmax for callers that cannot allocate: the scratch is the library's static device array."""
+    _check(lib().fpd_constrain_argmax_noalloc(model, batch, block_len, _ptr(hidden),
+                                              ctypes.byref(layout) if layout is not None else None,
+                                              _ptr(tokens_out), _ptr(logits_out), _stream(stream)),
+           "fpd_constrain_argmax_noalloc")
 
 
 def fpd_verify(mode, batch, block_len, draft, target, layout, rule, pad_id, accept_len, committed, valid_out,

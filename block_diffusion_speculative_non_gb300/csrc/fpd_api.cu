@@ -201,6 +201,19 @@ extern "C" {
 
 struct fpd_model : public Model {};
 
+}  // extern "C"
+
+namespace fpd {
+// Services of this file for entry points defined in other translation units of the library.
+fpd_status set_last_error(fpd_status s, const char* msg) {
+  t_err = msg;
+  return s;
+}
+size_t argmax_scratch_bytes(const fpd_model* m, int batch, int block_len) { return ws_argmax_bytes(*m, batch, block_len); }
+}  // namespace fpd
+
+extern "C" {
+
 const char* fpd_last_error(void) { return t_err.c_str(); }
 
 uint64_t fpd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -176,6 +176,25 @@ fpd_status fpd_constrain_argmax(fpd_model* model, int batch, int block_len, cons
                                 const fpd_vocab_layout* layout, int32_t* tokens_out, float* logits_out,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- a8 without a workspace argument ----------------------------------------------------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers that cannot allocate device memory
+ * (a host framework that owns the whole device heap and forbids plugins to call cudaMalloc, or a latency-critical
+ * loop where cudaMalloc's implicit device synchronisation is not allowed).  It computes exactly what
+ * fpd_constrain_argmax computes, with the same arguments minus the workspace: its scratch memory is a fixed
+ * 8 MiB array in the library's device memory (present on every device that loads the library until the process
+ * exits), so the caller supplies only inputs and outputs.
+ *   - Limit: batch * (block_len - 1) positions whose scratch fits 8 MiB (about 1300 positions at d_model 2560);
+ *     larger calls return FPD_ERR_CAPACITY with a message naming the bytes needed, without launching anything.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
+ *     current; make that first call before any stream capture on that device.
+ *   - Every call on a device shares the one array.  Calls whose kernels overlap on the GPU (other streams,
+ *     other host threads) race on it and give undefined results; serialise them.  Each call resets the parts
+ *     of the array it reads before reading them, so nothing carries over from the previous call.
+ *   - No call allocates or frees device memory. */
+fpd_status fpd_constrain_argmax_noalloc(fpd_model* model, int batch, int block_len, const void* hidden,
+                                        const fpd_vocab_layout* layout, int32_t* tokens_out, float* logits_out,
+                                        void* stream);
+
 /* ---- a9: acceptance-length scan ----------------------------------------------------------------------------
  * FPD_VERIFY_TEXT (VFlash blog "Method"; VFlash (zh) §2.1): target [B, L] holds t_1..t_L, the target's
  *   greedy token at block positions 1..L (t_L follows the last draft).  n = length of the longest prefix
