@@ -76,7 +76,7 @@ def lib():
         l.fpd_draft_block.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, i32, vp, vp, vp,
                                       sz, vp]
         l.fpd_constrain_argmax.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.POINTER(VocabLayout), vp, vp,
-                                           vp, sz, vp]
+                                           vp, vp, sz, vp]
         l.fpd_constrain_argmax_noalloc.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.POINTER(VocabLayout),
                                                    vp, vp, vp]
         l.fpd_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, ctypes.POINTER(VocabLayout), vp,
@@ -162,10 +162,11 @@ def make_layout(class_off, class_ranges, pos_class_dev) -> VocabLayout:
 
 
 def fpd_constrain_argmax(model, batch, block_len, hidden, layout, tokens_out, logits_out, workspace,
-                         workspace_bytes, stream=None):
+                         workspace_bytes, stream=None, margin_out=None):
     _check(lib().fpd_constrain_argmax(model, batch, block_len, _ptr(hidden),
                                       ctypes.byref(layout) if layout is not None else None, _ptr(tokens_out),
-                                      _ptr(logits_out), _ptr(workspace), workspace_bytes, _stream(stream)),
+                                      _ptr(logits_out), _ptr(margin_out), _ptr(workspace), workspace_bytes,
+                                      _stream(stream)),
            "fpd_constrain_argmax")
 
 

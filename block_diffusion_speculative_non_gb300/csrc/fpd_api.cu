@@ -81,9 +81,48 @@ struct DraftWs {
   float2* ml;
   int att_splits, att_chunk;
   TcPlan p_qkv, p_o, p_sw, p_down;
+  // few-token path (k_stream.cu)
+  bool stream;
+  StreamPlan s_qkv, s_o, s_sw, s_down;
+  float *ss_a, *ss_b;       // sums of squares of the residual stream [parts][16]
+  int *cnt_qkv, *cnt_o, *cnt_down, n_cnt;
 };
 
+// The few-token path takes calls with at most 16 block positions in all.
+bool use_stream(const Model& m, int B, int L) { return B * L <= kStreamMaxTokens && stream_shape_ok(m.d); }
+
+DraftWs carve_draft_stream(const Model& m, Carver& c, int B, int L, int t_cap) {
+  const auto& d = m.d;
+  DraftWs w{};
+  w.stream = true;
+  const int M = B * L, S = kStreamMaxTokens;
+  const int nqkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim, nqh = d.n_q_heads * d.head_dim;
+  w.s_qkv = stream_plan(nqkv / 128, d.d_model, m.num_sms, true);
+  w.s_o = stream_plan(d.d_model / 128, nqh, m.num_sms, true);
+  w.s_sw = stream_plan(d.d_ff / 64, d.d_model, m.num_sms, false);
+  w.s_down = stream_plan(d.d_model / 128, d.d_ff, m.num_sms, true);
+  const size_t part = std::max(std::max(stream_part_floats(w.s_qkv), stream_part_floats(w.s_o)),
+                               stream_part_floats(w.s_down));
+  w.part = c.take<float>(std::max<size_t>(part, 1));
+  w.q = c.take<bf16>((size_t)M * nqh);
+  w.kblk = c.take<bf16>((size_t)M * d.n_kv_heads * d.head_dim);
+  w.vblk = c.take<bf16>((size_t)M * d.n_kv_heads * d.head_dim);
+  w.o = c.take<bf16>((size_t)M * nqh);
+  w.hmid = c.take<bf16>((size_t)M * d.d_ff);
+  w.ss_a = c.take<float>((size_t)(d.d_model / 128) * S);
+  w.ss_b = c.take<float>((size_t)(d.d_model / 128) * S);
+  w.n_cnt = w.s_qkv.tiles + 2 * w.s_o.tiles;
+  w.cnt_qkv = c.take<int>(w.n_cnt);
+  w.cnt_o = w.cnt_qkv ? w.cnt_qkv + w.s_qkv.tiles : nullptr;
+  w.cnt_down = w.cnt_o ? w.cnt_o + w.s_o.tiles : nullptr;
+  attn_plan(B, L, d.n_q_heads, d.n_kv_heads, t_cap, m.num_sms, &w.att_splits, &w.att_chunk);
+  w.o_part = c.take<float>((size_t)w.att_splits * M * nqh);
+  w.ml = c.take<float2>((size_t)w.att_splits * M * d.n_q_heads);
+  return w;
+}
+
 DraftWs carve_draft(const Model& m, Carver& c, int B, int L, int t_cap) {
+  if (use_stream(m, B, L)) return carve_draft_stream(m, c, B, L, t_cap);
   const auto& d = m.d;
   DraftWs w{};
   const int M = B * L;
@@ -112,14 +151,27 @@ DraftWs carve_draft(const Model& m, Carver& c, int B, int L, int t_cap) {
 struct ArgmaxWs {
   bf16* z;   // final-normed rows in class-sorted order
   int *rows_sorted, *inv_sorted, *class_row_off, *n_items;
-  unsigned long long* packed;
+  unsigned long long *packed, *packed2;
   int4* items;
   int max_items, row_tile;
+  // few-token unconstrained path: per-CTA top-2 slots
+  bool stream;
+  StreamPlan s_lm;
+  unsigned long long* slots;
 };
 
-ArgmaxWs carve_argmax(const Model& m, Carver& c, int B, int L) {
+ArgmaxWs carve_argmax(const Model& m, Carver& c, int B, int L, bool constrained) {
   ArgmaxWs w{};
   const int n_rows = B * (L - 1);
+  if (!constrained && n_rows <= kStreamMaxTokens && stream_shape_ok(m.d)) {
+    w.stream = true;
+    w.s_lm.tiles = ceil_div(m.d.vocab, 128);
+    w.s_lm.splits = 1;
+    w.s_lm.k_split = m.d.d_model;
+    w.s_lm.grid = std::min(w.s_lm.tiles, m.num_sms);
+    w.slots = c.take<unsigned long long>((size_t)w.s_lm.grid * kStreamMaxTokens * 2);
+    return w;
+  }
   w.row_tile = tc_lm_row_tile(n_rows);
   w.z = c.take<bf16>((size_t)n_rows * m.d.d_model);
   w.rows_sorted = c.take<int>(n_rows);
@@ -127,6 +179,7 @@ ArgmaxWs carve_argmax(const Model& m, Carver& c, int B, int L) {
   w.class_row_off = c.take<int>(FPD_MAX_CLASSES + 1);
   w.n_items = c.take<int>(1);
   w.packed = c.take<unsigned long long>(n_rows);
+  w.packed2 = c.take<unsigned long long>(n_rows);
   w.max_items = (ceil_div(m.d.vocab, kLmColTile) + 1 + FPD_MAX_RANGES) * (ceil_div(n_rows, w.row_tile) + FPD_MAX_CLASSES);
   w.items = c.take<int4>(w.max_items);
   return w;
@@ -155,9 +208,10 @@ size_t ws_draft_bytes(const Model& m, int B, int L, int t_cap) {
   return c.off;
 }
 size_t ws_argmax_bytes(const Model& m, int B, int L) {
-  Carver c;
-  carve_argmax(m, c, B, L);
-  return c.off;
+  Carver c0, c1;
+  carve_argmax(m, c0, B, L, false);
+  carve_argmax(m, c1, B, L, true);
+  return std::max(c0.off, c1.off);
 }
 size_t ws_prep_bytes(const Model& m, int rows) {
   Carver c;
@@ -260,6 +314,7 @@ fpd_status fpd_model_create(const fpd_model_desc* desc, const fpd_weights* w, fp
     std::call_once(once, [] {
       init_err = tc_init_attributes();
       if (init_err == cudaSuccess) init_err = attn_init_attributes();
+      if (init_err == cudaSuccess) init_err = stream_init_attributes();
     });
     if (init_err != cudaSuccess) return cuda_fail(init_err, "kernel attributes");
   }
@@ -406,6 +461,109 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
   const int M = batch * L, dm = d.d_model, h = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.d_ff;
   const int nqkv = (nq + 2 * nkv) * h;
   bf16* x = (bf16*)hidden_out;
+  AttnArgs a{};
+  a.q = w.q;
+  a.store = (const bf16*)kv_store;
+  a.kblk = w.kblk;
+  a.vblk = w.vblk;
+  a.ctx_len = ctx_len;
+  a.o_part = w.o_part;
+  a.ml = w.ml;
+  a.batch = batch;
+  a.L = L;
+  a.nq = nq;
+  a.nkv = nkv;
+  a.head_dim = h;
+  a.t_cap = t_cap;
+  a.rows = M;
+  a.splits = w.att_splits;
+  a.chunk = w.att_chunk;
+  if (w.stream) {
+    // few-token path: 6 kernels per layer, norms applied on load, split-K reduced inside the GEMMs
+    FPD_CUDA(launch_embed_ss(x, w.ss_a, w.cnt_qkv, w.n_cnt, (const bf16*)m->w.embed, anchor, mask_id, batch, L, dm,
+                             d.vocab, st),
+             "embedding");
+    int n_ss = 1;
+    for (int l = 0; l < d.n_layers; l++) {
+      StreamGemm g{};
+      g.M = M;
+      g.eps = d.rms_eps;
+      g.part = w.part;
+      // QKV projection of RMSNorm_attn(x), q/k norm + RoPE at ctx_len + j
+      g.epi = SEPI_QKV;
+      g.plan = w.s_qkv;
+      g.w = (const bf16*)m->w.wqkv[l];
+      g.N = nqkv;
+      g.K = dm;
+      g.x = x;
+      g.ldx = dm;
+      g.xform = XF_NORM;
+      g.ss_in = w.ss_a;
+      g.n_ss = n_ss;
+      g.gain = (const bf16*)m->w.attn_norm[l];
+      g.counters = w.cnt_qkv;
+      g.q = w.q;
+      g.kblk = w.kblk;
+      g.vblk = w.vblk;
+      g.q_norm = (const bf16*)m->w.q_norm[l];
+      g.k_norm = (const bf16*)m->w.k_norm[l];
+      g.rope = m->rope;
+      g.ctx_len = ctx_len;
+      g.t_cap = t_cap;
+      g.L = L;
+      g.nq = nq;
+      g.nkv = nkv;
+      g.h = h;
+      FPD_CUDA(launch_stream_gemm(g, st), "QKV GEMM + q/k norm + RoPE");
+      a.layer = l;
+      FPD_CUDA(launch_attention(a, w.o, st), "attention");
+      // O projection + residual
+      StreamGemm o = g;
+      o.epi = SEPI_RESID;
+      o.plan = w.s_o;
+      o.w = (const bf16*)m->w.wo[l];
+      o.N = dm;
+      o.K = nq * h;
+      o.x = w.o;
+      o.ldx = nq * h;
+      o.xform = XF_COPY;
+      o.counters = w.cnt_o;
+      o.xres = x;
+      o.ss_out = w.ss_b;
+      FPD_CUDA(launch_stream_gemm(o, st), "O GEMM + residual");
+      // gate/up of RMSNorm_mlp(x) with SwiGLU
+      StreamGemm u = g;
+      u.epi = SEPI_SWIGLU;
+      u.plan = w.s_sw;
+      u.w = (const bf16*)m->w.w_gate_up[l];
+      u.N = F;
+      u.K = dm;
+      u.x = x;
+      u.ldx = dm;
+      u.xform = XF_NORM;
+      u.ss_in = w.ss_b;
+      u.n_ss = dm / 128;
+      u.gain = (const bf16*)m->w.mlp_norm[l];
+      u.hmid = w.hmid;
+      FPD_CUDA(launch_stream_gemm(u, st), "gate/up + SwiGLU");
+      // down projection + residual
+      StreamGemm dn = o;
+      dn.plan = w.s_down;
+      dn.w = (const bf16*)m->w.w_down[l];
+      dn.K = F;
+      dn.x = w.hmid;
+      dn.ldx = F;
+      dn.counters = w.cnt_down;
+      dn.ss_out = w.ss_a;
+      FPD_CUDA(launch_stream_gemm(dn, st), "down GEMM + residual");
+      n_ss = dm / 128;
+      if (layer_hidden)
+        FPD_CUDA(cudaMemcpyAsync((bf16*)layer_hidden + (size_t)l * M * dm, x, (size_t)M * dm * sizeof(bf16),
+                                 cudaMemcpyDeviceToDevice, st),
+                 "layer_hidden copy");
+    }
+    return FPD_OK;
+  }
   FPD_CUDA(launch_embed_norm(x, w.xn, (const bf16*)m->w.embed, anchor, mask_id, (const bf16*)m->w.attn_norm[0], batch,
                              L, dm, d.vocab, d.rms_eps, st),
            "embed + attention norm");
@@ -432,24 +590,7 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
                              (const bf16*)m->w.q_norm[l], (const bf16*)m->w.k_norm[l], m->rope, ctx_len, t_cap, batch,
                              L, nq, nkv, h, d.rms_eps, st),
              "q/k norm + RoPE");
-    AttnArgs a{};
-    a.q = w.q;
-    a.store = (const bf16*)kv_store;
-    a.kblk = w.kblk;
-    a.vblk = w.vblk;
-    a.ctx_len = ctx_len;
-    a.o_part = w.o_part;
-    a.ml = w.ml;
-    a.batch = batch;
-    a.L = L;
-    a.nq = nq;
-    a.nkv = nkv;
-    a.head_dim = h;
-    a.t_cap = t_cap;
     a.layer = l;
-    a.rows = M;
-    a.splits = w.att_splits;
-    a.chunk = w.att_chunk;
     FPD_CUDA(launch_attention(a, w.o, st), "attention");
     FPD_CUDA(gemm(w.o, nq * h, m->w.wo[l], dm, w.p_o), "O GEMM");
     FPD_CUDA(launch_residual_norm(x, w.xn, w.part, w.p_o.splits, (size_t)M * dm, (const bf16*)m->w.mlp_norm[l], M, dm,
@@ -470,8 +611,8 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
 
 // ---- a8 -----------------------------------------------------------------------------------------------------
 fpd_status fpd_constrain_argmax(fpd_model* m, int batch, int L, const void* hidden, const fpd_vocab_layout* layout,
-                                int32_t* tokens_out, float* logits_out, void* workspace, size_t ws_bytes,
-                                void* stream) {
+                                int32_t* tokens_out, float* logits_out, float* margin_out, void* workspace,
+                                size_t ws_bytes, void* stream) {
   if (!m) return fail(FPD_ERR_INVALID_ARG, "model is null");
   const auto& d = m->d;
   if (batch < 1 || L < 2) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d", batch, L);
@@ -485,10 +626,31 @@ fpd_status fpd_constrain_argmax(fpd_model* m, int batch, int L, const void* hidd
   if (ds) return ds;
   Carver c;
   c.base = (char*)workspace;
-  ArgmaxWs w = carve_argmax(*m, c, batch, L);
+  ArgmaxWs w = carve_argmax(*m, c, batch, L, layout != nullptr);
   if (c.off > ws_bytes) return fail(FPD_ERR_CAPACITY, "workspace %zu < %zu bytes", ws_bytes, c.off);
   cudaStream_t st = (cudaStream_t)stream;
   const int n_rows = batch * (L - 1);
+  if (w.stream) {
+    // few positions, whole vocabulary: final norm on load, per-CTA top-2 slots, one decode kernel
+    StreamGemm g{};
+    g.epi = SEPI_ARGMAX;
+    g.plan = w.s_lm;
+    g.w = (const bf16*)m->w.lm_head;
+    g.M = n_rows;
+    g.N = d.vocab;
+    g.K = d.d_model;
+    g.x = (const bf16*)hidden;
+    g.ldx = d.d_model;
+    g.xform = XF_NORM_FULL;
+    g.lm_block = L;
+    g.gain = (const bf16*)m->w.final_norm;
+    g.eps = d.rms_eps;
+    g.slots = w.slots;
+    g.logits = logits_out;
+    FPD_CUDA(launch_stream_gemm(g, st), "LM head + argmax");
+    FPD_CUDA(launch_stream_decode(tokens_out, margin_out, w.slots, w.s_lm.grid, n_rows, st), "argmax decode");
+    return FPD_OK;
+  }
   LmPlan p{};
   p.n_rows = n_rows;
   p.L = L;
@@ -511,15 +673,16 @@ fpd_status fpd_constrain_argmax(fpd_model* m, int batch, int L, const void* hidd
     p.range_class[0] = 0;
   }
   FPD_CUDA(launch_lm_plan(p, layout ? layout->pos_class : nullptr, w.rows_sorted, w.inv_sorted, w.class_row_off,
-                          w.items, w.n_items, w.packed, w.max_items, st),
+                          w.items, w.n_items, w.packed, w.packed2, w.max_items, st),
            "LM-head plan");
   FPD_CUDA(launch_rmsnorm_gather(w.z, (const bf16*)hidden, (const bf16*)m->w.final_norm, w.rows_sorted, n_rows,
                                  d.d_model, d.rms_eps, L, st),
            "final norm");
   FPD_CUDA(launch_tc_lmhead(p, w.z, n_rows, (const bf16*)m->w.lm_head, d.d_model, d.vocab, w.items, w.n_items,
-                            w.max_items, w.packed, w.rows_sorted, logits_out, m->num_sms, layout == nullptr, st),
+                            w.max_items, w.packed, margin_out ? w.packed2 : nullptr, w.rows_sorted, logits_out,
+                            m->num_sms, layout == nullptr, st),
            "LM head + argmax");
-  FPD_CUDA(launch_lm_decode(tokens_out, w.packed, w.inv_sorted, n_rows, st), "argmax decode");
+  FPD_CUDA(launch_lm_decode(tokens_out, margin_out, w.packed, w.packed2, w.inv_sorted, n_rows, st), "argmax decode");
   return FPD_OK;
 }
 

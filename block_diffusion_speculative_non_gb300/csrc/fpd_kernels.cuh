@@ -42,6 +42,47 @@ void tc_set_swap_variant(int v);      // tuning sweeps only (fpd_test_set_varian
 cudaError_t attn_init_attributes();
 cudaError_t launch_sum_splits(float* out, const float* part, int splits, size_t n, cudaStream_t st);
 
+// ---- few-token path (k_stream.cu): weight-streaming GEMMs with fused norm-on-load and epilogues ---------------
+enum { SEPI_QKV = 0, SEPI_RESID = 1, SEPI_SWIGLU = 2, SEPI_ARGMAX = 3 };
+enum { XF_COPY = 0, XF_NORM = 1, XF_NORM_FULL = 2 };
+constexpr int kStreamMaxTokens = 16;
+struct StreamPlan {
+  int tiles, splits, k_split, grid;
+};
+struct StreamGemm {
+  int epi;                        // SEPI_*
+  StreamPlan plan;
+  const bf16* w;                  // weights [N, K] ([2F, K] for SwiGLU), K-major
+  int M, N, K;
+  const bf16* x;                  // activation source rows, row stride ldx
+  int ldx, xform, lm_block;
+  const float* ss_in;             // sums of squares [n_ss][16] (XF_NORM)
+  int n_ss;
+  const bf16* gain;
+  float eps;
+  float* part;                    // split-K partials [splits][tiles][16][128]
+  int* counters;                  // [tiles], zero on entry
+  bf16 *q, *kblk, *vblk;          // SEPI_QKV outputs
+  const bf16 *q_norm, *k_norm;
+  const float2* rope;
+  const int32_t* ctx_len;
+  int t_cap, L, nq, nkv, h;
+  bf16* xres;                     // SEPI_RESID: residual stream [M][N]
+  float* ss_out;                  // SEPI_RESID: sums of squares [tiles][16]
+  bf16* hmid;                     // SEPI_SWIGLU output [M][N]
+  unsigned long long* slots;      // SEPI_ARGMAX: [grid][16][2]
+  float* logits;                  // SEPI_ARGMAX: [M][N] or null
+};
+bool stream_shape_ok(const fpd_model_desc& d);
+StreamPlan stream_plan(int tiles, int K, int num_sms, bool split_ok);
+size_t stream_part_floats(const StreamPlan& pl);
+cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st);
+cudaError_t stream_init_attributes();
+cudaError_t launch_embed_ss(bf16* x, float* ss, int* counters, int n_cnt, const bf16* embed, const int32_t* anchor,
+                            int32_t mask_id, int B, int L, int d, int V, cudaStream_t st);
+cudaError_t launch_stream_decode(int32_t* tokens, float* margin, const unsigned long long* slots, int n_slots,
+                                 int n_rows, cudaStream_t st);
+
 // ---- row ops -------------------------------------------------------------------------------------------------
 cudaError_t launch_rmsnorm_partials(bf16* out, const float* part, int nsplit, size_t split_stride, const bf16* g,
                                     int rows, int d, float eps, cudaStream_t st);
@@ -80,14 +121,16 @@ struct LmPlan {
 };
 // rows_sorted: sorted slot -> original row (-1 past the last placed row); inv_sorted: original row -> slot.
 cudaError_t launch_lm_plan(const LmPlan& p, const int16_t* pos_class, int* rows_sorted, int* inv_sorted,
-                           int* class_row_off, int4* items, int* n_items, unsigned long long* packed, int max_items,
-                           cudaStream_t st);
+                           int* class_row_off, int4* items, int* n_items, unsigned long long* packed,
+                           unsigned long long* packed2, int max_items, cudaStream_t st);
 int tc_lm_row_tile(int n_rows);
 cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows, const bf16* W, int d, int V,
                              const int4* items, const int* n_items, int max_items, unsigned long long* packed,
-                             const int* rows_sorted, float* logits, int num_sms, bool unconstrained, cudaStream_t st);
-cudaError_t launch_lm_decode(int32_t* tokens, const unsigned long long* packed, const int* inv_sorted, int n,
-                             cudaStream_t st);
+                             unsigned long long* packed2, const int* rows_sorted, float* logits, int num_sms,
+                             bool unconstrained, cudaStream_t st);
+// tokens[r] = argmax id; margin[r] (optional) = top-1 minus top-2 fp32 logit (+inf with one legal id)
+cudaError_t launch_lm_decode(int32_t* tokens, float* margin, const unsigned long long* packed,
+                             const unsigned long long* packed2, const int* inv_sorted, int n, cudaStream_t st);
 // RMSNorm of block rows into sorted order: out[i] = norm(hidden[map(rows_sorted[i])]), map drops anchors.
 cudaError_t launch_rmsnorm_gather(bf16* out, const bf16* in, const bf16* g, const int* rows_sorted, int rows, int d,
                                   float eps, int L, cudaStream_t st);

@@ -70,7 +70,7 @@ fpd_status fpd_constrain_argmax_noalloc(fpd_model* model, int batch, int block_l
   void* scratch = nullptr;
   fpd_status s = scratch_address(&scratch);
   if (s) return s;
-  return fpd_constrain_argmax(model, batch, block_len, hidden, layout, tokens_out, logits_out, scratch,
+  return fpd_constrain_argmax(model, batch, block_len, hidden, layout, tokens_out, logits_out, nullptr, scratch,
                               kNoAllocScratchBytes, stream);
 }
 

@@ -265,35 +265,47 @@ __global__ void __launch_bounds__(NWARP * 32) attn_mma_kernel(AttnArgs a, bf16* 
   }
 }
 
-// Combines the splits of one (row, q head); running maxima are in base-2 units.  The (m, l) pairs of all splits
-// are staged in shared memory first, then every thread sums its column over the splits in split order.
+// Combines the splits of one (row, q head); running maxima are in base-2 units.  Thread t handles splits
+// t, t + H, ...: the block takes the maximum of the split maxima, then every split's weight 2^(m_s - M) and the
+// denominator sum_s l_s w_s (fixed reduction tree: bit-reproducible); finally every thread sums its column over
+// the splits in split order.
 template <int H>
 __global__ void attn_merge_kernel(bf16* __restrict__ out, const float* __restrict__ o_part,
                                   const float2* __restrict__ ml, int nsplit, int rows, int nq) {
   pdl_trigger();
   pdl_wait();
+  constexpr int NW = H / 32;
   __shared__ float w_s[128];
-  __shared__ float den_s;
-  const int r = blockIdx.x, i = blockIdx.y, e = threadIdx.x;
+  __shared__ float red[NW];
+  const int r = blockIdx.x, i = blockIdx.y, e = threadIdx.x, lane = e & 31, wp = e >> 5;
   const int ns = nsplit < 128 ? nsplit : 128;   // attn_plan never makes more than 128 splits
-  for (int s = e; s < ns; s += blockDim.x) {
+  float mx = -INFINITY;
+  for (int s = e; s < ns; s += H) {
     const float2 v = __ldcg(ml + ((size_t)s * rows + r) * nq + i);
-    w_s[s] = v.y > 0.f ? v.x : -INFINITY;       // running max of split s (empty splits excluded)
+    const float m = v.y > 0.f ? v.x : -INFINITY;   // empty splits carry no weight
+    w_s[s] = m;
+    mx = fmaxf(mx, m);
   }
+  mx = warp_max(mx);
+  if (lane == 0) red[wp] = mx;
   __syncthreads();
-  if (e == 0) {
-    float M = -INFINITY;
-    for (int s = 0; s < ns; s++) M = fmaxf(M, w_s[s]);
-    float den = 0.f;
-    for (int s = 0; s < ns; s++) {
-      const float2 v = __ldcg(ml + ((size_t)s * rows + r) * nq + i);
-      const float wgt = w_s[s] == -INFINITY ? 0.f : exp2f(w_s[s] - M);
-      den += v.y * wgt;
-      w_s[s] = wgt;
-    }
-    den_s = den;
+  mx = red[0];
+#pragma unroll
+  for (int k = 1; k < NW; k++) mx = fmaxf(mx, red[k]);
+  __syncthreads();
+  float den = 0.f;
+  for (int s = e; s < ns; s += H) {
+    const float2 v = __ldcg(ml + ((size_t)s * rows + r) * nq + i);
+    const float wgt = w_s[s] == -INFINITY ? 0.f : exp2f(w_s[s] - mx);
+    den += v.y * wgt;
+    w_s[s] = wgt;
   }
+  den = warp_sum(den);
+  if (lane == 0) red[wp] = den;
   __syncthreads();
+  den = red[0];
+#pragma unroll
+  for (int k = 1; k < NW; k++) den += red[k];
   const float* op = o_part + ((size_t)r * nq + i) * H + e;
   const size_t sstride = (size_t)rows * nq * H;
   float num = 0.f;
@@ -305,7 +317,6 @@ __global__ void attn_merge_kernel(bf16* __restrict__ out, const float* __restric
     for (int u = 0; u < 8; u++)
       if (s0 + u < ns) num += t[u] * w_s[s0 + u];
   }
-  const float den = den_s;
   out[((size_t)r * nq + i) * H + e] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
 }
 }  // namespace
@@ -316,7 +327,7 @@ void attn_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* s
   const int base = q_tiles * batch * nkv;
   const int max_keys = t_cap + L;
   const int max_splits = ceil_div(max_keys, KT);
-  int s = ceil_div(2 * num_sms, base);
+  int s = ceil_div(num_sms, base);   // about one CTA per SM
   s = s < 1 ? 1 : (s > max_splits ? max_splits : s);
   s = s > 128 ? 128 : s;   // the merge kernel stages at most 128 splits' weights
   const int ch = ceil_div(ceil_div(max_keys, s), KT) * KT;

@@ -54,6 +54,7 @@ struct TcParams {
   int implicit_total;
   int hi_tab[FPD_MAX_RANGES];    // end (exclusive) of every legal id range
   unsigned long long* packed;    // [sorted rows]
+  unsigned long long* packed2;   // [sorted rows] second-best word (top-2 margin) or null
   const int* rows_sorted;        // sorted row -> original row (logits only)
   float* logits;                 // [n_rows, V] or null
   int V;
@@ -391,9 +392,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const int col = c0 + j;
             const bool ok = vok && col < w.b_cnt;
             unsigned long long best = ok ? pack_argmax(v[j], vid) : 0ull;
+            if (!p.packed2) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
-            if (lane == 0 && best) atomicMax(p.packed + w.b_row0 + col, best);
+              for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+              if (lane == 0 && best) atomicMax(p.packed + w.b_row0 + col, best);
+            } else {
+              // top-2: the value an atomicMax displaces (or the candidate it rejects) is a candidate for the
+              // second place, so every word but the final maximum reaches packed2
+              unsigned long long second = 0ull;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, best, o);
+                const unsigned long long b2 = __shfl_xor_sync(0xffffffffu, second, o);
+                const unsigned long long lo = min(best, b1);
+                best = max(best, b1);
+                second = max(lo, max(second, b2));
+              }
+              if (lane == 0 && best) {
+                const unsigned long long old = atomicMax(p.packed + w.b_row0 + col, best);
+                atomicMax(p.packed2 + w.b_row0 + col, max(min(old, best), second));
+              }
+            }
             if (p.logits && ok) p.logits[(size_t)p.rows_sorted[w.b_row0 + col] * p.V + vid] = v[j];
           }
         }
@@ -424,22 +443,6 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   });
   return fn;
-}
-
-// Row-major bf16 matrix [rows, cols] with row stride ld (elements), boxes of 64 columns x box_rows rows,
-// 128-byte swizzle (matches sw128_kmajor_desc).  Out-of-range boxes read zeros.
-cudaError_t make_tmap(CUtensorMap* tm, const void* ptr, int rows, int cols, int ld, int box_rows) {
-  auto enc = get_encode();
-  if (!enc) return cudaErrorNotSupported;
-  if (((uintptr_t)ptr & 15) || (ld * 2) % 16 || rows < 1 || cols < BK) return cudaErrorInvalidValue;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int BN, int STAGES, bool SWAP, int EPI, int KS>
@@ -479,6 +482,37 @@ cudaError_t launch_swap16(const TcParams& p, int grid, cudaStream_t st) {
   }
 }
 }  // namespace
+
+// Row-major bf16 matrix [rows, cols] with row stride ld (elements), boxes of 64 columns x box_rows rows,
+// 128-byte swizzle (matches sw128_kmajor_desc).  Out-of-range boxes read zeros.
+cudaError_t make_tmap(CUtensorMap* tm, const void* ptr, int rows, int cols, int ld, int box_rows) {
+  if (rows < 1 || cols < BK) return cudaErrorInvalidValue;
+  const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)ld * 2};
+  const uint32_t box[2] = {(uint32_t)BK, (uint32_t)box_rows};
+  return make_tmap_nd(tm, ptr, 2, dims, strides, box);
+}
+
+cudaError_t make_tmap_nd(CUtensorMap* tm, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                         const uint32_t* box) {
+  auto enc = get_encode();
+  if (!enc) return cudaErrorNotSupported;
+  if (((uintptr_t)ptr & 15) || rank < 2 || rank > 3) return cudaErrorInvalidValue;
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3], estr[3] = {1, 1, 1};
+  for (int i = 0; i < rank; i++) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; i++) {
+    if (strides[i] % 16) return cudaErrorInvalidValue;
+    st[i] = strides[i];
+  }
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), d, st, b, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 void tc_set_swap_variant(int v) { g_swap_variant = (v >= 0 && v < 5) ? v : 0; }
 
@@ -666,7 +700,8 @@ int tc_lm_row_tile(int n_rows) { return n_rows <= 16 ? 16 : (n_rows <= 32 ? 32 :
 
 cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows, const bf16* W, int d, int V,
                              const int4* items, const int* n_items, int max_items, unsigned long long* packed,
-                             const int* rows_sorted, float* logits, int num_sms, bool unconstrained, cudaStream_t st) {
+                             unsigned long long* packed2, const int* rows_sorted, float* logits, int num_sms,
+                             bool unconstrained, cudaStream_t st) {
   if (d % BK) return cudaErrorInvalidValue;
   const int bn = lp.rt;
   TcParams p;
@@ -688,6 +723,7 @@ cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows,
   }
   for (int q = 0; q < lp.n_range; q++) p.hi_tab[q] = lp.range_hi[q];
   p.packed = packed;
+  p.packed2 = packed2;
   p.rows_sorted = rows_sorted;
   p.logits = logits;
   p.V = V;

@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(1024) lm_plan_kernel(LmPlan p, const int16_t* 
                                                         int* __restrict__ rows_sorted, int* __restrict__ inv_sorted,
                                                         int* __restrict__ class_row_off, int4* __restrict__ items,
                                                         int* __restrict__ n_items,
-                                                        unsigned long long* __restrict__ packed, int max_items) {
+                                                        unsigned long long* __restrict__ packed,
+                                                        unsigned long long* __restrict__ packed2, int max_items) {
   pdl_trigger();
   pdl_wait();
   __shared__ int warp_tot[32];
@@ -47,6 +48,7 @@ __global__ void __launch_bounds__(1024) lm_plan_kernel(LmPlan p, const int16_t* 
   const int tid = threadIdx.x;
   for (int r = tid; r < p.n_rows; r += blockDim.x) {
     packed[r] = 0ull;
+    packed2[r] = 0ull;
     inv_sorted[r] = -1;
     rows_sorted[r] = -1;
   }
@@ -114,10 +116,10 @@ __global__ void __launch_bounds__(1024) lm_plan_kernel(LmPlan p, const int16_t* 
 }
 
 cudaError_t launch_lm_plan(const LmPlan& p, const int16_t* pos_class, int* rows_sorted, int* inv_sorted,
-                           int* class_row_off, int4* items, int* n_items, unsigned long long* packed, int max_items,
-                           cudaStream_t st) {
+                           int* class_row_off, int4* items, int* n_items, unsigned long long* packed,
+                           unsigned long long* packed2, int max_items, cudaStream_t st) {
   return launch_k(lm_plan_kernel, 1, 1024, 0, st, p, pos_class, rows_sorted, inv_sorted, class_row_off, items, n_items,
-                  packed, max_items);
+                  packed, packed2, max_items);
 }
 
 // ---- final RMSNorm into sorted order -------------------------------------------------------------------------------
@@ -169,9 +171,17 @@ cudaError_t launch_rmsnorm_gather(bf16* out, const bf16* in, const bf16* g, cons
   return launch_k(rmsnorm_gather_kernel, rows, 256, 0, st, out, in, g, rows_sorted, d, eps, L);
 }
 
-// ---- decode the packed argmax words into ids ---------------------------------------------------------------------
-__global__ void lm_decode_kernel(int32_t* __restrict__ tokens, const unsigned long long* __restrict__ packed,
-                                 const int* __restrict__ inv_sorted, int n) {
+// ---- decode the packed argmax words into ids (and the top-2 margin when asked) ------------------------------------
+__device__ __forceinline__ float unpack_value(unsigned long long p) {
+  uint32_t u = (uint32_t)(p >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+
+__global__ void lm_decode_kernel(int32_t* __restrict__ tokens, float* __restrict__ margin,
+                                 const unsigned long long* __restrict__ packed,
+                                 const unsigned long long* __restrict__ packed2, const int* __restrict__ inv_sorted,
+                                 int n) {
   pdl_trigger();
   pdl_wait();
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) {
@@ -179,13 +189,17 @@ __global__ void lm_decode_kernel(int32_t* __restrict__ tokens, const unsigned lo
     const unsigned long long p = i >= 0 ? packed[i] : 0ull;
     if (!p) record_check(kCheckNoLegalId);
     tokens[r] = p ? unpack_argmax_id(p) : -1;
+    if (margin) {
+      const unsigned long long p2 = i >= 0 ? packed2[i] : 0ull;
+      margin[r] = !p ? 0.f : (p2 ? (float)((double)unpack_value(p) - (double)unpack_value(p2)) : INFINITY);
+    }
   }
 }
 
-cudaError_t launch_lm_decode(int32_t* tokens, const unsigned long long* packed, const int* inv_sorted, int n,
-                             cudaStream_t st) {
+cudaError_t launch_lm_decode(int32_t* tokens, float* margin, const unsigned long long* packed,
+                             const unsigned long long* packed2, const int* inv_sorted, int n, cudaStream_t st) {
   const int grid = std::min(ceil_div(n, 256), 1024);
-  return launch_k(lm_decode_kernel, grid, 256, 0, st, tokens, packed, inv_sorted, n);
+  return launch_k(lm_decode_kernel, grid, 256, 0, st, tokens, margin, packed, packed2, inv_sorted, n);
 }
 
 }  // namespace fpd

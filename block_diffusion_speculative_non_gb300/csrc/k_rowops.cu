@@ -51,33 +51,6 @@ cudaError_t launch_rmsnorm_partials(bf16* out, const float* part, int nsplit, si
   return launch_k(rmsnorm_partials_kernel, rows, 256, 0, st, out, part, nsplit, split_stride, g, d, eps);
 }
 
-// ---- per-head RMSNorm + rotate-half RoPE on a warp's head ----------------------------------------------------------
-// Lane `lane` holds elements e = lane + 32k (k < H/32) of one head (H = head_dim).  The RoPE pair of element i
-// (< H/2) is i + H/2, held by the same lane.  rope[pos * H/2 + i] = (cos, sin) of angle pos * theta^(-2i/H).
-template <int H>
-__device__ __forceinline__ void head_norm_rope(float (&v)[H / 32], const bf16* __restrict__ gain, float eps,
-                                               const float2* __restrict__ rope_row, bool do_norm, bool do_rope) {
-  constexpr int NV = H / 32;
-  const int lane = threadIdx.x & 31;
-  if (do_norm) {
-    float ss = 0.f;
-#pragma unroll
-    for (int k = 0; k < NV; k++) ss += v[k] * v[k];
-    const float inv = rsqrtf(warp_sum(ss) / (float)H + eps);
-#pragma unroll
-    for (int k = 0; k < NV; k++) v[k] = v[k] * inv * __bfloat162float(gain[lane + 32 * k]);
-  }
-  if (do_rope) {
-#pragma unroll
-    for (int k = 0; k < NV / 2; k++) {
-      const float2 cs = rope_row[lane + 32 * k];
-      const float x1 = v[k], x2 = v[k + NV / 2];
-      v[k] = x1 * cs.x - x2 * cs.y;
-      v[k + NV / 2] = x2 * cs.x + x1 * cs.y;
-    }
-  }
-}
-
 // ---- a4 epilogue: sum split-K partials of [q | k | v], q/k RMSNorm + RoPE at pos = ctx_len[b] + j ------------------
 // grid (B*L, Hq + 2 Hkv), one warp per (row, head).
 template <int H>

@@ -1,0 +1,686 @@
+// k_stream.cu — the few-token path (at most 16 block positions in a call, e.g. one request's 16-position text
+// block): weight-streaming tcgen05 GEMMs with the preceding RMSNorm applied while the activations are loaded,
+// split-K reduced inside the GEMM, and the per-tile epilogues of the drafter layer fused in.
+//
+// At batch 1 the drafter pass is a stream of 1.8 GB of weights through 16 tokens (VFlash blog, "Key claims": the
+// five-layer drafter runs one forward per block; FlashDrive §3.4: decoding is bandwidth-bound), so the design
+// goal is to keep HBM busy and to spend as little time as possible between weight streams:
+//
+//   - One CTA per SM (grid = output tiles x K splits, each CTA one work item; the LM head is persistent over
+//     its id tiles).  Warp 0 streams 128-row weight atoms (K = 64, 16 KB, 128-byte swizzle) through an 8-deep
+//     TMA ring, starting before the predecessor kernel has finished (weights never depend on it).  Warp 1
+//     issues tcgen05.mma (M = 128 weight rows, N = 16 tokens, K = 16, fp32 in TMEM).  Warps 2-5 build the
+//     16-token activation slice ONCE in shared memory — applying RMSNorm on the way in when the GEMM consumes a
+//     normed residual stream — and later run the epilogue from TMEM.
+//   - RMSNorm on load: the residual kernels leave per-(tile, token) sums of squares of the bf16 residual; the
+//     consumer adds them in a fixed order, so xn = bf16(x * rsqrt(mean(x^2) + eps) * g) equals what a separate
+//     norm kernel would store (the bf16 storage point of the normed projection input).
+//   - Split-K without a reduce kernel: every CTA writes its fp32 partial tile; the LAST CTA of a tile to arrive
+//     (an atomic counter, no waiting) sums all partials in split order — bit-reproducible — and runs the
+//     epilogue: q/k RMSNorm + RoPE for the QKV projection, residual add + sum of squares for O and down.
+//   - LM head (no vocabulary constraint): every CTA keeps a running top-2 (logit, id) per position over its id
+//     tiles and writes it to its own slot; a one-warp-per-position decode merges the slots (argmax with
+//     lowest-id ties, and the top-2 margin).
+#include <cstring>
+
+#include "fpd_kernels.cuh"
+#include "tc_primitives.cuh"
+
+namespace fpd {
+
+namespace {
+
+constexpr int SBM = 128, SBK = 64, SBN = 16, SUK = 16;
+constexpr int kSThreads = 192;
+constexpr int kSStages = 8;
+constexpr int W_ATOM = SBM * SBK * 2;   // 16 KB: 128 weight rows x 64 K
+constexpr int X_ATOM = SBN * SBK * 2;   // 2 KB: 16 tokens x 64 K
+constexpr int G_ATOM = SBK * 2;         // 128 B of RMSNorm gain per K atom
+constexpr int kEpiScratch = SBN * SBM * 4;   // 8 KB: one fp32 output tile, token-major
+constexpr int kTmemCols = 32;                 // two 16-column accumulators
+// misc region: mbarriers full[S], empty[S], act_tma, act_full, tfull[2], tempty[2] | TMEM slot, abort, last-CTA
+// flag | inverse RMS per token [16] | context length per request [16] | running top-2 per token [16][2]
+constexpr int kMiscFlags = 8 * (2 * kSStages + 6);
+constexpr int kMiscInv = kMiscFlags + 16;
+constexpr int kMiscCtx = kMiscInv + SBN * 4;
+constexpr int kMiscRun = kMiscCtx + SBN * 4;
+constexpr int kMiscBytes = kMiscRun + SBN * 16;
+
+struct StreamParams {
+  CUtensorMap tm_w;            // weights [rows, K] bf16, box 64 x (128, SwiGLU: 64)
+  CUtensorMap tm_x;            // activation source: 2-D [M rows, K] (box 64 x 16) or, for the LM head, 3-D
+                               // [B][L-1 rows starting at block position 1][K] (box 64 x (L-1) x B)
+  int x_rank;                  // 2 or 3
+  uint32_t x_atom_bytes;       // bytes one activation atom load delivers
+  int M;                       // tokens (<= 16)
+  int N;                       // output features (SwiGLU: F; LM head: V)
+  int K;
+  int tiles, splits, k_split;  // output tiles, K splits, K elements per split (multiple of 64)
+  int xform;                   // XF_*
+  const float* ss_in;          // XF_NORM: sums of squares [n_ss][16]
+  int n_ss;
+  const bf16* gain;            // XF_NORM / XF_NORM_FULL: RMSNorm gain [K]
+  float eps;
+  // split-K reduction
+  float* part;                 // [splits][tiles][16][128]
+  int* counters;               // [tiles], zero on entry, left zero
+  // SEPI_QKV
+  bf16 *q, *kblk, *vblk;
+  const bf16 *q_norm, *k_norm;
+  const float2* rope;
+  const int32_t* ctx_len;
+  int t_cap, L, nq, nkv, h;
+  // SEPI_RESID
+  bf16* xres;                  // [M][N], updated in place
+  float* ss_out;               // [tiles][16]
+  // SEPI_SWIGLU
+  bf16* hmid;                  // [M][N]
+  // SEPI_ARGMAX
+  unsigned long long* slots;   // [gridDim][16][2]
+  float* logits;               // [M][N] or null
+};
+
+__device__ __forceinline__ float bf(const bf16 v) { return __bfloat162float(v); }
+
+// unpack of pack_argmax's value half
+__device__ __forceinline__ float unpack_argmax_val(unsigned long long p) {
+  uint32_t u = (uint32_t)(p >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ void top2_merge(unsigned long long& a1, unsigned long long& a2, unsigned long long b1,
+                                           unsigned long long b2) {
+  const unsigned long long hi = a1 > b1 ? a1 : b1, lo = a1 > b1 ? b1 : a1;
+  const unsigned long long s = a2 > b2 ? a2 : b2;
+  a1 = hi;
+  a2 = lo > s ? lo : s;
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// q/k RMSNorm + rotate-half RoPE (or plain v) of the heads of one 128-feature QKV tile.  vals: the tile's fp32
+// sums in shared memory, token-major [16][128].  Every head of a tile has the same kind (q, k or v) because the
+// q, k and v row blocks are multiples of 128 rows.  One warp per (token, head); the gain, the positions and the
+// RoPE rows are loaded before any arithmetic so the loads overlap.
+template <int H>
+__device__ __forceinline__ void qkv_tile_epilogue(const StreamParams& p, const float* vals, int tile, const int* s_ctx,
+                                                  int quarter, int lane) {
+  constexpr int NV = H / 32, HPT = SBM / H, NU = SBN * HPT / 4;
+  const int head0 = tile * HPT;
+  const int kind = head0 < p.nq ? 0 : (head0 < p.nq + p.nkv ? 1 : 2);
+  float g[NV];
+  if (kind < 2) {
+    const bf16* gp = kind == 0 ? p.q_norm : p.k_norm;
+#pragma unroll
+    for (int k = 0; k < NV; k++) g[k] = bf(gp[lane + 32 * k]);
+  }
+  float2 cs[NU][NV / 2];
+#pragma unroll
+  for (int i = 0; i < NU; i++) {
+    const int u = quarter + 4 * i, j = u / HPT;
+    if (kind < 2 && j < p.M) {
+      const int pos = s_ctx[j / p.L] + j % p.L;
+#pragma unroll
+      for (int k = 0; k < NV / 2; k++) cs[i][k] = p.rope[(size_t)pos * (H / 2) + lane + 32 * k];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NU; i++) {
+    const int u = quarter + 4 * i, j = u / HPT, hh = u % HPT;
+    if (j >= p.M) continue;
+    const int b = j / p.L, jj = j % p.L, head = head0 + hh;
+    float v[NV];
+#pragma unroll
+    for (int k = 0; k < NV; k++) v[k] = vals[j * SBM + hh * H + lane + 32 * k];
+    bf16* dst;
+    if (kind < 2) {
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < NV; k++) ss += v[k] * v[k];
+      const float inv = rsqrtf(warp_sum(ss) / (float)H + p.eps);
+#pragma unroll
+      for (int k = 0; k < NV; k++) v[k] = v[k] * inv * g[k];
+#pragma unroll
+      for (int k = 0; k < NV / 2; k++) {
+        const float x1 = v[k], x2 = v[k + NV / 2];
+        v[k] = x1 * cs[i][k].x - x2 * cs[i][k].y;
+        v[k + NV / 2] = x2 * cs[i][k].x + x1 * cs[i][k].y;
+      }
+      dst = kind == 0 ? p.q + ((size_t)j * p.nq + head) * H
+                      : p.kblk + (((size_t)b * p.nkv + head - p.nq) * p.L + jj) * H;
+    } else {
+      dst = p.vblk + (((size_t)b * p.nkv + head - p.nq - p.nkv) * p.L + jj) * H;
+    }
+#pragma unroll
+    for (int k = 0; k < NV; k++) dst[lane + 32 * k] = __float2bfloat16_rn(v[k]);
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_constant__ StreamParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int n_act = p.k_split / SBK;                          // activation atoms of one split (LM head: all K)
+  uint8_t* ring = smem;
+  uint8_t* act = smem + kSStages * W_ATOM;
+  uint8_t* gbuf = act + n_act * X_ATOM;
+  float* scratch = reinterpret_cast<float*>(gbuf + n_act * G_ATOM);
+  uint8_t* misc = reinterpret_cast<uint8_t*>(scratch) + kEpiScratch;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + kMiscFlags);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_flag = reinterpret_cast<int*>(tmem_slot + 2);
+  float* s_inv = reinterpret_cast<float*>(misc + kMiscInv);
+  int* s_ctx = reinterpret_cast<int*>(misc + kMiscCtx);
+  unsigned long long* s_run = reinterpret_cast<unsigned long long*>(misc + kMiscRun);
+  const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kSStages, actt = empty0 + 8 * kSStages,
+                 actb = actt + 8, tfull0 = actb + 8, tempty0 = tfull0 + 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  pdl_trigger();
+  const bool persistent = EPI == SEPI_ARGMAX;
+  const int total = persistent ? p.tiles : p.tiles * p.splits;
+  const int stride = persistent ? gridDim.x : total;   // one work item per CTA otherwise
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSStages; s++) {
+      tc::mbar_init(full0 + 8 * s, 1);
+      tc::mbar_init(empty0 + 8 * s, 1);
+    }
+    tc::mbar_init(actt, 1);
+    tc::mbar_init(actb, 1);
+    for (int a = 0; a < 2; a++) {
+      tc::mbar_init(tfull0 + 8 * a, 1);
+      tc::mbar_init(tempty0 + 8 * a, 4);
+    }
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch(&p.tm_w);
+    tc::tma_prefetch(&p.tm_x);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // work item t -> output tile, K range
+  auto item = [&](int t, int& tile, int& split, int& k0, int& nkb) {
+    tile = persistent ? t : t % p.tiles;
+    split = persistent ? 0 : t / p.tiles;
+    k0 = split * p.k_split;
+    nkb = (min(p.K, k0 + p.k_split) - k0) / SBK;
+  };
+  int tile0, split0, k00, nkb0;   // the CTA's first item: its K slice is the activation slice
+  item(blockIdx.x < total ? blockIdx.x : 0, tile0, split0, k00, nkb0);
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0, issued = 0, t = blockIdx.x, kb = 0, tile, split, k0, nkb;
+      uint32_t phase = 0;
+      if (t < total) item(t, tile, split, k0, nkb);
+      auto issue_w = [&]() {
+        const uint32_t fb = full0 + 8 * stage, dst = tc::smem_u32(ring + stage * W_ATOM);
+        tc::mbar_arrive_expect_tx(fb, W_ATOM);
+        if (EPI == SEPI_SWIGLU) {   // atom = [gate rows f0..f0+63 ; up rows F+f0..F+f0+63]
+          tc::tma_load_2d(dst, &p.tm_w, k0 + kb * SBK, tile * 64, fb);
+          tc::tma_load_2d(dst + W_ATOM / 2, &p.tm_w, k0 + kb * SBK, p.N + tile * 64, fb);
+        } else {
+          tc::tma_load_2d(dst, &p.tm_w, k0 + kb * SBK, tile * SBM, fb);
+        }
+        issued++;
+        if (++stage == kSStages) { stage = 0; phase ^= 1; }
+        if (++kb == nkb) {
+          kb = 0;
+          t += stride;
+          if (t < total) item(t, tile, split, k0, nkb);
+        }
+      };
+      // the first ring of weights: weights never depend on earlier kernels, so no griddepcontrol.wait yet
+      while (t < total && issued < kSStages) issue_w();
+      // the activation slice (and the norm gain slice) once the predecessor kernel has completed
+      pdl_wait();
+      if (blockIdx.x < total) {
+        const bool gains = p.xform != XF_COPY;
+        tc::mbar_arrive_expect_tx(actt, nkb0 * p.x_atom_bytes + (gains ? nkb0 * G_ATOM : 0));
+        for (int a = 0; a < nkb0; a++) {
+          if (p.x_rank == 3)
+            tc::tma_load_3d(tc::smem_u32(act + a * X_ATOM), &p.tm_x, k00 + a * SBK, 0, 0, actt);
+          else
+            tc::tma_load_2d(tc::smem_u32(act + a * X_ATOM), &p.tm_x, k00 + a * SBK, 0, actt);
+        }
+        if (gains) tc::bulk_load(tc::smem_u32(gbuf), p.gain + k00, nkb0 * G_ATOM, actt);
+      }
+      while (t < total && !*abort_flag) {
+        if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1)) {
+          *abort_flag = 1;
+          break;
+        }
+        issue_w();
+      }
+      if (*abort_flag) {   // let the copies already issued land before the CTA may exit (bounded)
+        for (int s = 0; s < kSStages && s < issued; s++) {
+          if (--stage < 0) { stage = kSStages - 1; phase ^= 1; }
+          tc::mbar_wait(full0 + 8 * stage, phase);
+        }
+        if (blockIdx.x < total) tc::mbar_wait(actt, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(SBM, SBN);
+      if (!tc::mbar_wait(actb, 0)) *abort_flag = 1;
+      tc::tc_fence_after();
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      const uint32_t xs = tc::smem_u32(act);
+      for (int t = blockIdx.x; t < total; t += stride, it++) {
+        int tile, split, k0, nkb;
+        item(t, tile, split, k0, nkb);
+        const int acc = it & 1;
+        if (it >= 2 && !*abort_flag && !tc::mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1)) *abort_flag = 1;
+        tc::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * SBN;
+        for (int kb = 0; kb < nkb && !*abort_flag; kb++) {
+          if (!tc::mbar_wait(full0 + 8 * stage, phase)) { *abort_flag = 1; break; }
+          tc::tc_fence_after();
+          const uint32_t ws = tc::smem_u32(ring + stage * W_ATOM);
+#pragma unroll
+          for (int kk = 0; kk < SBK / SUK; kk++) {
+            const uint64_t da = tc::sw128_kmajor_desc(ws + kk * SUK * 2);
+            const uint64_t db = tc::sw128_kmajor_desc(xs + kb * X_ATOM + kk * SUK * 2);
+            tc::umma_bf16(d_tmem, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::umma_commit(empty0 + 8 * stage);
+          if (++stage == kSStages) { stage = 0; phase ^= 1; }
+        }
+        tc::umma_commit(tfull0 + 8 * acc);
+      }
+    }
+  } else {
+    // ---------------- activation transform + epilogue: warps 2..5 ----------------
+    const int et = threadIdx.x - 64;          // 0..127
+    const int quarter = warp & 3;             // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int row_in_tile = quarter * 32 + lane;
+    pdl_wait();                               // inputs and outputs belong to earlier kernels
+    if (p.xform == XF_NORM) {                 // 1/rms per token from the residual kernels' partial sums
+      for (int i = et; i < p.n_ss * SBN; i += 128) scratch[i] = __ldcg(p.ss_in + i);
+      epi_bar();
+      if (et < SBN) {
+        float ss = 0.f;
+        for (int t = 0; t < p.n_ss; t++) ss += scratch[t * SBN + et];
+        s_inv[et] = rsqrtf(ss / (float)p.K + p.eps);
+      }
+    }
+    if (EPI == SEPI_QKV && et < SBN) {
+      int cl = et * p.L < p.M ? p.ctx_len[et] : 0;
+      s_ctx[et] = cl < 0 ? 0 : (cl > p.t_cap ? p.t_cap : cl);
+    }
+    if (EPI == SEPI_ARGMAX && et < SBN) s_run[2 * et] = s_run[2 * et + 1] = 0ull;
+    if (blockIdx.x < total && !tc::mbar_wait(actt, 0)) *abort_flag = 1;
+    if (p.xform == XF_NORM_FULL) {            // 1/rms per token over the whole row, read from shared memory
+      for (int j = quarter; j < p.M; j += 4) {
+        float ss = 0.f;
+        for (int a = 0; a < nkb0; a++) {
+          const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162*>(act + a * X_ATOM + j * 128 + lane * 4);
+          ss += bf(e.x) * bf(e.x) + bf(e.y) * bf(e.y);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) s_inv[j] = rsqrtf(ss / (float)p.K + p.eps);
+      }
+    }
+    epi_bar();
+    if (p.xform != XF_COPY) {
+      // xn = bf16(x * inv * g) in place; physical chunk pc of row j holds logical chunk pc ^ (j & 7)
+      const int cpr = nkb0 * 8;
+      for (int c = et; c < p.M * cpr; c += 128) {
+        const int j = c / cpr, cc = c % cpr, a = cc >> 3, pc = cc & 7, q = pc ^ (j & 7);
+        uint4* xp = reinterpret_cast<uint4*>(act + a * X_ATOM + j * 128 + (pc << 4));
+        const uint4 gu = *reinterpret_cast<const uint4*>(gbuf + a * G_ATOM + q * 16);
+        uint4 u = *xp;
+        bf16* e = reinterpret_cast<bf16*>(&u);
+        const bf16* gg = reinterpret_cast<const bf16*>(&gu);
+        const float inv = s_inv[j];
+#pragma unroll
+        for (int i = 0; i < 8; i++) e[i] = __float2bfloat16_rn(bf(e[i]) * inv * bf(gg[i]));
+        *xp = u;
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
+    epi_bar();
+    if (et == 0) tc::mbar_arrive(actb);
+
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += stride, it++) {
+      int tile, split, k0, nkb;
+      item(t, tile, split, k0, nkb);
+      const int acc = it & 1;
+      if (!tc::mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1)) *abort_flag = 1;
+      tc::tc_fence_after();
+      float v[16];
+      tc::tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * SBN, v);
+      if (*abort_flag) {
+#pragma unroll
+        for (int j = 0; j < 16; j++) v[j] = 0.f;
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tempty0 + 8 * acc);
+
+      if (EPI == SEPI_QKV || EPI == SEPI_RESID) {
+        // ---- split-K: partial -> global; the last CTA of the tile reduces in split order ----
+        bool last = true;
+        if (p.splits > 1) {
+          float* mine = p.part + (((size_t)split * p.tiles + tile) * SBN) * SBM + row_in_tile;
+#pragma unroll
+          for (int j = 0; j < 16; j++)
+            if (j < p.M) __stcg(mine + j * SBM, v[j]);
+          __threadfence();
+          epi_bar();
+          if (et == 0) *s_flag = atomicAdd(p.counters + tile, 1) == p.splits - 1;
+          epi_bar();
+          last = *s_flag != 0;
+          if (last) {
+            __threadfence();
+#pragma unroll
+            for (int j = 0; j < 16; j++) v[j] = 0.f;
+            for (int s0 = 0; s0 < p.splits; s0 += 4) {   // four splits' loads in flight, summed in split order
+              float pv[4][16];
+#pragma unroll
+              for (int u = 0; u < 4; u++) {
+                const float* ps = p.part + (((size_t)(s0 + u) * p.tiles + tile) * SBN) * SBM + row_in_tile;
+#pragma unroll
+                for (int j = 0; j < 16; j++) pv[u][j] = (s0 + u < p.splits && j < p.M) ? __ldcg(ps + j * SBM) : 0.f;
+              }
+#pragma unroll
+              for (int u = 0; u < 4; u++)
+#pragma unroll
+                for (int j = 0; j < 16; j++) v[j] += pv[u][j];
+            }
+            if (et == 0) p.counters[tile] = 0;
+          }
+        }
+        if (last) {
+          if (EPI == SEPI_RESID) {
+            // x[j][n] = bf16(x + sum); the tile's share of sum(x^2) per token
+            const int n = tile * SBM + row_in_tile;
+            float xv[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) xv[j] = j < p.M ? bf(p.xres[(size_t)j * p.N + n]) : 0.f;
+            float* red = scratch;   // [4 warps][16]
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+              float sq = 0.f;
+              if (j < p.M) {
+                const bf16 nb = __float2bfloat16_rn(xv[j] + v[j]);
+                p.xres[(size_t)j * p.N + n] = nb;
+                sq = bf(nb) * bf(nb);
+              }
+              sq = warp_sum(sq);
+              if (lane == 0) red[quarter * SBN + j] = sq;
+            }
+            epi_bar();
+            if (et < SBN) p.ss_out[tile * SBN + et] = red[et] + red[SBN + et] + red[2 * SBN + et] + red[3 * SBN + et];
+            epi_bar();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; j++) scratch[j * SBM + row_in_tile] = v[j];
+            epi_bar();
+            if (p.h == 128)
+              qkv_tile_epilogue<128>(p, scratch, tile, s_ctx, quarter, lane);
+            else
+              qkv_tile_epilogue<64>(p, scratch, tile, s_ctx, quarter, lane);
+            epi_bar();
+          }
+        }
+      } else if (EPI == SEPI_SWIGLU) {
+        // TMEM lanes 0..63: gate of features f0 + lane; lanes 64..127: up of the same features
+        float* xch = scratch;   // [64][16]
+        const bool up_half = row_in_tile >= 64;
+        const int fr = up_half ? row_in_tile - 64 : row_in_tile;
+        if (up_half) {
+#pragma unroll
+          for (int j = 0; j < 16; j++) xch[fr * SBN + j] = v[j];
+        }
+        epi_bar();
+        if (!up_half) {
+          const int f = tile * 64 + fr;
+#pragma unroll
+          for (int j = 0; j < 16; j++)
+            if (j < p.M) {
+              const float gv = v[j], uv = xch[fr * SBN + j];
+              p.hmid[(size_t)j * p.N + f] = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+            }
+        }
+        epi_bar();
+      } else {
+        // LM head: ids tile*128 + row, running top-2 per token
+        const int vid = tile * SBM + row_in_tile;
+        const bool ok = vid < p.N;
+        unsigned long long* w2 = reinterpret_cast<unsigned long long*>(scratch);   // [4 warps][16][2]
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+          unsigned long long a1 = (ok && j < p.M) ? pack_argmax(v[j], vid) : 0ull, a2 = 0ull;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, a1, o);
+            const unsigned long long b2 = __shfl_xor_sync(0xffffffffu, a2, o);
+            top2_merge(a1, a2, b1, b2);
+          }
+          if (lane == 0) {
+            w2[(quarter * SBN + j) * 2] = a1;
+            w2[(quarter * SBN + j) * 2 + 1] = a2;
+          }
+          if (p.logits && ok && j < p.M) p.logits[(size_t)j * p.N + vid] = v[j];
+        }
+        epi_bar();
+        if (et < SBN) {
+          unsigned long long r1 = s_run[2 * et], r2 = s_run[2 * et + 1];
+#pragma unroll
+          for (int w = 0; w < 4; w++) top2_merge(r1, r2, w2[(w * SBN + et) * 2], w2[(w * SBN + et) * 2 + 1]);
+          s_run[2 * et] = r1;
+          s_run[2 * et + 1] = r2;
+        }
+        epi_bar();
+      }
+    }
+    if (EPI == SEPI_ARGMAX && et < SBN) {
+      p.slots[((size_t)blockIdx.x * SBN + et) * 2] = s_run[2 * et];
+      p.slots[((size_t)blockIdx.x * SBN + et) * 2 + 1] = s_run[2 * et + 1];
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+size_t stream_smem_bytes(int act_atoms) {
+  return 1024 + (size_t)kSStages * W_ATOM + (size_t)act_atoms * (X_ATOM + G_ATOM) + kEpiScratch + kMiscBytes;
+}
+
+template <int EPI>
+cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
+  const size_t smem = stream_smem_bytes(p.k_split / SBK);
+  return launch_k(stream_gemm_kernel<EPI>, grid, kSThreads, smem, st, p);
+}
+
+// ---- embedding gather for the few-token path: x rows + their sums of squares; clears the split-K counters ---------
+__global__ void embed_ss_kernel(bf16* __restrict__ x, float* __restrict__ ss, int* __restrict__ counters, int n_cnt,
+                                const bf16* __restrict__ embed, const int32_t* __restrict__ anchor, int32_t mask_id,
+                                int L, int d, int V) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[32];
+  const int r = blockIdx.x, b = r / L, j = r % L;
+  if (r == 0)
+    for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) counters[i] = 0;
+  int id = j == 0 ? anchor[b] : mask_id;
+  const bool bad = id < 0 || id >= V;
+  if (bad) {
+    if (threadIdx.x == 0) record_check(kCheckBadToken);
+    id = 0;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(embed + (size_t)id * d);
+  uint4* dx = reinterpret_cast<uint4*>(x + (size_t)r * d);
+  float s = 0.f;
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+    const uint4 u = bad ? make_uint4(0, 0, 0, 0) : src[i];
+    dx[i] = u;
+    const bf16* e = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+    for (int k = 0; k < 8; k++) s += bf(e[k]) * bf(e[k]);
+  }
+  s = warp_sum(s);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); w++) t += red[w];
+    ss[r] = t;   // one partial per token: ss[0][r]
+  }
+}
+
+// ---- argmax decode of the LM-head slots: one warp per position -------------------------------------------------
+__global__ void stream_decode_kernel(int32_t* __restrict__ tokens, float* __restrict__ margin,
+                                     const unsigned long long* __restrict__ slots, int n_slots, int n_rows) {
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= n_rows) return;
+  unsigned long long a1 = 0ull, a2 = 0ull;
+  for (int g = lane; g < n_slots; g += 32)
+    top2_merge(a1, a2, __ldcg(slots + ((size_t)g * SBN + r) * 2), __ldcg(slots + ((size_t)g * SBN + r) * 2 + 1));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, a1, o);
+    const unsigned long long b2 = __shfl_xor_sync(0xffffffffu, a2, o);
+    top2_merge(a1, a2, b1, b2);
+  }
+  if (lane == 0) {
+    if (!a1) record_check(kCheckNoLegalId);
+    tokens[r] = a1 ? unpack_argmax_id(a1) : -1;
+    if (margin)
+      margin[r] = !a1 ? 0.f : (a2 ? (float)((double)unpack_argmax_val(a1) - (double)unpack_argmax_val(a2)) : INFINITY);
+  }
+}
+
+}  // namespace
+
+bool stream_shape_ok(const fpd_model_desc& d) {
+  return d.d_model % SBM == 0 && (d.n_q_heads * d.head_dim) % SBM == 0 && (d.n_kv_heads * d.head_dim) % SBM == 0 &&
+         d.d_ff % 64 == 0 && d.d_model % SBK == 0 && stream_smem_bytes(d.d_model / SBK) <= 227 * 1024;
+}
+
+StreamPlan stream_plan(int tiles, int K, int num_sms, bool split_ok) {
+  StreamPlan pl{};
+  pl.tiles = tiles;
+  const int nkb = K / SBK;
+  int splits = 1;
+  if (split_ok && tiles < num_sms) splits = std::max(1, std::min(num_sms / tiles, nkb / 2));
+  int kb_per = ceil_div(nkb, splits);
+  // the activation slice must fit next to the ring
+  while (stream_smem_bytes(kb_per) > 227 * 1024) kb_per = ceil_div(kb_per, 2);
+  pl.k_split = kb_per * SBK;
+  pl.splits = ceil_div(nkb, kb_per);
+  pl.grid = tiles * pl.splits;
+  return pl;
+}
+
+size_t stream_part_floats(const StreamPlan& pl) { return pl.splits > 1 ? (size_t)pl.splits * pl.tiles * SBN * SBM : 0; }
+
+cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st) {
+  StreamParams p;
+  memset(&p, 0, sizeof(p));
+  const int box_rows = g.epi == SEPI_SWIGLU ? 64 : SBM;
+  const int w_rows = g.epi == SEPI_SWIGLU ? 2 * g.N : g.N;
+  if (g.M < 1 || g.M > SBN || g.K % SBK) return cudaErrorInvalidValue;
+  cudaError_t e = make_tmap(&p.tm_w, g.w, w_rows, g.K, g.K, box_rows);
+  if (e != cudaSuccess) return e;
+  if (g.xform == XF_NORM_FULL) {
+    // rows of the LM head are block positions 1..L-1 of every request: a 3-D view [B][L-1][K] of hidden
+    const int nb = g.M / (g.lm_block - 1);
+    if (nb * (g.lm_block - 1) != g.M) return cudaErrorInvalidValue;
+    const uint64_t dims[3] = {(uint64_t)g.K, (uint64_t)(g.lm_block - 1), (uint64_t)nb};
+    const uint64_t strides[2] = {(uint64_t)g.ldx * 2, (uint64_t)g.lm_block * g.ldx * 2};
+    const uint32_t box[3] = {(uint32_t)SBK, (uint32_t)(g.lm_block - 1), (uint32_t)nb};
+    e = make_tmap_nd(&p.tm_x, g.x + g.ldx, 3, dims, strides, box);
+    p.x_rank = 3;
+    p.x_atom_bytes = (uint32_t)g.M * SBK * 2;
+  } else {
+    e = make_tmap(&p.tm_x, g.x, g.M, g.K, g.ldx, SBN);
+    p.x_rank = 2;
+    p.x_atom_bytes = X_ATOM;
+  }
+  if (e != cudaSuccess) return e;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.tiles = g.plan.tiles;
+  p.splits = g.plan.splits;
+  p.k_split = g.plan.k_split;
+  p.xform = g.xform;
+  p.ss_in = g.ss_in;
+  p.n_ss = g.n_ss;
+  p.gain = g.gain;
+  p.eps = g.eps;
+  p.part = g.part;
+  p.counters = g.counters;
+  p.q = g.q;
+  p.kblk = g.kblk;
+  p.vblk = g.vblk;
+  p.q_norm = g.q_norm;
+  p.k_norm = g.k_norm;
+  p.rope = g.rope;
+  p.ctx_len = g.ctx_len;
+  p.t_cap = g.t_cap;
+  p.L = g.L;
+  p.nq = g.nq;
+  p.nkv = g.nkv;
+  p.h = g.h;
+  p.xres = g.xres;
+  p.ss_out = g.ss_out;
+  p.hmid = g.hmid;
+  p.slots = g.slots;
+  p.logits = g.logits;
+  switch (g.epi) {
+    case SEPI_QKV: return launch_stream<SEPI_QKV>(p, g.plan.grid, st);
+    case SEPI_RESID: return launch_stream<SEPI_RESID>(p, g.plan.grid, st);
+    case SEPI_SWIGLU: return launch_stream<SEPI_SWIGLU>(p, g.plan.grid, st);
+    default: return launch_stream<SEPI_ARGMAX>(p, g.plan.grid, st);
+  }
+}
+
+cudaError_t stream_init_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(stream_gemm_kernel<SEPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_gemm_kernel<SEPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_gemm_kernel<SEPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_gemm_kernel<SEPI_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  return e;
+}
+
+cudaError_t launch_embed_ss(bf16* x, float* ss, int* counters, int n_cnt, const bf16* embed, const int32_t* anchor,
+                            int32_t mask_id, int B, int L, int d, int V, cudaStream_t st) {
+  return launch_k(embed_ss_kernel, B * L, 256, 0, st, x, ss, counters, n_cnt, embed, anchor, mask_id, L, d, V);
+}
+
+cudaError_t launch_stream_decode(int32_t* tokens, float* margin, const unsigned long long* slots, int n_slots,
+                                 int n_rows, cudaStream_t st) {
+  return launch_k(stream_decode_kernel, 1, SBN * 32, 0, st, tokens, margin, slots, n_slots, n_rows);
+}
+
+}  // namespace fpd

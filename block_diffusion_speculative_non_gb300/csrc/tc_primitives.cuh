@@ -69,6 +69,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+// 3-D tiled load of the box at (x, y, z) into shared memory; completes bytes on bar.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"((uint64_t)tm), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+// Contiguous global -> shared copy of `bytes` (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"((uint64_t)src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // ---- TMEM -----------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");
@@ -131,4 +146,11 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 }  // namespace tc
+
+// Row-major bf16 matrix [rows, cols] (row stride ld elements) as a TMA map with boxes of 64 columns x box_rows rows
+// and the 128-byte swizzle (k_gemm_tc.cu).
+cudaError_t make_tmap(CUtensorMap* tm, const void* ptr, int rows, int cols, int ld, int box_rows);
+// bf16 tensor of rank 2 or 3 (dims innermost first, byte strides of dims 1.., box in elements), 128-byte swizzle
+cudaError_t make_tmap_nd(CUtensorMap* tm, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                         const uint32_t* box);
 }  // namespace fpd

@@ -85,11 +85,12 @@ class Drafter:
                         layer_hidden, self.workspace, self.ws_bytes, stream)
         return hidden_out
 
-    def constrain_argmax(self, batch, block_len, hidden, layout=None, tokens_out=None, logits_out=None, stream=None):
+    def constrain_argmax(self, batch, block_len, hidden, layout=None, tokens_out=None, logits_out=None, stream=None,
+                         margin_out=None):
         if tokens_out is None:
             tokens_out = torch.empty(batch, block_len - 1, dtype=torch.int32, device=self.device)
         fpd_constrain_argmax(self.handle, batch, block_len, hidden, layout, tokens_out, logits_out, self.workspace,
-                             self.ws_bytes, stream)
+                             self.ws_bytes, stream, margin_out=margin_out)
         return tokens_out
 
     @staticmethod

@@ -171,10 +171,13 @@ fpd_status fpd_draft_block(fpd_model* model, int batch, int block_len, const voi
  *   hidden      device [batch * L, d] bf16 (fpd_draft_block's hidden_out)
  *   layout      NULL: every position may take any id in [0, V)
  *   tokens_out  device [batch, L-1] int32
- *   logits_out  device [batch * (L-1), V] fp32 or NULL; only legal columns are written */
+ *   logits_out  device [batch * (L-1), V] fp32 or NULL; only legal columns are written
+ *   margin_out  device [batch * (L-1)] fp32 or NULL: the largest minus the second largest fp32 logit over the
+ *               position's legal ids (0 on a tie; +inf when the class has a single legal id).  The margin tells a
+ *               caller how close the argmax decision was. */
 fpd_status fpd_constrain_argmax(fpd_model* model, int batch, int block_len, const void* hidden,
                                 const fpd_vocab_layout* layout, int32_t* tokens_out, float* logits_out,
-                                void* workspace, size_t workspace_bytes, void* stream);
+                                float* margin_out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- a8 without a workspace argument ----------------------------------------------------------------------------
  * The pages have no counterpart to this entry point; it exists for callers that cannot allocate device memory
@@ -182,7 +185,7 @@ fpd_status fpd_constrain_argmax(fpd_model* model, int batch, int block_len, cons
  * loop where cudaMalloc's implicit device synchronisation is not allowed).  It computes exactly what
  * fpd_constrain_argmax computes, with the same arguments minus the workspace: its scratch memory is a fixed
  * 8 MiB array in the library's device memory (present on every device that loads the library until the process
- * exits), so the caller supplies only inputs and outputs.
+ * exits), so the caller supplies only inputs and outputs.  It has no margin output.
  *   - Limit: batch * (block_len - 1) positions whose scratch fits 8 MiB (about 1300 positions at d_model 2560);
  *     larger calls return FPD_ERR_CAPACITY with a message naming the bytes needed, without launching anything.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device

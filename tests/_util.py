@@ -99,3 +99,22 @@ def assert_tokens_chain(gpu_tok, ref_tok, margin, gpu_logits, ref_logits, what="
             bad.append((int(r), float(margin[r]), err))
     assert not bad, f"{what}: ids differ beyond the logit error: {bad[:5]}"
     return int((gpu_tok != ref_tok).sum())
+
+
+def assert_margin(gpu_margin, gpu_logits, ref_margin, ref_logits, what="margin", few: int = 64):
+    """margin_out of fpd_constrain_argmax: exactly the top-1 minus top-2 of the GPU's own fp32 legal logits
+    (+inf with one legal id), and within twice the logit tolerance (the scale of assert_logits) of the oracle's
+    margin, since each of the two logits may move by the logit tolerance."""
+    gpu_margin = np.asarray(gpu_margin, np.float32).reshape(-1)
+    legal = ~np.isnan(ref_logits)
+    block_scale = np.nanmax(np.abs(ref_logits))
+    for r in range(len(gpu_margin)):
+        ids = np.nonzero(legal[r])[0]
+        gl = np.sort(gpu_logits[r, ids].astype(np.float32))[::-1]
+        own = np.float32(np.inf) if len(ids) == 1 else np.float32(float(gl[0]) - float(gl[1]))
+        assert gpu_margin[r] == own, f"{what}: row {r} margin {gpu_margin[r]} != own logits' {own}"
+        if len(ids) == 1:
+            assert np.isinf(ref_margin[r])
+            continue
+        scale = np.max(np.abs(ref_logits[r, ids])) if len(ids) >= few else block_scale
+        assert abs(float(gpu_margin[r]) - ref_margin[r]) <= 2 * REL_TOL * scale, (what, r, gpu_margin[r], ref_margin[r])

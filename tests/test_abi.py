@@ -82,7 +82,8 @@ def test_model_create_rejects_misaligned_weight(fpd):
 def test_null_model_calls(fpd):
     l = fpd.lib()
     assert l.fpd_draft_block(None, 1, 16, 16, 8, 16, 16, 0, 16, None, 16, 1, None) == 1
-    assert l.fpd_constrain_argmax(None, 1, 16, 16, None, 16, None, 16, 1, None) == 1
+    assert l.fpd_constrain_argmax(None, 1, 16, 16, None, 16, None, None, 16, 1, None) == 1
+    assert l.fpd_constrain_argmax_noalloc(None, 1, 16, 16, None, 16, None, None) == 1
     arr = (ctypes.c_void_p * 1)(16)
     assert l.fpd_prepare_context(None, 1, 1, 16, None, arr, 16, 8, 16, 1, None) == 1
     assert l.fpd_kv_store_bytes(None, 1, 1) == 0

@@ -9,7 +9,8 @@ import pytest
 import torch
 
 import synth
-from _util import (assert_logits, assert_rows_close, assert_tokens, assert_tokens_chain, bits_of, dev_i32, f64)
+from _util import (assert_logits, assert_margin, assert_rows_close, assert_tokens, assert_tokens_chain, bits_of,
+                   dev_i32, f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -93,10 +94,12 @@ def _draft_and_compare(pkg, orc, dr, om, kv_ref, t_cap, ctx_len, anchor, mask_id
         if layout is not None:
             lay_1, _ = pkg.Drafter.layout(lay_b, 1, L, DEV)
         lg1 = torch.full((L - 1, s.vocab), float("nan"), dtype=torch.float32, device=DEV)
-        t1 = dr.constrain_argmax(1, L, hid_o, layout=lay_1, logits_out=lg1)
+        mg1 = torch.full((L - 1,), float("nan"), dtype=torch.float32, device=DEV)
+        t1 = dr.constrain_argmax(1, L, hid_o, layout=lay_1, logits_out=lg1, margin_out=mg1)
         torch.cuda.synchronize()
         assert_logits(lg1.cpu().numpy(), o_log, f"request {b} logits from oracle hidden")
         assert_tokens(t1.cpu().numpy()[0], o_tok[0], o_margin, f"request {b} tokens from oracle hidden")
+        assert_margin(mg1.cpu().numpy(), lg1.cpu().numpy(), o_margin, o_log, f"request {b} margin")
     return g_tok, hid
 
 
@@ -139,6 +142,19 @@ def test_tiny_ragged_batch_with_append(pkg, orc):
     _compare_store(dr, kv, ctx_len, B)
     anchor = np.array([5, 6, 7, 4000], np.int32)
     _draft_and_compare(pkg, orc, dr, om, kv, t_cap, ctx_len, anchor, s.vocab - 1, L, B)
+    dr.close()
+
+
+def test_tiny_few_token_batch_ragged(pkg, orc):
+    """Three requests of 5 positions (15 block positions in all: the few-token path), ragged contexts."""
+    s = synth.TINY
+    w = synth.make_weights(s, 4242)
+    ctx_len = np.array([40, 0, 97], np.int32)
+    off = np.concatenate([[0], np.cumsum(ctx_len)]).astype(np.int32)
+    B, L = 3, 5
+    dr, om, kv, _ = _prepare_both(pkg, orc, s, w, off, int(ctx_len.max()), L, B, 4243)
+    _draft_and_compare(pkg, orc, dr, om, kv, int(ctx_len.max()), ctx_len, np.array([3, 4000, 77], np.int32),
+                       s.vocab - 1, L, B)
     dr.close()
 
 

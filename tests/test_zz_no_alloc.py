@@ -41,7 +41,7 @@ def _call_both(pkg, dr, batch, L, hidden, layout):
     log_ref = torch.full((batch * (L - 1), s.vocab), float("nan"), dtype=torch.float32, device=DEV)
     log = torch.full_like(log_ref, float("nan"))
     assert lib.fpd_constrain_argmax(dr.handle, batch, L, hidden.data_ptr(), lay, tok_ref.data_ptr(),
-                                    log_ref.data_ptr(), dr.workspace.data_ptr(), dr.ws_bytes, st) == 0, \
+                                    log_ref.data_ptr(), None, dr.workspace.data_ptr(), dr.ws_bytes, st) == 0, \
         pkg.fpd_last_error()
     assert lib.fpd_constrain_argmax_noalloc(dr.handle, batch, L, hidden.data_ptr(), lay, tok.data_ptr(),
                                             log.data_ptr(), st) == 0, pkg.fpd_last_error()
