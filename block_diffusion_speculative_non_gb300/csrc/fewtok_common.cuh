@@ -1,0 +1,255 @@
+// fewtok_common.cuh — device building blocks of the few-token path (at most 16 block positions per call) used by
+// the weight-streaming kernels of k_stream.cu.  Internal to libfpd.
+//
+// Conventions of that path: the 16 token rows are the N = 16 operand of tcgen05.mma and the weight tile is the
+// M = 128 operand, so an accumulator holds 128 output features (TMEM lanes) x 16 tokens (columns); warps 2..5
+// (128 threads, "epilogue threads") own TMEM lane quarters (warp & 3) and synchronise with named barrier 1.
+#pragma once
+
+#include "fpd_kernels.cuh"
+#include "tc_primitives.cuh"
+
+namespace fpd {
+namespace fewtok {
+
+constexpr int SBM = 128, SBK = 64, SBN = 16, SUK = 16;
+constexpr int W_ATOM = SBM * SBK * 2;   // 16 KB: 128 weight rows x 64 K, 128-byte swizzle
+constexpr int X_ATOM = SBN * SBK * 2;   // 2 KB: 16 tokens x 64 K
+constexpr int G_ATOM = SBK * 2;         // 128 B of RMSNorm gain per K atom
+constexpr int kEpiScratch = SBN * SBM * 4;   // 8 KB: one fp32 output tile, token-major [16][128]
+
+__device__ __forceinline__ float bf(const bf16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// the value half of pack_argmax
+__device__ __forceinline__ float unpack_argmax_val(unsigned long long p) {
+  uint32_t u = (uint32_t)(p >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+
+// (a1, a2) := the two largest of {a1, a2, b1, b2}, given a1 >= a2 and b1 >= b2 (packed words are distinct)
+__device__ __forceinline__ void top2_merge(unsigned long long& a1, unsigned long long& a2, unsigned long long b1,
+                                           unsigned long long b2) {
+  const unsigned long long hi = a1 > b1 ? a1 : b1, lo = a1 > b1 ? b1 : a1;
+  const unsigned long long s = a2 > b2 ? a2 : b2;
+  a1 = hi;
+  a2 = lo > s ? lo : s;
+}
+
+// 1/rms per token from per-(part, token) sums of squares left by the residual epilogues ([n_ss][16], fixed
+// summation order), staged through `stage` (n_ss * 16 floats).  Result in s_inv[16] after the next epi_bar.
+__device__ __forceinline__ void inv_from_partials(const float* ss_in, int n_ss, int d, float eps, float* stage,
+                                                  float* s_inv, int et) {
+  for (int i = et; i < n_ss * SBN; i += 128) stage[i] = __ldcg(ss_in + i);
+  epi_bar();
+  if (et < SBN) {
+    float ss = 0.f;
+    for (int t = 0; t < n_ss; t++) ss += stage[t * SBN + et];
+    s_inv[et] = rsqrtf(ss / (float)d + eps);
+  }
+}
+
+// 1/rms per token over whole rows already in the activation region (LM head: all K atoms resident).
+__device__ __forceinline__ void inv_from_rows(const uint8_t* act, int nkb, int M, int d, float eps, float* s_inv,
+                                              int quarter, int lane) {
+  for (int j = quarter; j < M; j += 4) {
+    float ss = 0.f;
+    for (int a = 0; a < nkb; a++) {   // the swizzle permutes 16-byte chunks within a row: the sum is unaffected
+      const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162*>(act + a * X_ATOM + j * 128 + lane * 4);
+      ss += bf(e.x) * bf(e.x) + bf(e.y) * bf(e.y);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) s_inv[j] = rsqrtf(ss / (float)d + eps);
+  }
+}
+
+// xn = bf16(x * inv[j] * g[k]) in place over nkb TMA-loaded atoms (rows j < M); physical 16-byte chunk pc of row
+// j holds logical chunk pc ^ (j & 7) (128-byte swizzle).  gbuf: the gain slice, 128 bytes per atom.  Thread et
+// takes chunks et, et + 128, ... of every row, so no index needs a division.
+__device__ __forceinline__ void norm_in_place(uint8_t* act, const uint8_t* gbuf, const float* s_inv, int M, int nkb,
+                                              int et) {
+  const int cpr = nkb * 8;
+  for (int j = 0; j < M; j++) {
+    const float inv = s_inv[j];
+    for (int cc = et; cc < cpr; cc += 128) {
+      const int a = cc >> 3, pc = cc & 7, q = pc ^ (j & 7);
+      uint4* xp = reinterpret_cast<uint4*>(act + a * X_ATOM + j * 128 + (pc << 4));
+      const uint4 gu = *reinterpret_cast<const uint4*>(gbuf + a * G_ATOM + q * 16);
+      uint4 u = *xp;
+      __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&u);
+      const __nv_bfloat162* gg = reinterpret_cast<const __nv_bfloat162*>(&gu);
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const float2 xf = __bfloat1622float2(e[i]), gf = __bfloat1622float2(gg[i]);
+        e[i] = __floats2bfloat162_rn(xf.x * inv * gf.x, xf.y * inv * gf.y);
+      }
+      *xp = u;
+    }
+  }
+}
+
+// Split-K without a reduce kernel: every CTA stores its fp32 partial tile ([splits][tiles][16][128]); the last CTA
+// of the tile to arrive (atomic counter, no waiting) sums all partials in split order into v — bit-reproducible —
+// and resets the counter.  Returns true in that CTA.  All 128 epilogue threads call it.  Ordering: the stores of
+// all threads precede thread 0's acquire-release counter update through the CTA barrier (the release is
+// cumulative), and the winner's reads follow its acquire through the second barrier.
+__device__ __forceinline__ bool splitk_last(float (&v)[16], float* part, int* counters, int split, int splits,
+                                            int tile, int tiles, int M, int row_in_tile, int et, int* s_flag) {
+  if (splits <= 1) return true;
+  float* mine = part + (((size_t)split * tiles + tile) * SBN) * SBM + row_in_tile;
+#pragma unroll
+  for (int j = 0; j < 16; j++)
+    if (j < M) __stcg(mine + j * SBM, v[j]);
+  epi_bar();
+  if (et == 0) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(counters + tile) : "memory");
+    *s_flag = old == splits - 1;
+  }
+  epi_bar();
+  if (!*s_flag) return false;
+#pragma unroll
+  for (int j = 0; j < 16; j++) v[j] = 0.f;
+  for (int s0 = 0; s0 < splits; s0 += 4) {   // four splits' loads in flight, summed in split order
+    float pv[4][16];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const float* ps = part + (((size_t)(s0 + u) * tiles + tile) * SBN) * SBM + row_in_tile;
+#pragma unroll
+      for (int j = 0; j < 16; j++) pv[u][j] = (s0 + u < splits && j < M) ? __ldcg(ps + j * SBM) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int j = 0; j < 16; j++) v[j] += pv[u][j];
+  }
+  if (et == 0) counters[tile] = 0;
+  return true;
+}
+
+// The residual-stream values of one 128-column tile that resid_epilogue adds to (loaded early, while the MMAs run:
+// only the tile's own epilogue writes these columns).
+__device__ __forceinline__ void resid_preload(float (&xv)[16], const bf16* x, int N, int tile, int M, int row_in_tile) {
+  const int n = tile * SBM + row_in_tile;
+#pragma unroll
+  for (int j = 0; j < 16; j++) xv[j] = j < M ? bf(x[(size_t)j * N + n]) : 0.f;
+}
+
+// Residual epilogue of one 128-column tile: x[j][n] = bf16(xv + v) (and a copy in layer_out when given), and the
+// tile's share of sum(x^2) per token into ss_out[tile][16].  All 128 epilogue threads call it.
+__device__ __forceinline__ void resid_epilogue(const float (&v)[16], const float (&xv)[16], bf16* x, int N, int tile,
+                                               int M, float* ss_out, bf16* layer_out, float* scratch, int quarter,
+                                               int lane, int et) {
+  const int n = tile * SBM + quarter * 32 + lane;
+  float* red = scratch;   // [4 warps][16]
+#pragma unroll
+  for (int j = 0; j < 16; j++) {
+    float sq = 0.f;
+    if (j < M) {
+      const bf16 nb = __float2bfloat16_rn(xv[j] + v[j]);
+      x[(size_t)j * N + n] = nb;
+      if (layer_out) layer_out[(size_t)j * N + n] = nb;
+      sq = bf(nb) * bf(nb);
+    }
+    sq = warp_sum(sq);
+    if (lane == 0) red[quarter * SBN + j] = sq;
+  }
+  epi_bar();
+  if (et < SBN) ss_out[tile * SBN + et] = red[et] + red[SBN + et] + red[2 * SBN + et] + red[3 * SBN + et];
+  epi_bar();
+}
+
+// SwiGLU epilogue of one 64-feature tile: TMEM lanes 0..63 hold the gate of features f0 + lane, lanes 64..127 the
+// up projection of the same features; hmid[j][f] = bf16(silu(gate) * up).
+__device__ __forceinline__ void swiglu_epilogue(const float (&v)[16], bf16* hmid, int F, int tile, int M,
+                                                float* scratch, int row_in_tile) {
+  float* xch = scratch;   // [64][16]
+  const bool up_half = row_in_tile >= 64;
+  const int fr = up_half ? row_in_tile - 64 : row_in_tile;
+  if (up_half) {
+#pragma unroll
+    for (int j = 0; j < 16; j++) xch[fr * SBN + j] = v[j];
+  }
+  epi_bar();
+  if (!up_half) {
+    const int f = tile * 64 + fr;
+#pragma unroll
+    for (int j = 0; j < 16; j++)
+      if (j < M) {
+        const float gv = v[j], uv = xch[fr * SBN + j];
+        hmid[(size_t)j * F + f] = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+      }
+  }
+  epi_bar();
+}
+
+struct QkvOut {
+  bf16 *q, *kblk, *vblk;           // q [M][nq][h], block keys / values [B][nkv][L][h]
+  const bf16 *q_norm, *k_norm;
+  const float2* rope;              // [positions][h/2] (cos, sin)
+  int M, L, nq, nkv;
+  float eps;
+};
+
+// q/k RMSNorm + rotate-half RoPE at position ctx_len + j (or plain v) of the heads of one 128-feature QKV tile.
+// vals: the tile's fp32 sums in shared memory, token-major [16][128]; s_ctx: context length per request.  Every
+// head of a tile has the same kind (q, k or v) because the q, k and v row blocks are multiples of 128 rows.  One
+// warp per (token, head); the gain and the RoPE rows are loaded before any arithmetic so the loads overlap.
+template <int H>
+__device__ __forceinline__ void qkv_tile_epilogue(const QkvOut& p, const float* vals, int tile, const int* s_ctx,
+                                                  int quarter, int lane) {
+  constexpr int NV = H / 32, HPT = SBM / H, NU = SBN * HPT / 4;
+  const int head0 = tile * HPT;
+  const int kind = head0 < p.nq ? 0 : (head0 < p.nq + p.nkv ? 1 : 2);
+  float g[NV];
+  if (kind < 2) {
+    const bf16* gp = kind == 0 ? p.q_norm : p.k_norm;
+#pragma unroll
+    for (int k = 0; k < NV; k++) g[k] = bf(gp[lane + 32 * k]);
+  }
+  float2 cs[NU][NV / 2];
+#pragma unroll
+  for (int i = 0; i < NU; i++) {
+    const int u = quarter + 4 * i, j = u / HPT;
+    if (kind < 2 && j < p.M) {
+      const int pos = s_ctx[j / p.L] + j % p.L;
+#pragma unroll
+      for (int k = 0; k < NV / 2; k++) cs[i][k] = p.rope[(size_t)pos * (H / 2) + lane + 32 * k];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NU; i++) {
+    const int u = quarter + 4 * i, j = u / HPT, hh = u % HPT;
+    if (j >= p.M) continue;
+    const int b = j / p.L, jj = j % p.L, head = head0 + hh;
+    float v[NV];
+#pragma unroll
+    for (int k = 0; k < NV; k++) v[k] = vals[j * SBM + hh * H + lane + 32 * k];
+    bf16* dst;
+    if (kind < 2) {
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < NV; k++) ss += v[k] * v[k];
+      const float inv = rsqrtf(warp_sum(ss) / (float)H + p.eps);
+#pragma unroll
+      for (int k = 0; k < NV; k++) v[k] = v[k] * inv * g[k];
+#pragma unroll
+      for (int k = 0; k < NV / 2; k++) {
+        const float x1 = v[k], x2 = v[k + NV / 2];
+        v[k] = x1 * cs[i][k].x - x2 * cs[i][k].y;
+        v[k + NV / 2] = x2 * cs[i][k].x + x1 * cs[i][k].y;
+      }
+      dst = kind == 0 ? p.q + ((size_t)j * p.nq + head) * H
+                      : p.kblk + (((size_t)b * p.nkv + head - p.nq) * p.L + jj) * H;
+    } else {
+      dst = p.vblk + (((size_t)b * p.nkv + head - p.nq - p.nkv) * p.L + jj) * H;
+    }
+#pragma unroll
+    for (int k = 0; k < NV; k++) dst[lane + 32 * k] = __float2bfloat16_rn(v[k]);
+  }
+}
+
+}  // namespace fewtok
+}  // namespace fpd

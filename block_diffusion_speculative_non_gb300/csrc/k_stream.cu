@@ -23,20 +23,15 @@
 //     lowest-id ties, and the top-2 margin).
 #include <cstring>
 
-#include "fpd_kernels.cuh"
-#include "tc_primitives.cuh"
+#include "fewtok_common.cuh"
 
 namespace fpd {
 
 namespace {
+using namespace fewtok;
 
-constexpr int SBM = 128, SBK = 64, SBN = 16, SUK = 16;
 constexpr int kSThreads = 192;
 constexpr int kSStages = 8;
-constexpr int W_ATOM = SBM * SBK * 2;   // 16 KB: 128 weight rows x 64 K
-constexpr int X_ATOM = SBN * SBK * 2;   // 2 KB: 16 tokens x 64 K
-constexpr int G_ATOM = SBK * 2;         // 128 B of RMSNorm gain per K atom
-constexpr int kEpiScratch = SBN * SBM * 4;   // 8 KB: one fp32 output tile, token-major
 constexpr int kTmemCols = 32;                 // two 16-column accumulators
 // misc region: mbarriers full[S], empty[S], act_tma, act_full, tfull[2], tempty[2] | TMEM slot, abort, last-CTA
 // flag | inverse RMS per token [16] | context length per request [16] | running top-2 per token [16][2]
@@ -79,83 +74,6 @@ struct StreamParams {
   unsigned long long* slots;   // [gridDim][16][2]
   float* logits;               // [M][N] or null
 };
-
-__device__ __forceinline__ float bf(const bf16 v) { return __bfloat162float(v); }
-
-// unpack of pack_argmax's value half
-__device__ __forceinline__ float unpack_argmax_val(unsigned long long p) {
-  uint32_t u = (uint32_t)(p >> 32);
-  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
-  return __uint_as_float(u);
-}
-
-__device__ __forceinline__ void top2_merge(unsigned long long& a1, unsigned long long& a2, unsigned long long b1,
-                                           unsigned long long b2) {
-  const unsigned long long hi = a1 > b1 ? a1 : b1, lo = a1 > b1 ? b1 : a1;
-  const unsigned long long s = a2 > b2 ? a2 : b2;
-  a1 = hi;
-  a2 = lo > s ? lo : s;
-}
-
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// q/k RMSNorm + rotate-half RoPE (or plain v) of the heads of one 128-feature QKV tile.  vals: the tile's fp32
-// sums in shared memory, token-major [16][128].  Every head of a tile has the same kind (q, k or v) because the
-// q, k and v row blocks are multiples of 128 rows.  One warp per (token, head); the gain, the positions and the
-// RoPE rows are loaded before any arithmetic so the loads overlap.
-template <int H>
-__device__ __forceinline__ void qkv_tile_epilogue(const StreamParams& p, const float* vals, int tile, const int* s_ctx,
-                                                  int quarter, int lane) {
-  constexpr int NV = H / 32, HPT = SBM / H, NU = SBN * HPT / 4;
-  const int head0 = tile * HPT;
-  const int kind = head0 < p.nq ? 0 : (head0 < p.nq + p.nkv ? 1 : 2);
-  float g[NV];
-  if (kind < 2) {
-    const bf16* gp = kind == 0 ? p.q_norm : p.k_norm;
-#pragma unroll
-    for (int k = 0; k < NV; k++) g[k] = bf(gp[lane + 32 * k]);
-  }
-  float2 cs[NU][NV / 2];
-#pragma unroll
-  for (int i = 0; i < NU; i++) {
-    const int u = quarter + 4 * i, j = u / HPT;
-    if (kind < 2 && j < p.M) {
-      const int pos = s_ctx[j / p.L] + j % p.L;
-#pragma unroll
-      for (int k = 0; k < NV / 2; k++) cs[i][k] = p.rope[(size_t)pos * (H / 2) + lane + 32 * k];
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < NU; i++) {
-    const int u = quarter + 4 * i, j = u / HPT, hh = u % HPT;
-    if (j >= p.M) continue;
-    const int b = j / p.L, jj = j % p.L, head = head0 + hh;
-    float v[NV];
-#pragma unroll
-    for (int k = 0; k < NV; k++) v[k] = vals[j * SBM + hh * H + lane + 32 * k];
-    bf16* dst;
-    if (kind < 2) {
-      float ss = 0.f;
-#pragma unroll
-      for (int k = 0; k < NV; k++) ss += v[k] * v[k];
-      const float inv = rsqrtf(warp_sum(ss) / (float)H + p.eps);
-#pragma unroll
-      for (int k = 0; k < NV; k++) v[k] = v[k] * inv * g[k];
-#pragma unroll
-      for (int k = 0; k < NV / 2; k++) {
-        const float x1 = v[k], x2 = v[k + NV / 2];
-        v[k] = x1 * cs[i][k].x - x2 * cs[i][k].y;
-        v[k + NV / 2] = x2 * cs[i][k].x + x1 * cs[i][k].y;
-      }
-      dst = kind == 0 ? p.q + ((size_t)j * p.nq + head) * H
-                      : p.kblk + (((size_t)b * p.nkv + head - p.nq) * p.L + jj) * H;
-    } else {
-      dst = p.vblk + (((size_t)b * p.nkv + head - p.nq - p.nkv) * p.L + jj) * H;
-    }
-#pragma unroll
-    for (int k = 0; k < NV; k++) dst[lane + 32 * k] = __float2bfloat16_rn(v[k]);
-  }
-}
 
 template <int EPI>
 __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_constant__ StreamParams p) {
@@ -311,49 +229,16 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
     const int quarter = warp & 3;             // TMEM lanes [32*quarter, 32*quarter + 32)
     const int row_in_tile = quarter * 32 + lane;
     pdl_wait();                               // inputs and outputs belong to earlier kernels
-    if (p.xform == XF_NORM) {                 // 1/rms per token from the residual kernels' partial sums
-      for (int i = et; i < p.n_ss * SBN; i += 128) scratch[i] = __ldcg(p.ss_in + i);
-      epi_bar();
-      if (et < SBN) {
-        float ss = 0.f;
-        for (int t = 0; t < p.n_ss; t++) ss += scratch[t * SBN + et];
-        s_inv[et] = rsqrtf(ss / (float)p.K + p.eps);
-      }
-    }
+    if (p.xform == XF_NORM) inv_from_partials(p.ss_in, p.n_ss, p.K, p.eps, scratch, s_inv, et);
     if (EPI == SEPI_QKV && et < SBN) {
       int cl = et * p.L < p.M ? p.ctx_len[et] : 0;
       s_ctx[et] = cl < 0 ? 0 : (cl > p.t_cap ? p.t_cap : cl);
     }
     if (EPI == SEPI_ARGMAX && et < SBN) s_run[2 * et] = s_run[2 * et + 1] = 0ull;
     if (blockIdx.x < total && !tc::mbar_wait(actt, 0)) *abort_flag = 1;
-    if (p.xform == XF_NORM_FULL) {            // 1/rms per token over the whole row, read from shared memory
-      for (int j = quarter; j < p.M; j += 4) {
-        float ss = 0.f;
-        for (int a = 0; a < nkb0; a++) {
-          const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162*>(act + a * X_ATOM + j * 128 + lane * 4);
-          ss += bf(e.x) * bf(e.x) + bf(e.y) * bf(e.y);
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) s_inv[j] = rsqrtf(ss / (float)p.K + p.eps);
-      }
-    }
+    if (p.xform == XF_NORM_FULL) inv_from_rows(act, nkb0, p.M, p.K, p.eps, s_inv, quarter, lane);
     epi_bar();
-    if (p.xform != XF_COPY) {
-      // xn = bf16(x * inv * g) in place; physical chunk pc of row j holds logical chunk pc ^ (j & 7)
-      const int cpr = nkb0 * 8;
-      for (int c = et; c < p.M * cpr; c += 128) {
-        const int j = c / cpr, cc = c % cpr, a = cc >> 3, pc = cc & 7, q = pc ^ (j & 7);
-        uint4* xp = reinterpret_cast<uint4*>(act + a * X_ATOM + j * 128 + (pc << 4));
-        const uint4 gu = *reinterpret_cast<const uint4*>(gbuf + a * G_ATOM + q * 16);
-        uint4 u = *xp;
-        bf16* e = reinterpret_cast<bf16*>(&u);
-        const bf16* gg = reinterpret_cast<const bf16*>(&gu);
-        const float inv = s_inv[j];
-#pragma unroll
-        for (int i = 0; i < 8; i++) e[i] = __float2bfloat16_rn(bf(e[i]) * inv * bf(gg[i]));
-        *xp = u;
-      }
-    }
+    if (p.xform != XF_COPY) norm_in_place(act, gbuf, s_inv, p.M, nkb0, et);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
     epi_bar();
     if (et == 0) tc::mbar_arrive(actb);
@@ -363,6 +248,8 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       int tile, split, k0, nkb;
       item(t, tile, split, k0, nkb);
       const int acc = it & 1;
+      float xv[16];
+      if (EPI == SEPI_RESID) resid_preload(xv, p.xres, p.N, tile, p.M, row_in_tile);
       if (!tc::mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1)) *abort_flag = 1;
       tc::tc_fence_after();
       float v[16];
@@ -376,91 +263,34 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       if (lane == 0) tc::mbar_arrive(tempty0 + 8 * acc);
 
       if (EPI == SEPI_QKV || EPI == SEPI_RESID) {
-        // ---- split-K: partial -> global; the last CTA of the tile reduces in split order ----
-        bool last = true;
-        if (p.splits > 1) {
-          float* mine = p.part + (((size_t)split * p.tiles + tile) * SBN) * SBM + row_in_tile;
-#pragma unroll
-          for (int j = 0; j < 16; j++)
-            if (j < p.M) __stcg(mine + j * SBM, v[j]);
-          __threadfence();
-          epi_bar();
-          if (et == 0) *s_flag = atomicAdd(p.counters + tile, 1) == p.splits - 1;
-          epi_bar();
-          last = *s_flag != 0;
-          if (last) {
-            __threadfence();
-#pragma unroll
-            for (int j = 0; j < 16; j++) v[j] = 0.f;
-            for (int s0 = 0; s0 < p.splits; s0 += 4) {   // four splits' loads in flight, summed in split order
-              float pv[4][16];
-#pragma unroll
-              for (int u = 0; u < 4; u++) {
-                const float* ps = p.part + (((size_t)(s0 + u) * p.tiles + tile) * SBN) * SBM + row_in_tile;
-#pragma unroll
-                for (int j = 0; j < 16; j++) pv[u][j] = (s0 + u < p.splits && j < p.M) ? __ldcg(ps + j * SBM) : 0.f;
-              }
-#pragma unroll
-              for (int u = 0; u < 4; u++)
-#pragma unroll
-                for (int j = 0; j < 16; j++) v[j] += pv[u][j];
-            }
-            if (et == 0) p.counters[tile] = 0;
-          }
-        }
-        if (last) {
+        if (splitk_last(v, p.part, p.counters, split, p.splits, tile, p.tiles, p.M, row_in_tile, et, s_flag)) {
           if (EPI == SEPI_RESID) {
-            // x[j][n] = bf16(x + sum); the tile's share of sum(x^2) per token
-            const int n = tile * SBM + row_in_tile;
-            float xv[16];
-#pragma unroll
-            for (int j = 0; j < 16; j++) xv[j] = j < p.M ? bf(p.xres[(size_t)j * p.N + n]) : 0.f;
-            float* red = scratch;   // [4 warps][16]
-#pragma unroll
-            for (int j = 0; j < 16; j++) {
-              float sq = 0.f;
-              if (j < p.M) {
-                const bf16 nb = __float2bfloat16_rn(xv[j] + v[j]);
-                p.xres[(size_t)j * p.N + n] = nb;
-                sq = bf(nb) * bf(nb);
-              }
-              sq = warp_sum(sq);
-              if (lane == 0) red[quarter * SBN + j] = sq;
-            }
-            epi_bar();
-            if (et < SBN) p.ss_out[tile * SBN + et] = red[et] + red[SBN + et] + red[2 * SBN + et] + red[3 * SBN + et];
-            epi_bar();
+            resid_epilogue(v, xv, p.xres, p.N, tile, p.M, p.ss_out, nullptr, scratch, quarter, lane, et);
           } else {
 #pragma unroll
             for (int j = 0; j < 16; j++) scratch[j * SBM + row_in_tile] = v[j];
             epi_bar();
+            QkvOut qo;
+            qo.q = p.q;
+            qo.kblk = p.kblk;
+            qo.vblk = p.vblk;
+            qo.q_norm = p.q_norm;
+            qo.k_norm = p.k_norm;
+            qo.rope = p.rope;
+            qo.M = p.M;
+            qo.L = p.L;
+            qo.nq = p.nq;
+            qo.nkv = p.nkv;
+            qo.eps = p.eps;
             if (p.h == 128)
-              qkv_tile_epilogue<128>(p, scratch, tile, s_ctx, quarter, lane);
+              qkv_tile_epilogue<128>(qo, scratch, tile, s_ctx, quarter, lane);
             else
-              qkv_tile_epilogue<64>(p, scratch, tile, s_ctx, quarter, lane);
+              qkv_tile_epilogue<64>(qo, scratch, tile, s_ctx, quarter, lane);
             epi_bar();
           }
         }
       } else if (EPI == SEPI_SWIGLU) {
-        // TMEM lanes 0..63: gate of features f0 + lane; lanes 64..127: up of the same features
-        float* xch = scratch;   // [64][16]
-        const bool up_half = row_in_tile >= 64;
-        const int fr = up_half ? row_in_tile - 64 : row_in_tile;
-        if (up_half) {
-#pragma unroll
-          for (int j = 0; j < 16; j++) xch[fr * SBN + j] = v[j];
-        }
-        epi_bar();
-        if (!up_half) {
-          const int f = tile * 64 + fr;
-#pragma unroll
-          for (int j = 0; j < 16; j++)
-            if (j < p.M) {
-              const float gv = v[j], uv = xch[fr * SBN + j];
-              p.hmid[(size_t)j * p.N + f] = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
-            }
-        }
-        epi_bar();
+        swiglu_epilogue(v, p.hmid, p.N, tile, p.M, scratch, row_in_tile);
       } else {
         // LM head: ids tile*128 + row, running top-2 per token
         const int vid = tile * SBM + row_in_tile;
