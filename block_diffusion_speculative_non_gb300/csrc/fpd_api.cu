@@ -81,6 +81,9 @@ struct DraftWs {
   float2* ml;
   int att_splits, att_chunk;
   TcPlan p_qkv, p_o, p_sw, p_down;
+  // many-token path: token-tile GEMMs with fused epilogues; sums of squares [column tiles][M]
+  bool tok;
+  float* ss_tok;
   // few-token path (k_stream.cu)
   bool stream;
   StreamPlan s_qkv, s_o, s_sw, s_down;
@@ -121,8 +124,35 @@ DraftWs carve_draft_stream(const Model& m, Carver& c, int B, int L, int t_cap) {
   return w;
 }
 
+// More than 64 block positions: token tiles on the 128-row MMA operand, epilogues fused into the GEMMs.
+constexpr int kTokMinRows = 65;
+
+DraftWs carve_draft_tok(const Model& m, Carver& c, int B, int L, int t_cap) {
+  const auto& d = m.d;
+  DraftWs w{};
+  w.tok = true;
+  const int M = B * L;
+  const int nqkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim, nqh = d.n_q_heads * d.head_dim;
+  w.p_qkv = tc_plan_tok(M, nqkv, d.d_model, m.num_sms);
+  w.p_o = tc_plan_tok(M, d.d_model, nqh, m.num_sms);
+  w.p_sw = tc_plan_swiglu(M, d.d_ff, d.d_model, m.num_sms);
+  w.p_down = tc_plan_tok(M, d.d_model, d.d_ff, m.num_sms);
+  w.xn = c.take<bf16>((size_t)M * d.d_model);
+  w.q = c.take<bf16>((size_t)M * nqh);
+  w.kblk = c.take<bf16>((size_t)M * d.n_kv_heads * d.head_dim);
+  w.vblk = c.take<bf16>((size_t)M * d.n_kv_heads * d.head_dim);
+  w.o = c.take<bf16>((size_t)M * nqh);
+  w.hmid = c.take<bf16>((size_t)M * d.d_ff);
+  w.ss_tok = c.take<float>((size_t)ceil_div(d.d_model, 128) * M);
+  attn_plan(B, L, d.n_q_heads, d.n_kv_heads, t_cap, m.num_sms, &w.att_splits, &w.att_chunk);
+  w.o_part = c.take<float>((size_t)w.att_splits * M * nqh);
+  w.ml = c.take<float2>((size_t)w.att_splits * M * d.n_q_heads);
+  return w;
+}
+
 DraftWs carve_draft(const Model& m, Carver& c, int B, int L, int t_cap) {
   if (use_stream(m, B, L)) return carve_draft_stream(m, c, B, L, t_cap);
+  if (B * L >= kTokMinRows) return carve_draft_tok(m, c, B, L, t_cap);
   const auto& d = m.d;
   DraftWs w{};
   const int M = B * L;
@@ -567,6 +597,59 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
   FPD_CUDA(launch_embed_norm(x, w.xn, (const bf16*)m->w.embed, anchor, mask_id, (const bf16*)m->w.attn_norm[0], batch,
                              L, dm, d.vocab, d.rms_eps, st),
            "embed + attention norm");
+  if (w.tok) {
+    for (int l = 0; l < d.n_layers; l++) {
+      TokGemm g{};
+      g.qkv = true;
+      g.x = w.xn;
+      g.w = (const bf16*)m->w.wqkv[l];
+      g.M = M;
+      g.N = nqkv;
+      g.K = dm;
+      g.q = w.q;
+      g.kblk = w.kblk;
+      g.vblk = w.vblk;
+      g.q_norm = (const bf16*)m->w.q_norm[l];
+      g.k_norm = (const bf16*)m->w.k_norm[l];
+      g.rope = m->rope;
+      g.ctx_len = ctx_len;
+      g.t_cap = t_cap;
+      g.L = L;
+      g.nq = nq;
+      g.nkv = nkv;
+      g.hd = h;
+      g.eps = d.rms_eps;
+      FPD_CUDA(launch_tc_tok(g, w.p_qkv, st), "QKV GEMM + q/k norm + RoPE");
+      a.layer = l;
+      FPD_CUDA(launch_attention(a, w.o, st), "attention");
+      TokGemm r{};
+      r.qkv = false;
+      r.x = w.o;
+      r.w = (const bf16*)m->w.wo[l];
+      r.M = M;
+      r.N = dm;
+      r.K = nq * h;
+      r.xres = x;
+      r.ss_part = w.ss_tok;
+      FPD_CUDA(launch_tc_tok(r, w.p_o, st), "O GEMM + residual");
+      FPD_CUDA(launch_norm_rows(w.xn, x, w.ss_tok, w.p_o.qt, (const bf16*)m->w.mlp_norm[l], M, dm, d.rms_eps, st),
+               "MLP norm");
+      FPD_CUDA(launch_tc_swiglu(w.xn, M, dm, (const bf16*)m->w.w_gate_up[l], F, w.hmid, w.p_sw, st), "gate/up + SwiGLU");
+      r.x = w.hmid;
+      r.w = (const bf16*)m->w.w_down[l];
+      r.K = F;
+      FPD_CUDA(launch_tc_tok(r, w.p_down, st), "down GEMM + residual");
+      if (l + 1 < d.n_layers)
+        FPD_CUDA(launch_norm_rows(w.xn, x, w.ss_tok, w.p_down.qt, (const bf16*)m->w.attn_norm[l + 1], M, dm, d.rms_eps,
+                                  st),
+                 "attention norm");
+      if (layer_hidden)
+        FPD_CUDA(cudaMemcpyAsync((bf16*)layer_hidden + (size_t)l * M * dm, x, (size_t)M * dm * sizeof(bf16),
+                                 cudaMemcpyDeviceToDevice, st),
+                 "layer_hidden copy");
+    }
+    return FPD_OK;
+  }
   auto gemm = [&](const bf16* A, int K, const void* W, int N, const TcPlan& pl) {
     GemmArgs g{};
     g.a[0] = A;

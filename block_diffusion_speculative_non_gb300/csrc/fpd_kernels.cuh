@@ -37,6 +37,28 @@ TcPlan tc_plan_swiglu(int M, int F, int K, int num_sms);
 // hmid[M][F] = bf16(silu(x . Wg^T) * (x . Wu^T)) with W = [Wg; Wu] ([2F, K]), one tcgen05 pass
 cudaError_t launch_tc_swiglu(const bf16* x, int M, int K, const bf16* w_gate_up, int F, bf16* hmid, const TcPlan& pl,
                              cudaStream_t st);
+// Token-tile GEMMs (many tokens) with the layer epilogue fused: qkv = true — q/k RMSNorm + RoPE, bf16 q / block
+// k / block v; qkv = false — residual add into xres and per-(column tile, token) sums of squares into ss_part
+// [N / plan.bn][M].  W [N, K] weights, x [M, K] activations; no split-K.
+struct TokGemm {
+  bool qkv;
+  const bf16* x;
+  const bf16* w;
+  int M, N, K;
+  bf16 *q, *kblk, *vblk;
+  const bf16 *q_norm, *k_norm;
+  const float2* rope;
+  const int32_t* ctx_len;
+  int t_cap, L, nq, nkv, hd;
+  float eps;
+  bf16* xres;
+  float* ss_part;
+};
+TcPlan tc_plan_tok(int M, int N, int K, int num_sms);
+cudaError_t launch_tc_tok(const TokGemm& g, const TcPlan& pl, cudaStream_t st);
+// xn[m][k] = bf16(x[m][k] * rsqrt(sum_t ss_part[t][m] / d + eps) * g[k]), one warp per row
+cudaError_t launch_norm_rows(bf16* xn, const bf16* x, const float* ss_part, int n_part, const bf16* g, int M, int d,
+                             float eps, cudaStream_t st);
 cudaError_t tc_init_attributes();     // once per process, before any stream capture
 void tc_set_swap_variant(int v);      // tuning sweeps only (fpd_test_set_variant)
 cudaError_t attn_init_attributes();

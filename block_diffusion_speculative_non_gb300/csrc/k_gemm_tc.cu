@@ -35,7 +35,7 @@ namespace {
 
 constexpr int BM = 128, BK = 64, UMMA_K = 16;
 constexpr int kThreads = 192;
-enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_SWIGLU = 2 };
+enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_SWIGLU = 2, EPI_QKV_TOK = 3, EPI_RESID_TOK = 4 };
 
 struct TcParams {
   CUtensorMap tm_x[8];   // activation K-segments (box rows: BN if swap else 128)
@@ -61,6 +61,16 @@ struct TcParams {
   // EPI_SWIGLU: W = [gate; up] rows [2F, K]; output hmid[M][F] = bf16(silu(gate) * up)
   bf16* hmid;
   int F;
+  // EPI_QKV_TOK (token tiles): per head q/k RMSNorm + RoPE at position ctx_len[b] + j, bf16 q / block k / block v
+  bf16 *q, *kblk, *vblk;
+  const bf16 *q_norm, *k_norm;
+  const float2* rope;
+  const int32_t* ctx_len;
+  int t_cap, L, nq, nkv, hd;
+  float eps;
+  // EPI_RESID_TOK (token tiles): x[m][n] = bf16(x + acc); ss_part[column tile][m] = that tile's sum of x^2
+  bf16* xres;
+  float* ss_part;
 };
 
 // A pipeline stage holds KS consecutive 64-element K atoms of both operands: [A atoms][B atoms].  Several
@@ -326,6 +336,104 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             }
           }
         }
+      } else if (EPI == EPI_QKV_TOK) {
+        // token m = a_row0 + row_in_tile holds the tile's BN features: whole heads, so the per-head RMSNorm and the
+        // rotate-half pairs (i, i + hd/2) are in this thread's registers.  tcgen05.ld is warp-wide: every lane
+        // loads, only rows below M store.
+        const int m = w.a_row0 + row_in_tile;
+        const bool mok = m < p.M;
+        const int b = mok ? m / p.L : 0, j = mok ? m % p.L : 0;
+        int cl = mok ? p.ctx_len[b] : 0;
+        cl = cl < 0 ? 0 : (cl > p.t_cap ? p.t_cap : cl);
+        const int hh = p.hd / 2;
+        const float2* rope_row = p.rope + (size_t)(cl + j) * hh;
+#pragma unroll 1
+        for (int h0 = 0; h0 < BN && w.b_row0 + h0 < p.N; h0 += p.hd) {
+          const int head = (w.b_row0 + h0) / p.hd;
+          const int kind = head < p.nq ? 0 : (head < p.nq + p.nkv ? 1 : 2);
+          bf16* dst = kind == 0 ? p.q + ((size_t)m * p.nq + head) * p.hd
+                    : kind == 1 ? p.kblk + (((size_t)b * p.nkv + head - p.nq) * p.L + j) * p.hd
+                                : p.vblk + (((size_t)b * p.nkv + head - p.nq - p.nkv) * p.L + j) * p.hd;
+          if (kind == 2) {
+#pragma unroll 1
+            for (int c = 0; c < p.hd; c += 16) {
+              float v[16];
+              tc::tmem_ld16(t_acc + h0 + c, v);
+              uint4 pk[2];
+              bf16* pe = reinterpret_cast<bf16*>(pk);
+#pragma unroll
+              for (int e = 0; e < 16; e++) pe[e] = __float2bfloat16_rn(v[e]);
+              if (mok) {
+                reinterpret_cast<uint4*>(dst + c)[0] = pk[0];
+                reinterpret_cast<uint4*>(dst + c)[1] = pk[1];
+              }
+            }
+            continue;
+          }
+          float ss = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < p.hd; c += 16) {
+            float v[16];
+            tc::tmem_ld16(t_acc + h0 + c, v);
+#pragma unroll
+            for (int e = 0; e < 16; e++) ss += v[e] * v[e];
+          }
+          const float inv = rsqrtf(ss / (float)p.hd + p.eps);
+          const bf16* gain = kind == 0 ? p.q_norm : p.k_norm;
+#pragma unroll 1
+          for (int c = 0; c < hh; c += 16) {
+            float a[16], bb[16];
+            tc::tmem_ld16(t_acc + h0 + c, a);
+            tc::tmem_ld16(t_acc + h0 + c + hh, bb);
+            uint4 g1u[2], g2u[2], o1[2], o2[2];
+            g1u[0] = reinterpret_cast<const uint4*>(gain + c)[0];
+            g1u[1] = reinterpret_cast<const uint4*>(gain + c)[1];
+            g2u[0] = reinterpret_cast<const uint4*>(gain + c + hh)[0];
+            g2u[1] = reinterpret_cast<const uint4*>(gain + c + hh)[1];
+            const bf16* g1 = reinterpret_cast<const bf16*>(g1u);
+            const bf16* g2 = reinterpret_cast<const bf16*>(g2u);
+            bf16* e1 = reinterpret_cast<bf16*>(o1);
+            bf16* e2 = reinterpret_cast<bf16*>(o2);
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+              const float2 cs = rope_row[c + e];
+              const float x1 = a[e] * inv * __bfloat162float(g1[e]), x2 = bb[e] * inv * __bfloat162float(g2[e]);
+              e1[e] = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
+              e2[e] = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
+            }
+            if (mok) {
+              reinterpret_cast<uint4*>(dst + c)[0] = o1[0];
+              reinterpret_cast<uint4*>(dst + c)[1] = o1[1];
+              reinterpret_cast<uint4*>(dst + c + hh)[0] = o2[0];
+              reinterpret_cast<uint4*>(dst + c + hh)[1] = o2[1];
+            }
+          }
+        }
+      } else if (EPI == EPI_RESID_TOK) {
+        // token m: x[m][n] = bf16(x + acc) over the tile's columns, and this column tile's share of sum(x^2)
+        const int m = w.a_row0 + row_in_tile;
+        const bool mok = m < p.M;
+        float ss = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tc::tmem_ld16(t_acc + c0, v);
+          const int n0 = w.b_row0 + c0;
+          if (mok && n0 + 16 <= p.N) {
+            uint4* xp = reinterpret_cast<uint4*>(p.xres + (size_t)m * p.N + n0);
+            uint4 xu[2] = {xp[0], xp[1]};
+            bf16* xe = reinterpret_cast<bf16*>(xu);
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+              xe[e] = __float2bfloat16_rn(__bfloat162float(xe[e]) + v[e]);
+              const float f = __bfloat162float(xe[e]);
+              ss += f * f;
+            }
+            xp[0] = xu[0];
+            xp[1] = xu[1];
+          }
+        }
+        if (mok) p.ss_part[(size_t)(w.b_row0 / BN) * p.M + m] = ss;
       } else if (EPI == EPI_SWIGLU) {
         if (SWAP) {
           // lanes 0..63: gate of feature f0 + lane; lanes 64..127: up of feature f0 + lane - 64
@@ -539,7 +647,66 @@ cudaError_t tc_init_attributes() {
   if (e == cudaSuccess) e = set_attr<32, 8, true, EPI_SWIGLU>();
   if (e == cudaSuccess) e = set_attr<64, 6, true, EPI_SWIGLU>();
   if (e == cudaSuccess) e = set_attr<256, 4, false, EPI_SWIGLU>();
+  if (e == cudaSuccess) e = set_attr<128, 6, false, EPI_QKV_TOK>();
+  if (e == cudaSuccess) e = set_attr<256, 4, false, EPI_QKV_TOK>();
+  if (e == cudaSuccess) e = set_attr<128, 6, false, EPI_RESID_TOK>();
+  if (e == cudaSuccess) e = set_attr<256, 4, false, EPI_RESID_TOK>();
   return e;
+}
+
+// Token-tile plan for the fused epilogues (no split-K: the epilogue needs complete sums).  Wide weight tiles
+// (256) when they still give every SM a tile, else 128.
+TcPlan tc_plan_tok(int M, int N, int K, int num_sms) {
+  TcPlan pl{};
+  pl.swap = false;
+  pl.pt = ceil_div(M, BM);
+  pl.bn = pl.pt * ceil_div(N, 256) >= num_sms ? 256 : 128;
+  pl.qt = ceil_div(N, pl.bn);
+  pl.splits = 1;
+  pl.k_split = K;
+  pl.grid = std::min(pl.pt * pl.qt, num_sms);
+  return pl;
+}
+
+cudaError_t launch_tc_tok(const TokGemm& g, const TcPlan& pl, cudaStream_t st) {
+  if (g.M <= 0) return cudaSuccess;
+  if (g.K % BK || pl.swap || pl.splits != 1) return cudaErrorInvalidValue;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  cudaError_t e = make_tmap(&p.tm_x[0], g.x, g.M, g.K, g.K, BM);
+  if (e != cudaSuccess) return e;
+  e = make_tmap(&p.tm_w, g.w, g.N, g.K, g.K, pl.bn);
+  if (e != cudaSuccess) return e;
+  p.n_seg = 1;
+  p.seg_k = g.K;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.pt = pl.pt;
+  p.qt = pl.qt;
+  p.splits = 1;
+  p.k_split = g.K;
+  p.q = g.q;
+  p.kblk = g.kblk;
+  p.vblk = g.vblk;
+  p.q_norm = g.q_norm;
+  p.k_norm = g.k_norm;
+  p.rope = g.rope;
+  p.ctx_len = g.ctx_len;
+  p.t_cap = g.t_cap;
+  p.L = g.L;
+  p.nq = g.nq;
+  p.nkv = g.nkv;
+  p.hd = g.hd;
+  p.eps = g.eps;
+  p.xres = g.xres;
+  p.ss_part = g.ss_part;
+  if (g.qkv) {
+    if (pl.bn == 128) return launch_kernel<128, 6, false, EPI_QKV_TOK>(p, pl.grid, st);
+    return launch_kernel<256, 4, false, EPI_QKV_TOK>(p, pl.grid, st);
+  }
+  if (pl.bn == 128) return launch_kernel<128, 6, false, EPI_RESID_TOK>(p, pl.grid, st);
+  return launch_kernel<256, 4, false, EPI_RESID_TOK>(p, pl.grid, st);
 }
 
 TcPlan tc_plan_gemm(int M, int N, int K, int num_sms) {

@@ -216,6 +216,39 @@ cudaError_t launch_residual_norm(bf16* x, bf16* xn, const float* part, int nspli
   return launch_k(residual_norm_kernel<16>, rows, 1024, 0, st, x, xn, part, nsplit, split_stride, g, d, eps);
 }
 
+// ---- RMSNorm of rows whose sums of squares were left by the residual GEMM epilogue: one warp per row -------------
+__global__ void norm_rows_kernel(bf16* __restrict__ xn, const bf16* __restrict__ x, const float* __restrict__ ss_part,
+                                 int n_part, const bf16* __restrict__ g, int M, int d, float eps) {
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= M) return;
+  float ss = 0.f;
+  for (int t = 0; t < n_part; t++) ss += __ldcg(ss_part + (size_t)t * M + r);   // fixed order: reproducible
+  const float inv = rsqrtf(ss / (float)d + eps);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)r * d);
+  const uint4* gs = reinterpret_cast<const uint4*>(g);
+  uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)r * d);
+  for (int c = lane; c < d / 8; c += 32) {
+    uint4 u = src[c];
+    const uint4 gu = gs[c];
+    __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&u);
+    const __nv_bfloat162* ge = reinterpret_cast<const __nv_bfloat162*>(&gu);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const float2 xf = __bfloat1622float2(e[i]), gf = __bfloat1622float2(ge[i]);
+      e[i] = __floats2bfloat162_rn(xf.x * inv * gf.x, xf.y * inv * gf.y);
+    }
+    dst[c] = u;
+  }
+}
+
+cudaError_t launch_norm_rows(bf16* xn, const bf16* x, const float* ss_part, int n_part, const bf16* g, int M, int d,
+                             float eps, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  return launch_k(norm_rows_kernel, ceil_div(M, 8), 256, 0, st, xn, x, ss_part, n_part, g, M, d, eps);
+}
+
 // ---- embedding gather fused with the first RMSNorm ----------------------------------------------------------------
 __global__ void embed_norm_kernel(bf16* __restrict__ x, bf16* __restrict__ xn, const bf16* __restrict__ embed,
                                   const int32_t* __restrict__ anchor, int32_t mask_id, const bf16* __restrict__ g,

@@ -4,10 +4,13 @@ Tolerances: hidden states, K/V and logits agree with the oracle within a max rel
 (max_i |gpu_i - ref_i| / max_i |ref_i|; bf16 storage, fp32 accumulation on the GPU).  Token ids are bit-exact
 except where the oracle's top-2 fp32 logit margin is below 1e-2 when the LM head + argmax stage is given the
 oracle's hidden states (assert_tokens).  Through the whole chain the bf16 storage points make the two sides'
-hidden states differ by about one bf16 ulp in most elements after five layers (the same happens between the
-fp64 oracle and an fp32-accumulating copy of it), so there a differing id is accepted only where the logit
-errors of the two competing ids explain it (assert_tokens_chain), and the GPU id must be the argmax of the
-GPU's own logits.  Acceptance lengths and committed tokens are bit-exact given the ids.
+hidden states differ by about one bf16 ulp in most elements after five layers; a correct fp32-accumulating
+restatement of the drafter (tests/fp32_restatement.py, pinned in tests/test_fp32_evidence.py) already flips ids
+at oracle margins above 1e-2 (up to 0.015) with per-logit errors up to about 5e-2.  So through the chain an id
+may differ only where the oracle margin is below MARGIN_CHAIN = 5e-2 (a fixed number: that restatement's
+largest logit error), at no more than 5 % of the positions of a request (at least one), and every GPU id must be
+the argmax of the GPU's own logits (assert_tokens_chain).  Acceptance lengths and committed tokens are bit-exact
+given the ids.
 """
 import numpy as np
 import torch
@@ -16,6 +19,8 @@ import synth
 
 REL_TOL = 2e-2
 MARGIN_EXEMPT = 1e-2
+MARGIN_CHAIN = 5e-2
+CHAIN_FLIP_FRAC = 0.05
 
 
 def bits_of(t: torch.Tensor) -> np.ndarray:
@@ -81,8 +86,8 @@ def assert_logits(gpu: np.ndarray, ref: np.ndarray, what: str = "logits", few: i
 
 def assert_tokens_chain(gpu_tok, ref_tok, margin, gpu_logits, ref_logits, what="tokens"):
     """End-to-end id check: every GPU id is the lowest-id argmax of the GPU's own legal logits; an id that
-    differs from the oracle's is accepted only at margin < 1e-2 or where the oracle margin is below twice
-    the larger logit error of the two ids involved."""
+    differs from the oracle's is accepted only where the oracle margin is below MARGIN_CHAIN, and at most
+    max(1, CHAIN_FLIP_FRAC * positions) ids may differ.  Prints and returns (flips, largest exempted margin)."""
     gpu_tok = np.asarray(gpu_tok).reshape(-1)
     ref_tok = np.asarray(ref_tok).reshape(-1)
     margin = np.asarray(margin).reshape(-1)
@@ -91,14 +96,14 @@ def assert_tokens_chain(gpu_tok, ref_tok, margin, gpu_logits, ref_logits, what="
         ids = np.nonzero(legal[r])[0]
         gl = gpu_logits[r, ids].astype(np.float32)
         assert gpu_tok[r] == ids[int(np.argmax(gl))], f"{what}: row {r} id is not the argmax of the GPU logits"
-    bad = []
-    for r in np.nonzero(gpu_tok != ref_tok)[0]:
-        a, b = gpu_tok[r], ref_tok[r]
-        err = max(abs(float(gpu_logits[r, a]) - ref_logits[r, a]), abs(float(gpu_logits[r, b]) - ref_logits[r, b]))
-        if not (margin[r] < MARGIN_EXEMPT or margin[r] < 2 * err):
-            bad.append((int(r), float(margin[r]), err))
-    assert not bad, f"{what}: ids differ beyond the logit error: {bad[:5]}"
-    return int((gpu_tok != ref_tok).sum())
+    flips = np.nonzero(gpu_tok != ref_tok)[0]
+    worst = float(margin[flips].max()) if len(flips) else 0.0
+    print(f"{what}: {len(flips)} of {len(gpu_tok)} ids differ from the oracle, largest exempted margin {worst:.4f}")
+    bad = [(int(r), float(margin[r])) for r in flips if not margin[r] < MARGIN_CHAIN]
+    assert not bad, f"{what}: ids differ at oracle margins >= {MARGIN_CHAIN}: {bad[:5]}"
+    cap = max(1, int(CHAIN_FLIP_FRAC * len(gpu_tok)))
+    assert len(flips) <= cap, f"{what}: {len(flips)} ids differ, more than {cap}"
+    return len(flips), worst
 
 
 def assert_margin(gpu_margin, gpu_logits, ref_margin, ref_logits, what="margin", few: int = 64):
