@@ -19,6 +19,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -282,8 +283,8 @@ def main():
             dist.barrier()
 
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clock_path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
-                              f"bench_clocks_r{rank}.csv")
+    clock_fd, clock_path = tempfile.mkstemp(prefix=f"fpd_bench_clocks_r{rank}_", suffix=".csv")
+    os.close(clock_fd)
     with ClockSampler(clock_path) as cs:
         barrier()
         torch.cuda.synchronize()
@@ -358,6 +359,10 @@ def main():
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": int(launches), "clocks": cs.summary(local_rank)}
         print(json.dumps(line), flush=True)
+    try:
+        os.remove(clock_path)
+    except OSError:
+        pass
     dr.close()
     if world > 1:
         import torch.distributed as dist

@@ -1,7 +1,5 @@
 #pragma once
 
-#include <cuda_fp16.h>
-
 #include "fpd_kernels.cuh"
 
 // attn_body.cuh — the attention work units (one query tile over one KV split; the merge of the splits of one
@@ -17,8 +15,8 @@
 // whole group.  Four warps each own 16 query rows; Q stays in registers as mma fragments; K/V tiles of 64
 // keys are staged in shared memory with cp.async (double buffered, 16-byte chunks XOR-swizzled so ldmatrix
 // is conflict free); S = Q K^T and O += P V run on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
-// accumulate; P is rounded to bf16 as the second product's operand); the online softmax works in base 2 on
-// the fp32 accumulators.  With one split the CTA writes the normalised bf16 output; with several it writes
+// accumulate; P enters the second product as two bf16 terms hi + lo, see split_bf16x2); the online softmax
+// works in base 2 on the fp32 accumulators.  With one split the CTA writes the normalised bf16 output; with several it writes
 // an unnormalised partial (o, m, l) and a merge kernel combines the splits in fixed order (deterministic,
 // no atomics).
 
@@ -57,35 +55,6 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// O += P V runs on fp16 operands: P (in [0, 1] after the running-max shift) keeps an 11-bit significand instead
-// of bf16's 8, and the bf16 values of V convert to fp16 exactly while |v| lies in fp16's normal range.
-__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-// bf16 -> fp16 of one V tile in shared memory, in place (each thread its 16-byte chunks; layout-agnostic).
-__device__ __forceinline__ void v_tile_to_f16(void* tile, int bytes, int tid) {
-  uint4* t = reinterpret_cast<uint4*>(tile);
-  for (int c = tid; c < bytes / 16; c += 128) {
-    uint4 u = t[c];
-    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-      w[i] = pack_f16(f.x, f.y);
-    }
-    t[c] = u;
-  }
-}
-
 // Tile of rows x H bf16 in shared memory; 16-byte chunk c of row r lives at chunk c ^ (r & 7).
 template <int H>
 __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
@@ -185,7 +154,6 @@ __device__ __forceinline__ void attn_tile(const AttnArgs& a, bf16* __restrict__ 
       cp_async_wait<0>();
     }
     sync();
-    v_tile_to_f16(sm.v[buf], KT * H * 2, tid);   // consumed after the next barrier
     const uint32_t ks = smem_addr(sm.k[buf]), vs = smem_addr(sm.v[buf]);
     // ---- S = Q K^T: 16 rows x 64 keys per warp ----
     float s[KT / 8][4];
@@ -245,14 +213,14 @@ __device__ __forceinline__ void attn_tile(const AttnArgs& a, bf16* __restrict__ 
       o[n][2] *= c1;
       o[n][3] *= c1;
     }
-    // ---- O += P V (fp16 operands) ----
-    sync();   // the V tile is fp16 now
+    // ---- O += (P_hi + P_lo) V ----
 #pragma unroll
     for (int kk = 0; kk < KT / 16; kk++) {
-      const uint32_t a0 = pack_f16(s[2 * kk][0], s[2 * kk][1]);
-      const uint32_t a1 = pack_f16(s[2 * kk][2], s[2 * kk][3]);
-      const uint32_t a2 = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      const uint32_t a3 = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      uint32_t h0, h1, h2, h3, l0_, l1_, l2_, l3_;
+      split_bf16x2(s[2 * kk][0], s[2 * kk][1], h0, l0_);
+      split_bf16x2(s[2 * kk][2], s[2 * kk][3], h1, l1_);
+      split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], h2, l2_);
+      split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], h3, l3_);
 #pragma unroll
       for (int np = 0; np < NOT / 2; np++) {
         // transposed 8x8 matrices: (keys +0..7, dims lo), (keys +8..15, dims lo), (keys +0..7, dims hi), (keys +8..15, dims hi)
@@ -260,8 +228,10 @@ __device__ __forceinline__ void attn_tile(const AttnArgs& a, bf16* __restrict__ 
         const int c = np * 2 + (lane >> 4);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(swz<H>(vs, key, c), b0, b1, b2, b3);
-        mma_f16(o[2 * np], a0, a1, a2, a3, b0, b1);
-        mma_f16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        mma_bf16(o[2 * np], h0, h1, h2, h3, b0, b1);
+        mma_bf16(o[2 * np + 1], h0, h1, h2, h3, b2, b3);
+        mma_bf16(o[2 * np], l0_, l1_, l2_, l3_, b0, b1);
+        mma_bf16(o[2 * np + 1], l0_, l1_, l2_, l3_, b2, b3);
       }
     }
     sync();   // this buffer is refilled by the next iteration's prefetch

@@ -82,7 +82,7 @@ struct DraftWs {
   int att_splits, att_chunk;
   TcPlan p_qkv, p_o, p_sw, p_down;
   // many-token path: token-tile GEMMs with fused epilogues; sums of squares [column tiles][M]
-  bool tok;
+  bool tok, att_tc;
   float* ss_tok;
   // few-token path (k_stream.cu)
   bool stream;
@@ -144,7 +144,11 @@ DraftWs carve_draft_tok(const Model& m, Carver& c, int B, int L, int t_cap) {
   w.o = c.take<bf16>((size_t)M * nqh);
   w.hmid = c.take<bf16>((size_t)M * d.d_ff);
   w.ss_tok = c.take<float>((size_t)ceil_div(d.d_model, 128) * M);
-  attn_plan(B, L, d.n_q_heads, d.n_kv_heads, t_cap, m.num_sms, &w.att_splits, &w.att_chunk);
+  w.att_tc = attn_tc_supported(d.head_dim, L, d.n_q_heads, d.n_kv_heads);
+  if (w.att_tc)
+    attn_tc_plan(B, L, d.n_q_heads, d.n_kv_heads, t_cap, m.num_sms, &w.att_splits, &w.att_chunk);
+  else
+    attn_plan(B, L, d.n_q_heads, d.n_kv_heads, t_cap, m.num_sms, &w.att_splits, &w.att_chunk);
   w.o_part = c.take<float>((size_t)w.att_splits * M * nqh);
   w.ml = c.take<float2>((size_t)w.att_splits * M * d.n_q_heads);
   return w;
@@ -345,6 +349,7 @@ fpd_status fpd_model_create(const fpd_model_desc* desc, const fpd_weights* w, fp
       init_err = tc_init_attributes();
       if (init_err == cudaSuccess) init_err = attn_init_attributes();
       if (init_err == cudaSuccess) init_err = stream_init_attributes();
+      if (init_err == cudaSuccess) init_err = attn_tc_init_attributes();
     });
     if (init_err != cudaSuccess) return cuda_fail(init_err, "kernel attributes");
   }
@@ -621,7 +626,7 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
       g.eps = d.rms_eps;
       FPD_CUDA(launch_tc_tok(g, w.p_qkv, st), "QKV GEMM + q/k norm + RoPE");
       a.layer = l;
-      FPD_CUDA(launch_attention(a, w.o, st), "attention");
+      FPD_CUDA(w.att_tc ? launch_attention_tc(a, w.o, st) : launch_attention(a, w.o, st), "attention");
       TokGemm r{};
       r.qkv = false;
       r.x = w.o;

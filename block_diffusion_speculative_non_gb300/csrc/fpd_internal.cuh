@@ -70,6 +70,16 @@ struct Model {
 __host__ __device__ constexpr inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr inline size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 
+// Softmax weights as the operand of O += P V: (a, b) -> two packed bf16 pairs (a in the low half) with
+// a = hi_a + lo_a and b = hi_b + lo_b to about 2^-17 relative (hi = bf16(x), lo = bf16(x - hi), round to nearest
+// even).  Both pairs multiply the bf16 V tile with fp32 accumulation, so the product sees P nearly as exactly as
+// fp32 arithmetic would while both operands stay bf16.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(b), "f"(a));
+  const float ha = __uint_as_float(hi << 16), hb = __uint_as_float(hi & 0xFFFF0000u);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(b - hb), "f"(a - ha));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

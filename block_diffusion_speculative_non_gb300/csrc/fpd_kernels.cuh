@@ -20,7 +20,6 @@ struct GemmArgs {
   int M, N, K;
   int k_split;          // K elements per split (multiple of 64)
 };
-cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t st);
 
 // tcgen05 GEMM: the plan fixes operand placement, tile width, split-K and grid for a shape.
 struct TcPlan {
@@ -60,7 +59,6 @@ cudaError_t launch_tc_tok(const TokGemm& g, const TcPlan& pl, cudaStream_t st);
 cudaError_t launch_norm_rows(bf16* xn, const bf16* x, const float* ss_part, int n_part, const bf16* g, int M, int d,
                              float eps, cudaStream_t st);
 cudaError_t tc_init_attributes();     // once per process, before any stream capture
-void tc_set_swap_variant(int v);      // tuning sweeps only (fpd_test_set_variant)
 cudaError_t attn_init_attributes();
 cudaError_t launch_sum_splits(float* out, const float* part, int splits, size_t n, cudaStream_t st);
 
@@ -133,7 +131,13 @@ struct AttnArgs {
   int splits, chunk;    // KV splits and keys per split
 };
 void attn_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* splits, int* chunk);
-cudaError_t launch_attention(const AttnArgs& a, bf16* out, cudaStream_t st);
+cudaError_t launch_attention(const AttnArgs& a, bf16* out, cudaStream_t st);          // mma.sync tiles of 64 rows
+cudaError_t launch_attn_merge(const AttnArgs& a, bf16* out, cudaStream_t st);         // split merge, fixed order
+// tcgen05 attention (k_attention_tc.cu): 128-row query tiles, head_dim 128; same partial layout and merge
+bool attn_tc_supported(int head_dim, int L, int nq, int nkv);
+void attn_tc_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* splits, int* chunk);
+cudaError_t attn_tc_init_attributes();
+cudaError_t launch_attention_tc(const AttnArgs& a, bf16* out, cudaStream_t st);
 
 // ---- LM head + constrained argmax ------------------------------------------------------------------------------
 struct LmPlan {

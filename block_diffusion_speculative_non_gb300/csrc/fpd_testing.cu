@@ -11,6 +11,23 @@ int current_sms() {
     return 0;
   return n;
 }
+
+bool attributes_ready() {
+  static cudaError_t e = [] {
+    cudaError_t r = tc_init_attributes();
+    if (r == cudaSuccess) r = attn_init_attributes();
+    if (r == cudaSuccess) r = attn_tc_init_attributes();
+    return r;
+  }();
+  return e == cudaSuccess;
+}
+
+void attn_test_plan(int impl, int batch, int L, int nq, int nkv, int t_cap, int sms, int* splits, int* chunk) {
+  if (impl == 1)
+    attn_tc_plan(batch, L, nq, nkv, t_cap, sms, splits, chunk);
+  else
+    attn_plan(batch, L, nq, nkv, t_cap, sms, splits, chunk);
+}
 }  // namespace
 
 extern "C" {
@@ -27,12 +44,13 @@ size_t fpd_test_gemm_workspace_bytes(int M, int N, int K) {
   return best * sizeof(float);
 }
 
-fpd_status fpd_test_gemm(int impl, int placement, int M, int N, int K, const void* A, const void* B, float* C,
-                         void* workspace, size_t workspace_bytes, void* stream) {
-  if (M < 1 || N < 1 || K < 64 || K % 64 || impl < 0 || impl > 1 || placement < -1 || placement > 1)
-    return FPD_ERR_SHAPE;
+fpd_status fpd_test_gemm(int placement, int M, int N, int K, const void* A, const void* B, float* C, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (M < 1 || N < 1 || K < 64 || K % 64 || placement < -1 || placement > 1) return FPD_ERR_SHAPE;
   if (!A || !B || !C || !workspace) return FPD_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
+  const int sms = current_sms();
+  if (!sms || !attributes_ready()) return FPD_ERR_CUDA;
   GemmArgs g{};
   g.a[0] = (const bf16*)A;
   g.seg_k = K;
@@ -43,15 +61,6 @@ fpd_status fpd_test_gemm(int impl, int placement, int M, int N, int K, const voi
   g.M = M;
   g.N = N;
   g.K = K;
-  if (impl == 1) {
-    g.c = C;
-    g.k_split = K;
-    return launch_gemm_simt(g, st) == cudaSuccess ? FPD_OK : FPD_ERR_CUDA;
-  }
-  const int sms = current_sms();
-  if (!sms) return FPD_ERR_CUDA;
-  static cudaError_t init_err = tc_init_attributes();
-  if (init_err != cudaSuccess) return FPD_ERR_CUDA;
   const TcPlan pl = tc_plan_force(M, N, K, sms, placement);
   if ((size_t)pl.splits * M * N * sizeof(float) > workspace_bytes) return FPD_ERR_CAPACITY;
   g.c = (float*)workspace;
@@ -65,15 +74,54 @@ fpd_status fpd_test_swiglu(int M, int F, int K, const void* X, const void* W, vo
   if (M < 1 || F < 1 || K < 64 || K % 64) return FPD_ERR_SHAPE;
   if (!X || !W || !hmid) return FPD_ERR_INVALID_ARG;
   const int sms = current_sms();
-  if (!sms) return FPD_ERR_CUDA;
-  static cudaError_t init_err = tc_init_attributes();
-  if (init_err != cudaSuccess) return FPD_ERR_CUDA;
+  if (!sms || !attributes_ready()) return FPD_ERR_CUDA;
   const TcPlan pl = tc_plan_swiglu(M, F, K, sms);
   return launch_tc_swiglu((const bf16*)X, M, K, (const bf16*)W, F, (bf16*)hmid, pl, (cudaStream_t)stream) == cudaSuccess
              ? FPD_OK
              : FPD_ERR_CUDA;
 }
 
-void fpd_test_set_variant(int variant) { tc_set_swap_variant(variant); }
+size_t fpd_test_attention_workspace_bytes(int impl, int batch, int L, int nq, int nkv, int head_dim, int t_cap) {
+  const int sms = current_sms();
+  if (!sms || batch < 1 || L < 1 || nkv < 1 || nq % nkv) return 0;
+  int splits = 1, chunk = 0;
+  attn_test_plan(impl, batch, L, nq, nkv, t_cap, sms, &splits, &chunk);
+  const size_t rows = (size_t)batch * L;
+  return align_up((size_t)splits * rows * nq * head_dim * sizeof(float), 256) + (size_t)splits * rows * nq * sizeof(float2);
+}
+
+fpd_status fpd_test_attention(int impl, int batch, int L, int nq, int nkv, int head_dim, int t_cap, int layer,
+                              const int32_t* ctx_len, const void* q, const void* kblk, const void* vblk,
+                              const void* store, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (impl < 0 || impl > 1 || batch < 1 || L < 1 || nkv < 1 || nq % nkv || t_cap < 1 || layer < 0) return FPD_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return FPD_ERR_UNSUPPORTED;
+  if (impl == 1 && !attn_tc_supported(head_dim, L, nq, nkv)) return FPD_ERR_UNSUPPORTED;
+  if (!ctx_len || !q || !kblk || !vblk || !store || !out || !workspace) return FPD_ERR_INVALID_ARG;
+  const int sms = current_sms();
+  if (!sms || !attributes_ready()) return FPD_ERR_CUDA;
+  if (workspace_bytes < fpd_test_attention_workspace_bytes(impl, batch, L, nq, nkv, head_dim, t_cap))
+    return FPD_ERR_CAPACITY;
+  AttnArgs a{};
+  a.q = (const bf16*)q;
+  a.store = (const bf16*)store;
+  a.kblk = (const bf16*)kblk;
+  a.vblk = (const bf16*)vblk;
+  a.ctx_len = ctx_len;
+  a.batch = batch;
+  a.L = L;
+  a.nq = nq;
+  a.nkv = nkv;
+  a.head_dim = head_dim;
+  a.t_cap = t_cap;
+  a.layer = layer;
+  a.rows = batch * L;
+  attn_test_plan(impl, batch, L, nq, nkv, t_cap, sms, &a.splits, &a.chunk);
+  const size_t rows = (size_t)batch * L;
+  a.o_part = (float*)workspace;
+  a.ml = (float2*)((char*)workspace + align_up((size_t)a.splits * rows * nq * head_dim * sizeof(float), 256));
+  cudaStream_t st = (cudaStream_t)stream;
+  const cudaError_t e = impl == 1 ? launch_attention_tc(a, (bf16*)out, st) : launch_attention(a, (bf16*)out, st);
+  return e == cudaSuccess ? FPD_OK : FPD_ERR_CUDA;
+}
 
 }  // extern "C"

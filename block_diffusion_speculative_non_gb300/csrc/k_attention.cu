@@ -53,20 +53,24 @@ cudaError_t attn_init_attributes() {
   return e;
 }
 
+cudaError_t launch_attn_merge(const AttnArgs& a, bf16* out, cudaStream_t st) {
+  if (a.head_dim == 128)
+    return launch_k(attn_merge_kernel<128>, dim3(a.rows, a.nq), 128, 0, st, out, (const float*)a.o_part,
+                    (const float2*)a.ml, a.splits, a.rows, a.nq);
+  return launch_k(attn_merge_kernel<64>, dim3(a.rows, a.nq), 64, 0, st, out, (const float*)a.o_part,
+                  (const float2*)a.ml, a.splits, a.rows, a.nq);
+}
+
 cudaError_t launch_attention(const AttnArgs& a, bf16* out, cudaStream_t st) {
   const int grp = a.nq / a.nkv;
   dim3 grid(ceil_div(a.L * grp, QT), a.batch * a.nkv, a.splits);
   cudaError_t err;
-  if (a.head_dim == 128) {
+  if (a.head_dim == 128)
     err = launch_k(attn_mma_kernel<128>, grid, NWARP * 32, sizeof(Smem<128>), st, a, out);
-    if (err != cudaSuccess || a.splits == 1) return err;
-    return launch_k(attn_merge_kernel<128>, dim3(a.rows, a.nq), 128, 0, st, out, (const float*)a.o_part,
-                    (const float2*)a.ml, a.splits, a.rows, a.nq);
-  }
-  err = launch_k(attn_mma_kernel<64>, grid, NWARP * 32, sizeof(Smem<64>), st, a, out);
+  else
+    err = launch_k(attn_mma_kernel<64>, grid, NWARP * 32, sizeof(Smem<64>), st, a, out);
   if (err != cudaSuccess || a.splits == 1) return err;
-  return launch_k(attn_merge_kernel<64>, dim3(a.rows, a.nq), 64, 0, st, out, (const float*)a.o_part,
-                  (const float2*)a.ml, a.splits, a.rows, a.nq);
+  return launch_attn_merge(a, out, st);
 }
 
 }  // namespace fpd

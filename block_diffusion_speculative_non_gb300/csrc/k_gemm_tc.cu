@@ -571,24 +571,8 @@ cudaError_t launch_kernel(const TcParams& p, int grid, cudaStream_t st) {
                   st, p);
 }
 
-// Pipeline shapes of the few-token (weight-tile) kernels with 16-token tiles: (atoms per stage, stages,
-// CTAs per SM).  Entry 0 is the production choice; the others exist for tuning sweeps (fpd_test_set_variant).
-struct SwapVariant {
-  int ks, stages, ctas_per_sm;
-};
-constexpr SwapVariant kSwapVariants[] = {{1, 6, 2}, {2, 6, 1}, {4, 3, 1}, {2, 3, 2}, {1, 12, 1}};
-int g_swap_variant = 0;
-
-template <int EPI>
-cudaError_t launch_swap16(const TcParams& p, int grid, cudaStream_t st) {
-  switch (g_swap_variant) {
-    case 1: return launch_kernel<16, 6, true, EPI, 2>(p, grid, st);
-    case 2: return launch_kernel<16, 3, true, EPI, 4>(p, grid, st);
-    case 3: return launch_kernel<16, 3, true, EPI, 2>(p, grid, st);
-    case 4: return launch_kernel<16, 12, true, EPI, 1>(p, grid, st);
-    default: return launch_kernel<16, 6, true, EPI, 1>(p, grid, st);
-  }
-}
+// Few-token (weight-tile) kernels with 16-token tiles: one 64-element K atom per stage, 6 stages, 2 CTAs per SM.
+constexpr int kSwap16CtasPerSm = 2;
 }  // namespace
 
 // Row-major bf16 matrix [rows, cols] with row stride ld (elements), boxes of 64 columns x box_rows rows,
@@ -622,20 +606,10 @@ cudaError_t make_tmap_nd(CUtensorMap* tm, const void* ptr, int rank, const uint6
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-void tc_set_swap_variant(int v) { g_swap_variant = (v >= 0 && v < 5) ? v : 0; }
-
 // Opt every instantiation into its shared-memory size once, outside any stream capture (fpd_model_create).
 cudaError_t tc_init_attributes() {
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = set_attr<16, 6, true, EPI_STORE>();
-  if (e == cudaSuccess) e = set_attr<16, 6, true, EPI_STORE, 2>();
-  if (e == cudaSuccess) e = set_attr<16, 3, true, EPI_STORE, 4>();
-  if (e == cudaSuccess) e = set_attr<16, 3, true, EPI_STORE, 2>();
-  if (e == cudaSuccess) e = set_attr<16, 12, true, EPI_STORE, 1>();
-  if (e == cudaSuccess) e = set_attr<16, 6, true, EPI_ARGMAX, 2>();
-  if (e == cudaSuccess) e = set_attr<16, 3, true, EPI_ARGMAX, 4>();
-  if (e == cudaSuccess) e = set_attr<16, 3, true, EPI_ARGMAX, 2>();
-  if (e == cudaSuccess) e = set_attr<16, 12, true, EPI_ARGMAX, 1>();
   if (e == cudaSuccess) e = set_attr<32, 5, true, EPI_STORE>();
   if (e == cudaSuccess) e = set_attr<64, 4, true, EPI_STORE>();
   if (e == cudaSuccess) e = set_attr<128, 6, false, EPI_STORE>();
@@ -718,7 +692,7 @@ TcPlan tc_plan_gemm(int M, int N, int K, int num_sms) {
     pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     pl.pt = ceil_div(N, BM);
     pl.qt = ceil_div(M, pl.bn);
-    ctas_per_sm = pl.bn == 16 ? kSwapVariants[g_swap_variant].ctas_per_sm : 2;
+    ctas_per_sm = pl.bn == 16 ? kSwap16CtasPerSm : 2;
   } else {
     pl.swap = false;
     pl.bn = N >= 1024 ? 256 : 128;
@@ -751,7 +725,7 @@ TcPlan tc_plan_force(int M, int N, int K, int num_sms, int placement) {
     pl.pt = ceil_div(M, BM);
     pl.qt = ceil_div(N, pl.bn);
   }
-  const int slots = num_sms * (pl.swap ? (pl.bn == 16 ? kSwapVariants[g_swap_variant].ctas_per_sm : 2) : 1);
+  const int slots = num_sms * (pl.swap ? 2 : 1);
   const int tiles = pl.pt * pl.qt;
   int splits = 1;
   if (tiles < slots) splits = std::max(1, std::min(slots / tiles, nkb / 4));
@@ -804,7 +778,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& g, const TcPlan& pl, cudaStream_t st)
   p.splits = pl.splits;
   p.k_split = pl.k_split;
   if (pl.swap) {
-    if (pl.bn == 16) return launch_swap16<EPI_STORE>(p, pl.grid, st);
+    if (pl.bn == 16) return launch_kernel<16, 6, true, EPI_STORE>(p, pl.grid, st);
     if (pl.bn == 32) return launch_kernel<32, 5, true, EPI_STORE>(p, pl.grid, st);
     return launch_kernel<64, 4, true, EPI_STORE>(p, pl.grid, st);
   }
@@ -895,9 +869,9 @@ cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows,
   p.logits = logits;
   p.V = V;
   const int n_work = p.implicit_rowtiles > 0 ? p.implicit_total : max_items;
-  const int per_sm = bn == 16 ? kSwapVariants[g_swap_variant].ctas_per_sm : 2;
+  const int per_sm = 2;
   const int grid = std::max(1, std::min(n_work, per_sm * num_sms));
-  if (bn == 16) return launch_swap16<EPI_ARGMAX>(p, grid, st);
+  if (bn == 16) return launch_kernel<16, 6, true, EPI_ARGMAX>(p, grid, st);
   if (bn == 32) return launch_kernel<32, 5, true, EPI_ARGMAX>(p, grid, st);
   return launch_kernel<64, 4, true, EPI_ARGMAX>(p, grid, st);
 }

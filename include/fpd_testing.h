@@ -1,7 +1,7 @@
 /*
  * fpd_testing.h — diagnostic entry points of libfpd used by the test-suite to check single kernels in
- * isolation.  They are not part of the drafter hot path and no paper passage defines them; the hot-path
- * entry points are declared in fpd.h.
+ * isolation against plain PyTorch fp32 references.  They are not part of the drafter hot path and no paper
+ * passage defines them; the hot-path entry points are declared in fpd.h.
  */
 #ifndef FPD_TESTING_H_
 #define FPD_TESTING_H_
@@ -13,24 +13,27 @@ extern "C" {
 #endif
 
 /* C[M, N] (fp32, row-major) = A[M, K] . B[N, K]^T with A, B bf16 row-major device matrices, computed by the
- * library's GEMM kernels.  impl 0: the tcgen05 tensor-core kernel with the production plan for this shape
- * (placement -1), or with the token tile on the 128-row MMA operand (placement 0), or with the weight tile
- * there (placement 1); impl 1: the CUDA-core tile kernel.  K must be a multiple of 64.  workspace holds the
- * split-K partial sums: at least fpd_test_gemm_workspace_bytes(M, N, K) bytes.  Asynchronous on stream. */
-fpd_status fpd_test_gemm(int impl, int placement, int M, int N, int K, const void* A, const void* B, float* C,
-                         void* workspace, size_t workspace_bytes, void* stream);
+ * library's tcgen05 GEMM kernel with the production plan for this shape (placement -1), or with the token tile on
+ * the 128-row MMA operand (placement 0), or with the weight tile there (placement 1).  K must be a multiple of 64.
+ * workspace holds the split-K partial sums: at least fpd_test_gemm_workspace_bytes(M, N, K) bytes.  Asynchronous. */
+fpd_status fpd_test_gemm(int placement, int M, int N, int K, const void* A, const void* B, float* C, void* workspace,
+                         size_t workspace_bytes, void* stream);
 size_t fpd_test_gemm_workspace_bytes(int M, int N, int K);
 
 /* hmid[M, F] (bf16) = silu(X . Wg^T) * (X . Wu^T) for X [M, K] and W = [Wg; Wu] ([2F, K]) bf16 row-major device
- * matrices, with the gate/up tcgen05 kernel and its SwiGLU epilogue (weight-tile placement for M <= 64, token
- * tiles above).  Asynchronous on stream. */
+ * matrices, with the gate/up tcgen05 kernel and its SwiGLU epilogue.  Asynchronous on stream. */
 fpd_status fpd_test_swiglu(int M, int F, int K, const void* X, const void* W, void* hmid, void* stream);
 
-/* Selects the pipeline shape of the 16-token weight-tile GEMM kernels for tuning sweeps: 0 (default) = one
- * 64-element K atom per stage, 6 stages, 2 CTAs per SM; 1 = 2 atoms x 6 stages, 1 CTA/SM; 2 = 4 atoms x 3 stages,
- * 1 CTA/SM; 3 = 2 atoms x 3 stages, 2 CTAs/SM; 4 = 1 atom x 12 stages, 1 CTA/SM.  Affects plans (and so
- * workspace sizes) made afterwards: set it before fpd_workspace_bytes. */
-void fpd_test_set_variant(int variant);
+/* The drafter's block attention of one layer in isolation: out [batch * L, n_q_heads, head_dim] bf16 =
+ * softmax(q . [K_ctx ; K_blk]^T / sqrt(h)) [V_ctx ; V_blk] per request and q head (kv head = q head / group), with
+ * q [batch * L, nq, h], k_blk / v_blk [batch, nkv, L, h], the context of layer `layer` in store
+ * ([n_layers >= layer + 1][batch][K|V][nkv][t_cap][h]) and ctx_len [batch] (all device).  impl 0: the mma.sync
+ * kernel (64-row tiles); impl 1: the tcgen05 kernel (128-row tiles, head_dim 128 and L * group >= 128 only).
+ * workspace: fpd_test_attention_workspace_bytes bytes.  Asynchronous on stream. */
+fpd_status fpd_test_attention(int impl, int batch, int L, int nq, int nkv, int head_dim, int t_cap, int layer,
+                              const int32_t* ctx_len, const void* q, const void* kblk, const void* vblk,
+                              const void* store, void* out, void* workspace, size_t workspace_bytes, void* stream);
+size_t fpd_test_attention_workspace_bytes(int impl, int batch, int L, int nq, int nkv, int head_dim, int t_cap);
 
 #ifdef __cplusplus
 }
