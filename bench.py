@@ -6,10 +6,15 @@ row whose agreement prefix is Geometric(0.25).  The context K/V is prepared once
 reported separately).  All inputs are seeded synthetic data; the drafter weights (1.83 GB streamed per
 block) are far larger than the 129 MB L2, so every step reads them from HBM.
 
+The line's `roofline` is the whole step's: algorithmic bytes (HBM-bound workloads) or flops (tensor-bound ones)
+per step over the measured step time.  The default run also times the batched fixed-width workload (32 requests,
+L = 381) and reports its tensor-core fraction under `batched`.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+  python bench.py --sweep          # the 32-point throughput sweep, one JSON line per point
 
 N > 1 runs N independent replicas (one per rank, launched by torchrun): the path has no exchange step.
-Prints ONE JSON line (rank 0).
+Prints ONE JSON line (rank 0), or one per point with --sweep.
 """
 from __future__ import annotations
 
@@ -31,22 +36,69 @@ METRIC = "draft tokens/s per GB300 (fwd+constrain+verify)"
 
 
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, kind)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+        burst = float(p["bf16_tflops"])
+        return float(p["hbm_gbs"]), burst, float(p.get("bf16_tflops_sustained", burst)), "measured"
     except Exception:
-        return 6800.0, 1900.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def algorithmic_bytes(shape, batch, L, ctx_len):
-    """Bytes one block must move at minimum: drafter layer weights, LM-head rows, context K/V reads."""
-    s = shape
-    layer = (s.qkv_rows * s.d_model + s.d_model * s.n_q_heads * s.head_dim + 2 * s.d_ff * s.d_model
-             + s.d_model * s.d_ff) * 2
-    lm = s.vocab * s.d_model * 2
-    kv = int(np.sum(ctx_len)) * s.n_layers * 2 * s.n_kv_heads * s.head_dim * 2
-    return s.n_layers * layer, lm, kv
+def legal_counts(wl):
+    """Legal ids of each drafted position 1..L-1 and the set of LM-head rows any position needs."""
+    s, L = wl.shape, wl.block_len
+    if wl.layout is None:
+        return np.full(L - 1, s.vocab, dtype=np.int64), s.vocab
+    lay = wl.layout
+    off, rng = lay["class_off"], lay["class_ranges"]
+    per_class, rows = [], set()
+    full = False
+    for c in range(len(off) - 1):
+        n = 0
+        for k in range(off[c], off[c + 1]):
+            lo, hi = int(rng[2 * k]), int(rng[2 * k + 1])
+            n += hi - lo
+        per_class.append(n)
+    used = set(int(c) for c in lay["pos_class"][1:L])
+    for c in used:
+        if per_class[c] >= s.vocab:
+            full = True
+        for k in range(off[c], off[c + 1]):
+            rows.update(range(int(rng[2 * k]), int(rng[2 * k + 1])))
+    counts = np.array([per_class[int(c)] for c in lay["pos_class"][1:L]], dtype=np.int64)
+    return counts, (s.vocab if full else len(rows))
+
+
+def algorithmic_work(wl):
+    """Minimum bytes and flops of one step (every request's block): drafter layer weights, the LM-head rows some
+    position can select, the context K/V reads; 2 flops per multiply-add of the projections, the LM-head columns
+    of the legal ids and the attention (4 (T_b + L) L h per q head and layer)."""
+    s, B, L = wl.shape, wl.batch, wl.block_len
+    layer_params = (s.qkv_rows * s.d_model + s.d_model * s.n_q_heads * s.head_dim + 2 * s.d_ff * s.d_model
+                    + s.d_model * s.d_ff)
+    counts, lm_rows = legal_counts(wl)
+    ctx = wl.ctx_len.astype(np.int64)
+    bytes_ = {"layers": s.n_layers * layer_params * 2, "lm_head": lm_rows * s.d_model * 2,
+              "kv": int(ctx.sum()) * s.n_layers * 2 * s.n_kv_heads * s.head_dim * 2}
+    flops = {"layers": 2 * B * L * layer_params * s.n_layers, "lm_head": 2 * B * int(counts.sum()) * s.d_model,
+             "attention": 4 * int((ctx + L).sum()) * L * s.head_dim * s.n_q_heads * s.n_layers}
+    return bytes_, flops
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per step (dram__bytes_read.sum + dram__bytes_write.sum over every kernel of one step) from the
+    committed ncu summary, or None when no summary covers this workload."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_per_step.md")
+    try:
+        for ln in open(path):
+            cells = [c.strip() for c in ln.strip().strip("|").split("|")]
+            if len(cells) >= 3 and cells[0] == workload:
+                return int(float(cells[2]))
+    except (OSError, ValueError):
+        pass
+    return None
 
 
 class ClockSampler:
@@ -130,6 +182,214 @@ def oracle_sample(wl, w, kv_np, target):
     return om, one, kv1, (target[:1] if target is not None else None), lay
 
 
+class StepRunner:
+    """One workload on one drafter: device inputs, the step as three CUDA graphs (draft | LM head + argmax |
+    verify), and CUDA-event timing of each part on the launching stream."""
+
+    def __init__(self, pkg, dr, wl, dev, prepare=True, kv_seed=None):
+        import torch
+        import synth
+        self.pkg, self.dr, self.wl, self.dev = pkg, dr, wl, dev
+        s, B, L = wl.shape, wl.batch, wl.block_len
+        self.stream = torch.cuda.current_stream(dev)
+        self.prepare_ms = None
+        if prepare:
+            feats = synth.make_features(s, int(wl.row_off[-1]), wl.seed + 1)
+            fd, row_off_d, _ = dr.prepare_context(B, wl.row_off, feats)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            pkg.fpd_prepare_context(dr.handle, B, int(wl.row_off[-1]), row_off_d, None, fd, dr.kv_store, dr.t_cap,
+                                    dr.workspace, dr.ws_bytes, self.stream)
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            self.prepare_ms = e0.elapsed_time(e1)
+            del fd, feats
+        else:
+            # a prepared context stands in as seeded N(0, 1) bf16 K/V drawn on the device
+            g = torch.Generator(device=dev).manual_seed(int(kv_seed if kv_seed is not None else wl.seed + 5))
+            kv = dr.kv_view(B)
+            for l in range(s.n_layers):
+                kv[l].normal_(generator=g)
+        self.ctx_len = torch.from_numpy(wl.ctx_len).to(dev)
+        self.anchor = torch.from_numpy(wl.anchor).to(dev)
+        self.hidden = torch.empty(B * L, s.d_model, dtype=torch.bfloat16, device=dev)
+        self.tokens = torch.empty(B, L - 1, dtype=torch.int32, device=dev)
+        self.accept = torch.empty(B, dtype=torch.int32, device=dev)
+        self.committed = torch.empty(B, L, dtype=torch.int32, device=dev)
+        self.valid = torch.empty(B, dtype=torch.int32, device=dev)
+        self.lay_d = self.rule_d = None
+        if wl.layout is not None:
+            self.lay_d, self.rule_d = pkg.Drafter.layout(wl.layout, B, L, dev)
+        # target rows: Geometric(p) agreement with the drafter's own ids (text mode)
+        self.do_draft(self.stream)
+        self.do_argmax(self.stream)
+        torch.cuda.synchronize()
+        self.target_np = self.target = None
+        if wl.layout is None:
+            self.target_np, _ = synth.make_target_rows(self.tokens.cpu().numpy(), s.vocab, wl.geo_p or 0.25,
+                                                       wl.seed + 2)
+            self.target = torch.from_numpy(self.target_np).to(dev)
+
+    def do_draft(self, st):
+        wl, dr = self.wl, self.dr
+        self.pkg.fpd_draft_block(dr.handle, wl.batch, wl.block_len, dr.kv_store, dr.t_cap, self.ctx_len, self.anchor,
+                                 wl.mask_id, self.hidden, None, dr.workspace, dr.ws_bytes, st)
+
+    def do_argmax(self, st):
+        wl, dr = self.wl, self.dr
+        self.pkg.fpd_constrain_argmax(dr.handle, wl.batch, wl.block_len, self.hidden, self.lay_d, self.tokens, None,
+                                      dr.workspace, dr.ws_bytes, st)
+
+    def do_verify(self, st):
+        wl = self.wl
+        if wl.layout is None:
+            self.pkg.fpd_verify(0, wl.batch, wl.block_len, self.tokens, self.target, None, None, -1, self.accept,
+                                self.committed, self.valid, st)
+        else:
+            self.pkg.fpd_verify(1, wl.batch, wl.block_len, self.tokens, None, self.lay_d, self.rule_d,
+                                wl.layout["pad_id"], self.accept, self.committed, self.valid, st)
+
+    def capture(self, warmup):
+        import torch
+        for _ in range(max(3, warmup)):   # eager warm-up (also counts the kernels one step launches)
+            n0 = self.pkg.fpd_kernel_launches()
+            self.do_draft(self.stream)
+            self.do_argmax(self.stream)
+            self.do_verify(self.stream)
+            self.launches_per_step = self.pkg.fpd_kernel_launches() - n0
+        torch.cuda.synchronize()
+        cap = torch.cuda.Stream(self.dev)
+        self.graphs = []
+        for fn in (self.do_draft, self.do_argmax, self.do_verify):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                fn(torch.cuda.current_stream(self.dev))
+            self.graphs.append(g)
+        for _ in range(max(3, warmup)):
+            self.step()
+        torch.cuda.synchronize()
+
+    def step(self, ev=None):
+        g_draft, g_argmax, g_verify = self.graphs
+        if ev is not None:
+            ev[0].record(self.stream)
+        g_draft.replay()
+        if ev is not None:
+            ev[1].record(self.stream)
+        g_argmax.replay()
+        if ev is not None:
+            ev[2].record(self.stream)
+        g_verify.replay()
+
+    def time_steps(self, steps, barrier=lambda: None):
+        """Device time of `steps` back-to-back steps, plus the mean draft and LM-head call times."""
+        import torch
+        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+        t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        t0e.record(self.stream)
+        for i in range(steps):
+            self.step(ev[i])
+        t1e.record(self.stream)
+        torch.cuda.synchronize()
+        barrier()
+        draft_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
+        lm_ms = float(np.mean([b.elapsed_time(c) for _, b, c in ev]))
+        return t0e.elapsed_time(t1e), draft_ms, lm_ms
+
+
+def roofline_of(wl, ms_per_step, draft_ms, lm_ms, traffic=None):
+    """The step's roofline: HBM-bound when the bytes take longer than the flops at the measured peaks."""
+    hbm, tc_burst, tc_sus, kind = peaks()
+    by, fl = algorithmic_work(wl)
+    B_tot, F_tot = sum(by.values()), sum(fl.values())
+    sec = ms_per_step * 1e-3
+    lm_bytes = by["lm_head"] + wl.batch * (wl.block_len - 1) * wl.shape.d_model * 2
+    calls = {
+        "fpd_draft_block": {"ms": draft_ms, "achieved_gbs": (by["layers"] + by["kv"]) / (draft_ms * 1e-3) / 1e9,
+                            "achieved_tflops": (fl["layers"] + fl["attention"]) / (draft_ms * 1e-3) / 1e12},
+        "fpd_constrain_argmax": {"ms": lm_ms, "achieved_gbs": lm_bytes / (lm_ms * 1e-3) / 1e9,
+                                 "achieved_tflops": fl["lm_head"] / (lm_ms * 1e-3) / 1e12},
+    }
+    if B_tot / (hbm * 1e9) >= F_tot / (tc_burst * 1e12):
+        for c in calls.values():
+            c["frac"] = c["achieved_gbs"] / hbm
+        ach = B_tot / sec / 1e9
+        return {"bound": "hbm", "kernel": "whole step (draft block + constrained argmax + verify)",
+                "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_kind": f"{kind} copy bandwidth", "traffic": traffic, "algorithmic_bytes": B_tot,
+                "bytes_parts": by, "calls": calls}
+    for c in calls.values():
+        c["frac"] = c["achieved_tflops"] / tc_sus
+    ach = F_tot / sec / 1e12
+    return {"bound": "tensor", "kernel": "whole step (draft block + constrained argmax + verify)",
+            "achieved": ach, "peak": tc_sus, "unit": "TFLOP/s", "frac": ach / tc_sus,
+            "frac_of_burst": ach / tc_burst, "peak_kind": f"{kind} bf16 cuBLAS, sustained (steps run back to back)",
+            "traffic": traffic, "algorithmic_flops": F_tot, "flops_parts": fl, "calls": calls}
+
+
+def workload_config(name, wl):
+    import synth
+    s = wl.shape
+    return {"workload": name, "batch": wl.batch, "block_len": wl.block_len,
+            "context": wl.ctx_len.tolist() if wl.batch <= 4 else [int(wl.ctx_len.min()), int(wl.ctx_len.max())],
+            "d_model": s.d_model, "layers": s.n_layers, "vocab": s.vocab,
+            "layout": "unconstrained" if wl.layout is None else synth.CONFIGS[wl.name]["layout"],
+            "l2": "inputs larger than L2 (1.83 GB weights streamed per step)"}
+
+
+def run_batched_extra(pkg, w, dev, steps=10, warmup=3):
+    """The batched fixed-width workload (32 requests, L = 381) timed after the main line: its tensor fraction."""
+    import synth
+    wl = synth.make_workload("primitive_fixedwidth_b32")
+    dr = pkg.Drafter(wl.shape, w, wl.batch, wl.block_len, wl.t_cap, device=dev)
+    r = StepRunner(pkg, dr, wl, dev)
+    r.capture(warmup)
+    ms, dms, lms = r.time_steps(steps)
+    rf = roofline_of(wl, ms / steps, dms, lms)
+    out = {"workload": "primitive_fixedwidth_b32", "ms_per_step": ms / steps,
+           "value": wl.batch * (wl.block_len - 1) * steps / (ms * 1e-3), "unit": "draft tokens/s",
+           "prepare_ms": r.prepare_ms, "bound": rf["bound"], "achieved": rf["achieved"], "unit_roofline": rf["unit"],
+           "frac": rf["frac"], "frac_of_burst": rf.get("frac_of_burst"), "peak": rf["peak"],
+           "weights": "the main workload's synthetic draw (values do not change the work)"}
+    del r
+    dr.close()
+    return out
+
+
+def run_sweep(pkg, steps, warmup):
+    """The 32-point sweep: batch {1,4,16,64} x context {512,2048,8192,16384} x block {16 text, 385 special}.
+    Each point's context K/V is drawn on the device (seed 5000 + point index); the LM head, attention and
+    verification run exactly as in the named workloads."""
+    import torch
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = synth.CONFIGS["text_4b_b1"]["shape"]
+    w = synth.make_weights(s, 5000)
+    points = [(B, T, L) for L in (16, 385) for B in (1, 4, 16, 64) for T in (512, 2048, 8192, 16384)]
+    dr = pkg.Drafter(s, w, 64, 385, 16384, device=dev)
+    for idx, (B, T, L) in enumerate(points):
+        base = "text_4b_b1" if L == 16 else "primitive_special_b1"
+        wl = synth.make_workload(base, batch=B, t_ctx=T, seed=5000 + idx)
+        r = StepRunner(pkg, dr, wl, dev, prepare=False, kv_seed=5000 + idx)
+        r.capture(warmup)
+        ms, dms, lms = r.time_steps(steps)
+        rf = roofline_of(wl, ms / steps, dms, lms)
+        assert pkg.fpd_device_status(r.stream) == 0, "device-side check failed"
+        line = {"metric": METRIC, "value": B * (L - 1) * steps / (ms * 1e-3), "unit": "draft tokens/s",
+                "n_gpus": 1, "steps": steps, "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+                "dtype": "bf16", "data": "synthetic", "sweep_point": idx,
+                "config": workload_config(f"sweep_B{B}_T{T}_L{L}", wl),
+                "blocks_per_s": B * steps / (ms * 1e-3), "roofline": rf, "gpu_launches": r.launches_per_step * steps}
+        print(json.dumps(line), flush=True)
+        del r
+        torch.cuda.synchronize()
+    dr.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -138,10 +398,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="text_4b_b1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-batched", action="store_true", help="skip the batched workload's extra measurement")
+    ap.add_argument("--sweep", action="store_true", help="time the 32-point sweep, one line per point")
     args = ap.parse_args()
 
     import torch
     import synth
+
+    if args.sweep:
+        import block_diffusion_speculative_non_gb300 as pkg
+        run_sweep(pkg, min(args.steps, 10), args.warmup)
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -157,10 +424,7 @@ def main():
     s = wl.shape
     L, B = wl.block_len, wl.batch
     draft_tokens_per_step = B * (L - 1)
-    config = {"workload": args.workload, "batch": B, "block_len": L, "context": wl.ctx_len.tolist() if B <= 4 else
-              [int(wl.ctx_len.min()), int(wl.ctx_len.max())], "d_model": s.d_model, "layers": s.n_layers,
-              "vocab": s.vocab, "layout": "unconstrained" if wl.layout is None else args.workload.split("_")[1],
-              "l2": "inputs larger than L2 (1.83 GB weights streamed per step)"}
+    config = workload_config(args.workload, wl)
 
     if args.impl == "reference":
         # the CPU oracle, as it stands, on the host cores: rank 0 only
@@ -194,117 +458,30 @@ def main():
     import block_diffusion_speculative_non_gb300 as pkg
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    hbm_peak, tc_peak, peak_kind = peaks()
 
     w = synth.make_weights(s, wl.seed)
     dr = pkg.Drafter(s, w, B, L, wl.t_cap, device=dev)
-    feats = synth.make_features(s, int(wl.row_off[-1]), wl.seed + 1)
-    stream = torch.cuda.current_stream(dev)
-    # context preparation (timed separately, once)
-    fd, row_off_d, _ = dr.prepare_context(B, wl.row_off, feats)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    pkg.fpd_prepare_context(dr.handle, B, int(wl.row_off[-1]), row_off_d, None, fd, dr.kv_store, dr.t_cap,
-                            dr.workspace, dr.ws_bytes, stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    prepare_ms = e0.elapsed_time(e1)
-
-    ctx_len = torch.from_numpy(wl.ctx_len).to(dev)
-    anchor = torch.from_numpy(wl.anchor).to(dev)
-    hidden = torch.empty(B * L, s.d_model, dtype=torch.bfloat16, device=dev)
-    tokens = torch.empty(B, L - 1, dtype=torch.int32, device=dev)
-    accept = torch.empty(B, dtype=torch.int32, device=dev)
-    committed = torch.empty(B, L, dtype=torch.int32, device=dev)
-    valid = torch.empty(B, dtype=torch.int32, device=dev)
-    lay_d = rule_d = None
-    if wl.layout is not None:
-        lay_d, rule_d = pkg.Drafter.layout(wl.layout, B, L, dev)
-    # target rows: Geometric(p) agreement with the drafter's own ids (text mode)
-    pkg.fpd_draft_block(dr.handle, B, L, dr.kv_store, dr.t_cap, ctx_len, anchor, wl.mask_id, hidden, None,
-                        dr.workspace, dr.ws_bytes, stream)
-    pkg.fpd_constrain_argmax(dr.handle, B, L, hidden, lay_d, tokens, None, dr.workspace, dr.ws_bytes, stream)
-    torch.cuda.synchronize()
-    target_np = None
-    if wl.layout is None:
-        target_np, _ = synth.make_target_rows(tokens.cpu().numpy(), s.vocab, wl.geo_p or 0.25, wl.seed + 2)
-    target = torch.from_numpy(target_np).to(dev) if target_np is not None else None
-
-    def do_draft(st):
-        pkg.fpd_draft_block(dr.handle, B, L, dr.kv_store, dr.t_cap, ctx_len, anchor, wl.mask_id, hidden, None,
-                            dr.workspace, dr.ws_bytes, st)
-
-    def do_argmax(st):
-        pkg.fpd_constrain_argmax(dr.handle, B, L, hidden, lay_d, tokens, None, dr.workspace, dr.ws_bytes, st)
-
-    def do_verify(st):
-        if wl.layout is None:
-            pkg.fpd_verify(0, B, L, tokens, target, None, None, -1, accept, committed, valid, st)
-        else:
-            pkg.fpd_verify(1, B, L, tokens, None, lay_d, rule_d, wl.layout["pad_id"], accept, committed, valid, st)
-
-    # eager warm-up (also counts the kernels one step launches)
-    for _ in range(max(3, args.warmup)):
-        n0 = pkg.fpd_kernel_launches()
-        do_draft(stream)
-        do_argmax(stream)
-        do_verify(stream)
-        launches_per_step = pkg.fpd_kernel_launches() - n0
-    torch.cuda.synchronize()
-
-    # the step as three CUDA graphs (draft | LM head + argmax | verify) so the LM-head call can be timed live
-    cap = torch.cuda.Stream(dev)
-    graphs = []
-    for fn in (do_draft, do_argmax, do_verify):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            fn(torch.cuda.current_stream(dev))
-        graphs.append(g)
-    g_draft, g_argmax, g_verify = graphs
-    ev_lm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-
-    def step(i=None):
-        g_draft.replay()
-        if i is not None:
-            ev_lm[i][0].record(stream)
-        g_argmax.replay()
-        if i is not None:
-            ev_lm[i][1].record(stream)
-        g_verify.replay()
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
+    r = StepRunner(pkg, dr, wl, dev)
+    r.capture(args.warmup)
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clock_fd, clock_path = tempfile.mkstemp(prefix=f"fpd_bench_clocks_r{rank}_", suffix=".csv")
     os.close(clock_fd)
     with ClockSampler(clock_path) as cs:
-        barrier()
-        torch.cuda.synchronize()
-        t0e.record(stream)
-        for i in range(args.steps):
-            step(i)
-        t1e.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-    launches = launches_per_step * args.steps      # graph replays: the kernels of one step, K times
-    elapsed_ms = t0e.elapsed_time(t1e)
-    lm_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_lm]))
-    assert pkg.fpd_device_status(stream) == 0, "device-side check failed"
+        elapsed_ms, draft_ms, lm_ms = r.time_steps(args.steps, barrier)
+    launches = r.launches_per_step * args.steps      # graph replays: the kernels of one step, K times
+    assert pkg.fpd_device_status(r.stream) == 0, "device-side check failed"
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     ms_per_step = elapsed_ms / args.steps
     value = replica_throughput(world, draft_tokens_per_step, args.steps, elapsed_ms)
 
     # ---- end to end through the C ABI with host buffers: H2D of the step's inputs, D2H of its results --------
     a_h = torch.from_numpy(wl.anchor.copy()).pin_memory()
-    t_h = torch.from_numpy(target_np.copy()).pin_memory() if target_np is not None else None
+    t_h = torch.from_numpy(r.target_np.copy()).pin_memory() if r.target_np is not None else None
     acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
     com_h = torch.empty(B, L, dtype=torch.int32).pin_memory()
     h2d = a_h.numel() * 4 + (t_h.numel() * 4 if t_h is not None else 0)
@@ -314,25 +491,17 @@ def main():
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        anchor.copy_(a_h, non_blocking=True)
+        r.anchor.copy_(a_h, non_blocking=True)
         if t_h is not None:
-            target.copy_(t_h, non_blocking=True)
-        step()
-        acc_h.copy_(accept, non_blocking=True)
-        com_h.copy_(committed, non_blocking=True)
-        stream.synchronize()
+            r.target.copy_(t_h, non_blocking=True)
+        r.step()
+        acc_h.copy_(r.accept, non_blocking=True)
+        com_h.copy_(r.committed, non_blocking=True)
+        r.stream.synchronize()
     e2e_s = time.perf_counter() - t0
     e2e_value = world * draft_tokens_per_step * e2e_steps / e2e_s
 
-    # ---- roofline of the dominant kernel (LM head call: final norm + LM-head GEMM/argmax + decode) -------
-    layer_b, lm_b, kv_b = algorithmic_bytes(s, B, L, wl.ctx_len)
-    lm_bytes = lm_b + B * (L - 1) * s.d_model * 2
-    achieved = lm_bytes / (lm_ms * 1e-3) / 1e9
-    block_bytes = layer_b + lm_b + kv_b
-    roofline = {"bound": "hbm", "kernel": "fpd_constrain_argmax (LM head, 128-id x token tiles, tcgen05)",
-                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "peak_kind": f"{peak_kind} (copy, burst)", "traffic": None,
-                "block_bytes": block_bytes, "block_frac": block_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak}
+    roofline = roofline_of(wl, ms_per_step, draft_ms, lm_ms, profiled_traffic(args.workload))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -349,6 +518,13 @@ def main():
         except Exception as e:  # the baseline is reported, never required
             cpu = {"value": None, "unit": "draft tokens/s", "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
 
+    prepare_ms = r.prepare_ms
+    del r
+    dr.close()
+    batched = None
+    if rank == 0 and world == 1 and B * L < 300 and not args.no_batched:
+        batched = run_batched_extra(pkg, w, dev)
+
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "draft tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -358,12 +534,13 @@ def main():
                 "e2e": {"value": e2e_value, "unit": "draft tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": int(launches), "clocks": cs.summary(local_rank)}
+        if batched is not None:
+            line["batched"] = batched
         print(json.dumps(line), flush=True)
     try:
         os.remove(clock_path)
     except OSError:
         pass
-    dr.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -68,6 +68,96 @@ struct Smem {
   bf16 v[2][KT * H];
 };
 
+// One 64-key tile of the online softmax for one warp's 16 query rows (rows lane/4 and lane/4 + 8 of its m16
+// fragment): S = Q K^T on mma.sync from the swizzled K tile at ks, keys at or past k_end masked, running maximum
+// (m0, m1) and sum (l0, l1) in base 2, O += (P_hi + P_lo) V from the V tile at vs.  k0: the tile's first key.
+template <int H>
+__device__ __forceinline__ void attn_tile_math(uint32_t ks, uint32_t vs, const uint32_t (&qf)[H / 16][4],
+                                               float (&o)[H / 8][4], float& m0, float& m1, float& l0, float& l1,
+                                               int k0, int k_end, int lane, float sl2) {
+  constexpr int NKS = H / 16;   // k-steps over the head dimension
+  constexpr int NOT = H / 8;    // 8-wide n-tiles of O
+  // ---- S = Q K^T: 16 rows x 64 keys per warp ----
+  float s[KT / 8][4];
+#pragma unroll
+  for (int n = 0; n < KT / 8; n++) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+  for (int kp = 0; kp < KT / 16; kp++) {
+#pragma unroll
+    for (int kk = 0; kk < NKS; kk++) {
+      // 8x8 matrices: (keys +0..7, dims lo), (keys +0..7, dims hi), (keys +8..15, dims lo), (keys +8..15, dims hi)
+      const int key = kp * 16 + (lane & 7) + ((lane >> 4) << 3);
+      const int c = kk * 2 + ((lane >> 3) & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(swz<H>(ks, key, c), b0, b1, b2, b3);
+      mma_bf16(s[2 * kp], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+      mma_bf16(s[2 * kp + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+    }
+  }
+  // ---- online softmax (base 2) ----
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int n = 0; n < KT / 8; n++) {
+    const int key = k0 + n * 8 + (lane & 3) * 2;
+    const bool v0 = key < k_end, v1 = key + 1 < k_end;
+    s[n][0] = v0 ? s[n][0] * sl2 : -INFINITY;
+    s[n][1] = v1 ? s[n][1] * sl2 : -INFINITY;
+    s[n][2] = v0 ? s[n][2] * sl2 : -INFINITY;
+    s[n][3] = v1 ? s[n][3] * sl2 : -INFINITY;
+    mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
+    mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+  }
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: every tile holds at least one valid key
+  const float c0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mn0);
+  const float c1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mn1);
+  m0 = mn0;
+  m1 = mn1;
+  float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+  for (int n = 0; n < KT / 8; n++) {
+    s[n][0] = exp2f(s[n][0] - mn0);
+    s[n][1] = exp2f(s[n][1] - mn0);
+    s[n][2] = exp2f(s[n][2] - mn1);
+    s[n][3] = exp2f(s[n][3] - mn1);
+    ps0 += s[n][0] + s[n][1];
+    ps1 += s[n][2] + s[n][3];
+  }
+  l0 = l0 * c0 + ps0;
+  l1 = l1 * c1 + ps1;
+#pragma unroll
+  for (int n = 0; n < NOT; n++) {
+    o[n][0] *= c0;
+    o[n][1] *= c0;
+    o[n][2] *= c1;
+    o[n][3] *= c1;
+  }
+  // ---- O += (P_hi + P_lo) V ----
+#pragma unroll
+  for (int kk = 0; kk < KT / 16; kk++) {
+    uint32_t h0, h1, h2, h3, l0_, l1_, l2_, l3_;
+    split_bf16x2(s[2 * kk][0], s[2 * kk][1], h0, l0_);
+    split_bf16x2(s[2 * kk][2], s[2 * kk][3], h1, l1_);
+    split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], h2, l2_);
+    split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], h3, l3_);
+#pragma unroll
+    for (int np = 0; np < NOT / 2; np++) {
+      // transposed 8x8 matrices: (keys +0..7, dims lo), (keys +8..15, dims lo), (keys +0..7, dims hi), (keys +8..15, dims hi)
+      const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int c = np * 2 + (lane >> 4);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(swz<H>(vs, key, c), b0, b1, b2, b3);
+      mma_bf16(o[2 * np], h0, h1, h2, h3, b0, b1);
+      mma_bf16(o[2 * np + 1], h0, h1, h2, h3, b2, b3);
+      mma_bf16(o[2 * np], l0_, l1_, l2_, l3_, b0, b1);
+      mma_bf16(o[2 * np + 1], l0_, l1_, l2_, l3_, b2, b3);
+    }
+  }
+}
+
 // One (query tile, request x kv head, KV split) unit of the attention, run by 128 threads (tid 0..127) that
 // synchronise with `sync` (the whole CTA in the standalone kernel, a named barrier inside the persistent kernel).
 template <int H, class Sync>
@@ -154,86 +244,7 @@ __device__ __forceinline__ void attn_tile(const AttnArgs& a, bf16* __restrict__ 
       cp_async_wait<0>();
     }
     sync();
-    const uint32_t ks = smem_addr(sm.k[buf]), vs = smem_addr(sm.v[buf]);
-    // ---- S = Q K^T: 16 rows x 64 keys per warp ----
-    float s[KT / 8][4];
-#pragma unroll
-    for (int n = 0; n < KT / 8; n++) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-    for (int kp = 0; kp < KT / 16; kp++) {
-#pragma unroll
-      for (int kk = 0; kk < NKS; kk++) {
-        // 8x8 matrices: (keys +0..7, dims lo), (keys +0..7, dims hi), (keys +8..15, dims lo), (keys +8..15, dims hi)
-        const int key = kp * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int c = kk * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(swz<H>(ks, key, c), b0, b1, b2, b3);
-        mma_bf16(s[2 * kp], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-        mma_bf16(s[2 * kp + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
-      }
-    }
-    // ---- online softmax (base 2) ----
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < KT / 8; n++) {
-      const int key = k0 + n * 8 + (lane & 3) * 2;
-      const bool v0 = key < k_end, v1 = key + 1 < k_end;
-      s[n][0] = v0 ? s[n][0] * sl2 : -INFINITY;
-      s[n][1] = v1 ? s[n][1] * sl2 : -INFINITY;
-      s[n][2] = v0 ? s[n][2] * sl2 : -INFINITY;
-      s[n][3] = v1 ? s[n][3] * sl2 : -INFINITY;
-      mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: every tile holds at least one valid key
-    const float c0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mn0);
-    const float c1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int n = 0; n < KT / 8; n++) {
-      s[n][0] = exp2f(s[n][0] - mn0);
-      s[n][1] = exp2f(s[n][1] - mn0);
-      s[n][2] = exp2f(s[n][2] - mn1);
-      s[n][3] = exp2f(s[n][3] - mn1);
-      ps0 += s[n][0] + s[n][1];
-      ps1 += s[n][2] + s[n][3];
-    }
-    l0 = l0 * c0 + ps0;
-    l1 = l1 * c1 + ps1;
-#pragma unroll
-    for (int n = 0; n < NOT; n++) {
-      o[n][0] *= c0;
-      o[n][1] *= c0;
-      o[n][2] *= c1;
-      o[n][3] *= c1;
-    }
-    // ---- O += (P_hi + P_lo) V ----
-#pragma unroll
-    for (int kk = 0; kk < KT / 16; kk++) {
-      uint32_t h0, h1, h2, h3, l0_, l1_, l2_, l3_;
-      split_bf16x2(s[2 * kk][0], s[2 * kk][1], h0, l0_);
-      split_bf16x2(s[2 * kk][2], s[2 * kk][3], h1, l1_);
-      split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], h2, l2_);
-      split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], h3, l3_);
-#pragma unroll
-      for (int np = 0; np < NOT / 2; np++) {
-        // transposed 8x8 matrices: (keys +0..7, dims lo), (keys +8..15, dims lo), (keys +0..7, dims hi), (keys +8..15, dims hi)
-        const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int c = np * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(swz<H>(vs, key, c), b0, b1, b2, b3);
-        mma_bf16(o[2 * np], h0, h1, h2, h3, b0, b1);
-        mma_bf16(o[2 * np + 1], h0, h1, h2, h3, b2, b3);
-        mma_bf16(o[2 * np], l0_, l1_, l2_, l3_, b0, b1);
-        mma_bf16(o[2 * np + 1], l0_, l1_, l2_, l3_, b2, b3);
-      }
-    }
+    attn_tile_math<H>(smem_addr(sm.k[buf]), smem_addr(sm.v[buf]), qf, o, m0, m1, l0, l1, k0, k_end, lane, sl2);
     sync();   // this buffer is refilled by the next iteration's prefetch
   }
 

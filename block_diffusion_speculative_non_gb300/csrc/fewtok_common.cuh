@@ -51,57 +51,65 @@ __device__ __forceinline__ void inv_from_partials(const float* ss_in, int n_ss, 
   }
 }
 
-// 1/rms per token over whole rows already in the activation region (LM head: all K atoms resident).
-__device__ __forceinline__ void inv_from_rows(const uint8_t* act, int nkb, int M, int d, float eps, float* s_inv,
-                                              int quarter, int lane) {
-  for (int j = quarter; j < M; j += 4) {
-    float ss = 0.f;
-    for (int a = 0; a < nkb; a++) {   // the swizzle permutes 16-byte chunks within a row: the sum is unaffected
-      const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162*>(act + a * X_ATOM + j * 128 + lane * 4);
-      ss += bf(e.x) * bf(e.x) + bf(e.y) * bf(e.y);
+// 1/rms per token over whole rows already in the activation region (LM head: all K atoms resident).  Thread et
+// sums the squares of row j = et / 8, physical 16-byte chunk et % 8 of every atom (the swizzle permutes chunks
+// within a row, so the row sum is unaffected), then the 8 threads of a row combine in a fixed xor tree.
+__device__ __forceinline__ void inv_from_rows(const uint8_t* act, int nkb, int d, float eps, float* s_inv, int et) {
+  const int j = et >> 3, pc = et & 7;
+  float ss = 0.f;
+#pragma unroll 8
+  for (int a = 0; a < nkb; a++) {
+    const uint4 u = *reinterpret_cast<const uint4*>(act + a * X_ATOM + j * 128 + (pc << 4));
+    const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const float2 f = __bfloat1622float2(e[k]);
+      ss += f.x * f.x + f.y * f.y;
     }
-    ss = warp_sum(ss);
-    if (lane == 0) s_inv[j] = rsqrtf(ss / (float)d + eps);
   }
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+  if (pc == 0) s_inv[j] = rsqrtf(ss / (float)d + eps);
 }
 
-// xn = bf16(x * inv[j] * g[k]) in place over nkb TMA-loaded atoms (rows j < M); physical 16-byte chunk pc of row
-// j holds logical chunk pc ^ (j & 7) (128-byte swizzle).  gbuf: the gain slice, 128 bytes per atom.  Thread et
-// takes chunks et, et + 128, ... of every row, so no index needs a division.
-__device__ __forceinline__ void norm_in_place(uint8_t* act, const uint8_t* gbuf, const float* s_inv, int M, int nkb,
-                                              int et) {
-  const int cpr = nkb * 8;
-  for (int j = 0; j < M; j++) {
-    const float inv = s_inv[j];
-    for (int cc = et; cc < cpr; cc += 128) {
-      const int a = cc >> 3, pc = cc & 7, q = pc ^ (j & 7);
-      uint4* xp = reinterpret_cast<uint4*>(act + a * X_ATOM + j * 128 + (pc << 4));
-      const uint4 gu = *reinterpret_cast<const uint4*>(gbuf + a * G_ATOM + q * 16);
+// xn = bf16(x * inv[j] * g[k]) in place over the TMA-loaded atoms [a0, a0 + na) (na <= 4, 16 rows each): thread et
+// takes row j = et / 8 and physical 16-byte chunk pc = et % 8 of every atom, which holds logical chunk pc ^ (j & 7)
+// (128-byte swizzle).  gbuf: the gain slice, 128 bytes per atom.  Rows past the call's tokens are zero and stay so.
+__device__ __forceinline__ void norm_atoms(uint8_t* act, const uint8_t* gbuf, const float* s_inv, int a0, int na,
+                                           int et) {
+  const int j = et >> 3, pc = et & 7, q = pc ^ (j & 7);
+  const float inv = s_inv[j];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    if (i < na) {
+      uint4* xp = reinterpret_cast<uint4*>(act + (a0 + i) * X_ATOM + j * 128 + (pc << 4));
+      const uint4 gu = *reinterpret_cast<const uint4*>(gbuf + (a0 + i) * G_ATOM + q * 16);
       uint4 u = *xp;
       __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&u);
       const __nv_bfloat162* gg = reinterpret_cast<const __nv_bfloat162*>(&gu);
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const float2 xf = __bfloat1622float2(e[i]), gf = __bfloat1622float2(gg[i]);
-        e[i] = __floats2bfloat162_rn(xf.x * inv * gf.x, xf.y * inv * gf.y);
+      for (int k = 0; k < 4; k++) {
+        const float2 xf = __bfloat1622float2(e[k]), gf = __bfloat1622float2(gg[k]);
+        e[k] = __floats2bfloat162_rn(xf.x * inv * gf.x, xf.y * inv * gf.y);
       }
       *xp = u;
     }
   }
 }
 
-// Split-K without a reduce kernel: every CTA stores its fp32 partial tile ([splits][tiles][16][128]); the last CTA
-// of the tile to arrive (atomic counter, no waiting) sums all partials in split order into v — bit-reproducible —
-// and resets the counter.  Returns true in that CTA.  All 128 epilogue threads call it.  Ordering: the stores of
-// all threads precede thread 0's acquire-release counter update through the CTA barrier (the release is
-// cumulative), and the winner's reads follow its acquire through the second barrier.
+// Split-K without a reduce kernel: every CTA stores its fp32 partial tile ([splits][tiles][128 rows][16 tokens],
+// 64 contiguous bytes per row); the last CTA of the tile to arrive (atomic counter, no waiting) sums all partials in
+// split order into v — bit-reproducible — and resets the counter.  Returns true in that CTA.  All 128 epilogue
+// threads call it.  Ordering: the stores of all threads precede thread 0's acquire-release counter update through
+// the CTA barrier (the release is cumulative), and the winner's reads follow its acquire through the second
+// barrier.  The winner loads up to eight splits at once: the reduction is one round trip to L2 per eight splits.
 __device__ __forceinline__ bool splitk_last(float (&v)[16], float* part, int* counters, int split, int splits,
-                                            int tile, int tiles, int M, int row_in_tile, int et, int* s_flag) {
+                                            int tile, int tiles, int row_in_tile, int et, int* s_flag) {
   if (splits <= 1) return true;
-  float* mine = part + (((size_t)split * tiles + tile) * SBN) * SBM + row_in_tile;
+  float4* mine = reinterpret_cast<float4*>(part + (((size_t)split * tiles + tile) * SBM + row_in_tile) * SBN);
 #pragma unroll
-  for (int j = 0; j < 16; j++)
-    if (j < M) __stcg(mine + j * SBM, v[j]);
+  for (int q = 0; q < 4; q++) __stcg(mine + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
   epi_bar();
   if (et == 0) {
     int old;
@@ -112,21 +120,52 @@ __device__ __forceinline__ bool splitk_last(float (&v)[16], float* part, int* co
   if (!*s_flag) return false;
 #pragma unroll
   for (int j = 0; j < 16; j++) v[j] = 0.f;
-  for (int s0 = 0; s0 < splits; s0 += 4) {   // four splits' loads in flight, summed in split order
-    float pv[4][16];
+  for (int s0 = 0; s0 < splits; s0 += 8) {
+    float4 pv[8][4];
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const float* ps = part + (((size_t)(s0 + u) * tiles + tile) * SBN) * SBM + row_in_tile;
+    for (int u = 0; u < 8; u++) {
+      const float4* ps =
+          reinterpret_cast<const float4*>(part + (((size_t)(s0 + u) * tiles + tile) * SBM + row_in_tile) * SBN);
 #pragma unroll
-      for (int j = 0; j < 16; j++) pv[u][j] = (s0 + u < splits && j < M) ? __ldcg(ps + j * SBM) : 0.f;
+      for (int q = 0; q < 4; q++) pv[u][q] = s0 + u < splits ? __ldcg(ps + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 4; u++)
+    for (int u = 0; u < 8; u++)
 #pragma unroll
-      for (int j = 0; j < 16; j++) v[j] += pv[u][j];
+      for (int q = 0; q < 4; q++) {
+        v[4 * q] += pv[u][q].x;
+        v[4 * q + 1] += pv[u][q].y;
+        v[4 * q + 2] += pv[u][q].z;
+        v[4 * q + 3] += pv[u][q].w;
+      }
   }
   if (et == 0) counters[tile] = 0;
   return true;
+}
+
+// Sums each of 16 per-lane values over the 32 lanes of a warp in 16 shuffles (each round halves the values a lane
+// keeps and trades the other half with its partner); returns the sum of value (lane >> 1) & 15, held by lanes 2t
+// and 2t + 1 for token t.  Fixed order, so bit-reproducible.
+__device__ __forceinline__ float warp_sum16(const float (&x)[16], int lane) {
+  float a[8], b[4], c[2];
+  const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const float send = h16 ? x[i] : x[i + 8];
+    a[i] = (h16 ? x[i + 8] : x[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float send = h8 ? a[i] : a[i + 4];
+    b[i] = (h8 ? a[i + 4] : a[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; i++) {
+    const float send = h4 ? b[i] : b[i + 2];
+    c[i] = (h4 ? b[i + 2] : b[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  const float d = (h2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, h2 ? c[0] : c[1], 2);
+  return d + __shfl_xor_sync(0xffffffffu, d, 1);
 }
 
 // The residual-stream values of one 128-column tile that resid_epilogue adds to (loaded early, while the MMAs run:
@@ -144,18 +183,19 @@ __device__ __forceinline__ void resid_epilogue(const float (&v)[16], const float
                                                int lane, int et) {
   const int n = tile * SBM + quarter * 32 + lane;
   float* red = scratch;   // [4 warps][16]
+  float sq[16];
 #pragma unroll
   for (int j = 0; j < 16; j++) {
-    float sq = 0.f;
+    sq[j] = 0.f;
     if (j < M) {
       const bf16 nb = __float2bfloat16_rn(xv[j] + v[j]);
       x[(size_t)j * N + n] = nb;
       if (layer_out) layer_out[(size_t)j * N + n] = nb;
-      sq = bf(nb) * bf(nb);
+      sq[j] = bf(nb) * bf(nb);
     }
-    sq = warp_sum(sq);
-    if (lane == 0) red[quarter * SBN + j] = sq;
   }
+  const float st = warp_sum16(sq, lane);
+  if ((lane & 1) == 0) red[quarter * SBN + (lane >> 1)] = st;
   epi_bar();
   if (et < SBN) ss_out[tile * SBN + et] = red[et] + red[SBN + et] + red[2 * SBN + et] + red[3 * SBN + et];
   epi_bar();

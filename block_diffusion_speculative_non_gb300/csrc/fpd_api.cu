@@ -350,6 +350,7 @@ fpd_status fpd_model_create(const fpd_model_desc* desc, const fpd_weights* w, fp
       if (init_err == cudaSuccess) init_err = attn_init_attributes();
       if (init_err == cudaSuccess) init_err = stream_init_attributes();
       if (init_err == cudaSuccess) init_err = attn_tc_init_attributes();
+      if (init_err == cudaSuccess) init_err = attn_short_init_attributes();
     });
     if (init_err != cudaSuccess) return cuda_fail(init_err, "kernel attributes");
   }
@@ -514,7 +515,9 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
   a.splits = w.att_splits;
   a.chunk = w.att_chunk;
   if (w.stream) {
-    // few-token path: 6 kernels per layer, norms applied on load, split-K reduced inside the GEMMs
+    // few-token path: 5 kernels per layer, norms applied on load, split-K reduced inside the GEMMs, attention
+    // splits merged inside the attention kernel
+    const bool short_attn = attn_short_supported(h, L, nq, nkv);
     FPD_CUDA(launch_embed_ss(x, w.ss_a, w.cnt_qkv, w.n_cnt, (const bf16*)m->w.embed, anchor, mask_id, batch, L, dm,
                              d.vocab, st),
              "embedding");
@@ -551,7 +554,7 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
       g.h = h;
       FPD_CUDA(launch_stream_gemm(g, st), "QKV GEMM + q/k norm + RoPE");
       a.layer = l;
-      FPD_CUDA(launch_attention(a, w.o, st), "attention");
+      FPD_CUDA(short_attn ? launch_attention_short(a, w.o, st) : launch_attention(a, w.o, st), "attention");
       // O projection + residual
       StreamGemm o = g;
       o.epi = SEPI_RESID;

@@ -133,6 +133,13 @@ struct AttnArgs {
 void attn_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* splits, int* chunk);
 cudaError_t launch_attention(const AttnArgs& a, bf16* out, cudaStream_t st);          // mma.sync tiles of 64 rows
 cudaError_t launch_attn_merge(const AttnArgs& a, bf16* out, cudaStream_t st);         // split merge, fixed order
+// few-token attention (k_attention_short.cu): at most 64 query rows per (request, kv head); the KV splits of one
+// (request, kv head) form a thread-block cluster and merge through distributed shared memory (no partials, no merge
+// kernel).  The call's first kernel must trigger its successors only after its own griddepcontrol.wait: the
+// kernel reads the context store before waiting.
+bool attn_short_supported(int head_dim, int L, int nq, int nkv);
+cudaError_t attn_short_init_attributes();
+cudaError_t launch_attention_short(const AttnArgs& a, bf16* out, cudaStream_t st);
 // tcgen05 attention (k_attention_tc.cu): 128-row query tiles, head_dim 128; same partial layout and merge
 bool attn_tc_supported(int head_dim, int L, int nq, int nkv);
 void attn_tc_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* splits, int* chunk);

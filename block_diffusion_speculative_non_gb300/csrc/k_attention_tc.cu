@@ -195,6 +195,9 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
     tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
   }
+  // The single-lane roles reconverge with their warps first: a CTA barrier reached by part of a diverged
+  // warp counts the whole warp, and the lagging lane would then pass it without waiting.
+  __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -416,6 +419,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
     }
   }
 
+  __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -174,6 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     tc::tma_prefetch(&p.tm_w);
     for (int s = 0; s < p.n_seg; s++) tc::tma_prefetch(&p.tm_x[s]);
   }
+  // The single-lane roles reconverge with their warps first: a CTA barrier reached by part of a diverged
+  // warp counts the whole warp, and the lagging lane would then pass it without waiting.
+  __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -531,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
   }
 
+  __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) {

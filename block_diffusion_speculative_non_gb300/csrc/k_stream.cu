@@ -31,11 +31,14 @@ namespace {
 using namespace fewtok;
 
 constexpr int kSThreads = 192;
-constexpr int kSStages = 8;
+constexpr int kMinStages = 8;                 // weight ring depth: 8 atoms (128 KB) in flight per CTA; deeper rings
+constexpr int kMaxStages = 8;                 // (10-14 atoms) measured slower on the 4B shape at batch 1
 constexpr int kTmemCols = 32;                 // two 16-column accumulators
-// misc region: mbarriers full[S], empty[S], act_tma, act_full, tfull[2], tempty[2] | TMEM slot, abort, last-CTA
-// flag | inverse RMS per token [16] | context length per request [16] | running top-2 per token [16][2]
-constexpr int kMiscFlags = 8 * (2 * kSStages + 6);
+constexpr int kActGroup = 4;                  // activation atoms per readiness barrier
+constexpr int kMaxActGroups = 12;             // activation slices of up to 48 atoms (K <= 3072)
+// misc region: mbarriers full[S], empty[S], act_tma[G], act_ready[G], tfull[2], tempty[2] | TMEM slot, abort,
+// last-CTA flag | inverse RMS per token [16] | context length per request [16] | running top-2 per token [16][2]
+constexpr int kMiscFlags = 8 * (2 * kMaxStages + 2 * kMaxActGroups + 4);
 constexpr int kMiscInv = kMiscFlags + 16;
 constexpr int kMiscCtx = kMiscInv + SBN * 4;
 constexpr int kMiscRun = kMiscCtx + SBN * 4;
@@ -57,7 +60,7 @@ struct StreamParams {
   const bf16* gain;            // XF_NORM / XF_NORM_FULL: RMSNorm gain [K]
   float eps;
   // split-K reduction
-  float* part;                 // [splits][tiles][16][128]
+  float* part;                 // [splits][tiles][128][16]
   int* counters;               // [tiles], zero on entry, left zero
   // SEPI_QKV
   bf16 *q, *kblk, *vblk;
@@ -73,6 +76,7 @@ struct StreamParams {
   // SEPI_ARGMAX
   unsigned long long* slots;   // [gridDim][16][2]
   float* logits;               // [M][N] or null
+  int stages;                  // weight ring depth, kMinStages..kMaxStages
 };
 
 template <int EPI>
@@ -81,7 +85,8 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int n_act = p.k_split / SBK;                          // activation atoms of one split (LM head: all K)
   uint8_t* ring = smem;
-  uint8_t* act = smem + kSStages * W_ATOM;
+  const int n_stages = p.stages;
+  uint8_t* act = smem + n_stages * W_ATOM;
   uint8_t* gbuf = act + n_act * X_ATOM;
   float* scratch = reinterpret_cast<float*>(gbuf + n_act * G_ATOM);
   uint8_t* misc = reinterpret_cast<uint8_t*>(scratch) + kEpiScratch;
@@ -92,8 +97,8 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
   float* s_inv = reinterpret_cast<float*>(misc + kMiscInv);
   int* s_ctx = reinterpret_cast<int*>(misc + kMiscCtx);
   unsigned long long* s_run = reinterpret_cast<unsigned long long*>(misc + kMiscRun);
-  const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kSStages, actt = empty0 + 8 * kSStages,
-                 actb = actt + 8, tfull0 = actb + 8, tempty0 = tfull0 + 16;
+  const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kMaxStages, actt0 = empty0 + 8 * kMaxStages,
+                 actr0 = actt0 + 8 * kMaxActGroups, tfull0 = actr0 + 8 * kMaxActGroups, tempty0 = tfull0 + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   pdl_trigger();
@@ -102,12 +107,14 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
   const int stride = persistent ? gridDim.x : total;   // one work item per CTA otherwise
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSStages; s++) {
+    for (int s = 0; s < n_stages; s++) {
       tc::mbar_init(full0 + 8 * s, 1);
       tc::mbar_init(empty0 + 8 * s, 1);
     }
-    tc::mbar_init(actt, 1);
-    tc::mbar_init(actb, 1);
+    for (int g = 0; g < kMaxActGroups; g++) {
+      tc::mbar_init(actt0 + 8 * g, 1);
+      tc::mbar_init(actr0 + 8 * g, 1);
+    }
     for (int a = 0; a < 2; a++) {
       tc::mbar_init(tfull0 + 8 * a, 1);
       tc::mbar_init(tempty0 + 8 * a, 4);
@@ -123,6 +130,9 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
     tc::tma_prefetch(&p.tm_w);
     tc::tma_prefetch(&p.tm_x);
   }
+  // The single-lane roles reconverge with their warps first: a CTA barrier reached by part of a diverged
+  // warp counts the whole warp, and the lagging lane would then pass it without waiting.
+  __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -154,7 +164,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
           tc::tma_load_2d(dst, &p.tm_w, k0 + kb * SBK, tile * SBM, fb);
         }
         issued++;
-        if (++stage == kSStages) { stage = 0; phase ^= 1; }
+        if (++stage == n_stages) { stage = 0; phase ^= 1; }
         if (++kb == nkb) {
           kb = 0;
           t += stride;
@@ -162,19 +172,24 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
         }
       };
       // the first ring of weights: weights never depend on earlier kernels, so no griddepcontrol.wait yet
-      while (t < total && issued < kSStages) issue_w();
-      // the activation slice (and the norm gain slice) once the predecessor kernel has completed
+      while (t < total && issued < n_stages) issue_w();
+      // the activation slice (and the norm gain slice) once the predecessor kernel has completed, in groups of
+      // kActGroup atoms so that the transform and the products start on the first group
       pdl_wait();
       if (blockIdx.x < total) {
         const bool gains = p.xform != XF_COPY;
-        tc::mbar_arrive_expect_tx(actt, nkb0 * p.x_atom_bytes + (gains ? nkb0 * G_ATOM : 0));
-        for (int a = 0; a < nkb0; a++) {
-          if (p.x_rank == 3)
-            tc::tma_load_3d(tc::smem_u32(act + a * X_ATOM), &p.tm_x, k00 + a * SBK, 0, 0, actt);
-          else
-            tc::tma_load_2d(tc::smem_u32(act + a * X_ATOM), &p.tm_x, k00 + a * SBK, 0, actt);
+        for (int g = 0; g * kActGroup < nkb0; g++) {
+          const int a0 = g * kActGroup, na = min(kActGroup, nkb0 - a0);
+          const uint32_t bar = actt0 + 8 * g;
+          tc::mbar_arrive_expect_tx(bar, na * p.x_atom_bytes + (gains ? na * G_ATOM : 0));
+          for (int a = a0; a < a0 + na; a++) {
+            if (p.x_rank == 3)
+              tc::tma_load_3d(tc::smem_u32(act + a * X_ATOM), &p.tm_x, k00 + a * SBK, 0, 0, bar);
+            else
+              tc::tma_load_2d(tc::smem_u32(act + a * X_ATOM), &p.tm_x, k00 + a * SBK, 0, bar);
+          }
+          if (gains) tc::bulk_load(tc::smem_u32(gbuf + a0 * G_ATOM), p.gain + k00 + a0 * SBK, na * G_ATOM, bar);
         }
-        if (gains) tc::bulk_load(tc::smem_u32(gbuf), p.gain + k00, nkb0 * G_ATOM, actt);
       }
       while (t < total && !*abort_flag) {
         if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1)) {
@@ -184,19 +199,20 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
         issue_w();
       }
       if (*abort_flag) {   // let the copies already issued land before the CTA may exit (bounded)
-        for (int s = 0; s < kSStages && s < issued; s++) {
-          if (--stage < 0) { stage = kSStages - 1; phase ^= 1; }
+        for (int s = 0; s < n_stages && s < issued; s++) {
+          if (--stage < 0) { stage = n_stages - 1; phase ^= 1; }
           tc::mbar_wait(full0 + 8 * stage, phase);
         }
-        if (blockIdx.x < total) tc::mbar_wait(actt, 0);
+        if (blockIdx.x < total)
+          for (int g = 0; g * kActGroup < nkb0; g++) tc::mbar_wait(actt0 + 8 * g, 0);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(SBM, SBN);
-      if (!tc::mbar_wait(actb, 0)) *abort_flag = 1;
-      tc::tc_fence_after();
+      // activation atoms are ready group by group: straight from TMA, or after the norm transform
+      const uint32_t rdy0 = p.xform == XF_COPY ? actt0 : actr0;
       int stage = 0, it = 0;
       uint32_t phase = 0;
       const uint32_t xs = tc::smem_u32(act);
@@ -208,6 +224,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * SBN;
         for (int kb = 0; kb < nkb && !*abort_flag; kb++) {
+          if (kb % kActGroup == 0 && !tc::mbar_wait(rdy0 + 8 * (kb / kActGroup), 0)) { *abort_flag = 1; break; }
           if (!tc::mbar_wait(full0 + 8 * stage, phase)) { *abort_flag = 1; break; }
           tc::tc_fence_after();
           const uint32_t ws = tc::smem_u32(ring + stage * W_ATOM);
@@ -218,7 +235,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
             tc::umma_bf16(d_tmem, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           tc::umma_commit(empty0 + 8 * stage);
-          if (++stage == kSStages) { stage = 0; phase ^= 1; }
+          if (++stage == n_stages) { stage = 0; phase ^= 1; }
         }
         tc::umma_commit(tfull0 + 8 * acc);
       }
@@ -235,13 +252,21 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       s_ctx[et] = cl < 0 ? 0 : (cl > p.t_cap ? p.t_cap : cl);
     }
     if (EPI == SEPI_ARGMAX && et < SBN) s_run[2 * et] = s_run[2 * et + 1] = 0ull;
-    if (blockIdx.x < total && !tc::mbar_wait(actt, 0)) *abort_flag = 1;
-    if (p.xform == XF_NORM_FULL) inv_from_rows(act, nkb0, p.M, p.K, p.eps, s_inv, quarter, lane);
-    epi_bar();
-    if (p.xform != XF_COPY) norm_in_place(act, gbuf, s_inv, p.M, nkb0, et);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
-    epi_bar();
-    if (et == 0) tc::mbar_arrive(actb);
+    if (blockIdx.x < total && p.xform != XF_COPY) {
+      if (p.xform == XF_NORM_FULL) {   // 1/rms from the whole rows: every group first
+        for (int g = 0; g * kActGroup < nkb0; g++)
+          if (!tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
+        inv_from_rows(act, nkb0, p.K, p.eps, s_inv, et);
+      }
+      epi_bar();   // s_inv complete
+      for (int g = 0; g * kActGroup < nkb0; g++) {
+        if (p.xform == XF_NORM && !tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
+        norm_atoms(act, gbuf, s_inv, g * kActGroup, min(kActGroup, nkb0 - g * kActGroup), et);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
+        epi_bar();
+        if (et == 0) tc::mbar_arrive(actr0 + 8 * g);
+      }
+    }
 
     int it = 0;
     for (int t = blockIdx.x; t < total; t += stride, it++) {
@@ -263,7 +288,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       if (lane == 0) tc::mbar_arrive(tempty0 + 8 * acc);
 
       if (EPI == SEPI_QKV || EPI == SEPI_RESID) {
-        if (splitk_last(v, p.part, p.counters, split, p.splits, tile, p.tiles, p.M, row_in_tile, et, s_flag)) {
+        if (splitk_last(v, p.part, p.counters, split, p.splits, tile, p.tiles, row_in_tile, et, s_flag)) {
           if (EPI == SEPI_RESID) {
             resid_epilogue(v, xv, p.xres, p.N, tile, p.M, p.ss_out, nullptr, scratch, quarter, lane, et);
           } else {
@@ -328,6 +353,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
     }
   }
 
+  __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -336,13 +362,23 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
   }
 }
 
-size_t stream_smem_bytes(int act_atoms) {
-  return 1024 + (size_t)kSStages * W_ATOM + (size_t)act_atoms * (X_ATOM + G_ATOM) + kEpiScratch + kMiscBytes;
+size_t stream_smem_bytes(int act_atoms, int stages) {
+  return 1024 + (size_t)stages * W_ATOM + (size_t)act_atoms * (X_ATOM + G_ATOM) + kEpiScratch + kMiscBytes;
+}
+
+size_t stream_smem_bytes(int act_atoms) { return stream_smem_bytes(act_atoms, kMinStages); }
+
+// The deepest ring that fits next to the activation slice: the more weight atoms a CTA holds, the more of its
+// stream arrives while the preceding kernel is still finishing.
+int stream_stages(int act_atoms) {
+  int st = kMaxStages;
+  while (st > kMinStages && stream_smem_bytes(act_atoms, st) > 227 * 1024) st--;
+  return st;
 }
 
 template <int EPI>
 cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
-  const size_t smem = stream_smem_bytes(p.k_split / SBK);
+  const size_t smem = stream_smem_bytes(p.k_split / SBK, p.stages);
   return launch_k(stream_gemm_kernel<EPI>, grid, kSThreads, smem, st, p);
 }
 
@@ -350,8 +386,10 @@ cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
 __global__ void embed_ss_kernel(bf16* __restrict__ x, float* __restrict__ ss, int* __restrict__ counters, int n_cnt,
                                 const bf16* __restrict__ embed, const int32_t* __restrict__ anchor, int32_t mask_id,
                                 int L, int d, int V) {
-  pdl_trigger();
+  // wait first, trigger second: the kernels after this one may then read anything written before the call
+  // (the context store, ctx_len) ahead of their own griddepcontrol.wait
   pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
   const int r = blockIdx.x, b = r / L, j = r % L;
   if (r == 0)
@@ -410,7 +448,8 @@ __global__ void stream_decode_kernel(int32_t* __restrict__ tokens, float* __rest
 
 bool stream_shape_ok(const fpd_model_desc& d) {
   return d.d_model % SBM == 0 && (d.n_q_heads * d.head_dim) % SBM == 0 && (d.n_kv_heads * d.head_dim) % SBM == 0 &&
-         d.d_ff % 64 == 0 && d.d_model % SBK == 0 && stream_smem_bytes(d.d_model / SBK) <= 227 * 1024;
+         d.d_ff % 64 == 0 && d.d_model % SBK == 0 && stream_smem_bytes(d.d_model / SBK) <= 227 * 1024 &&
+         d.d_model / SBK <= kActGroup * kMaxActGroups;
 }
 
 StreamPlan stream_plan(int tiles, int K, int num_sms, bool split_ok) {
@@ -435,7 +474,8 @@ cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st) {
   memset(&p, 0, sizeof(p));
   const int box_rows = g.epi == SEPI_SWIGLU ? 64 : SBM;
   const int w_rows = g.epi == SEPI_SWIGLU ? 2 * g.N : g.N;
-  if (g.M < 1 || g.M > SBN || g.K % SBK) return cudaErrorInvalidValue;
+  if (g.M < 1 || g.M > SBN || g.K % SBK || g.plan.k_split / SBK > kActGroup * kMaxActGroups)
+    return cudaErrorInvalidValue;
   cudaError_t e = make_tmap(&p.tm_w, g.w, w_rows, g.K, g.K, box_rows);
   if (e != cudaSuccess) return e;
   if (g.xform == XF_NORM_FULL) {
@@ -460,6 +500,7 @@ cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st) {
   p.tiles = g.plan.tiles;
   p.splits = g.plan.splits;
   p.k_split = g.plan.k_split;
+  p.stages = stream_stages(g.plan.k_split / SBK);
   p.xform = g.xform;
   p.ss_in = g.ss_in;
   p.n_ss = g.n_ss;
