@@ -51,8 +51,8 @@ class VocabLayout(ctypes.Structure):
 
 _lib = None
 _EXPORTS = ["fpd_model_create", "fpd_model_destroy", "fpd_kv_store_bytes", "fpd_workspace_bytes",
-            "fpd_prepare_context", "fpd_draft_block", "fpd_constrain_argmax", "fpd_constrain_argmax_noalloc",
-            "fpd_verify", "fpd_last_error",
+            "fpd_prepare_context", "fpd_prepare_context_rows", "fpd_draft_block", "fpd_constrain_argmax",
+            "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_sd_advance", "fpd_last_error",
             "fpd_kernel_launches", "fpd_device_status"]
 
 
@@ -73,6 +73,9 @@ def lib():
         l.fpd_workspace_bytes.restype = sz
         l.fpd_prepare_context.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp, ctypes.POINTER(vp), vp,
                                           ctypes.c_int, vp, sz, vp]
+        l.fpd_prepare_context_rows.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.POINTER(vp), vp,
+                                               ctypes.c_int, vp, sz, vp]
+        l.fpd_sd_advance.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp]
         l.fpd_draft_block.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, i32, vp, vp, vp,
                                       sz, vp]
         l.fpd_constrain_argmax.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.POINTER(VocabLayout), vp, vp,
@@ -84,8 +87,9 @@ def lib():
         l.fpd_last_error.restype = ctypes.c_char_p
         l.fpd_kernel_launches.restype = ctypes.c_uint64
         l.fpd_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
-        for f in ("fpd_model_create", "fpd_prepare_context", "fpd_draft_block", "fpd_constrain_argmax",
-                  "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_device_status"):
+        for f in ("fpd_model_create", "fpd_prepare_context", "fpd_prepare_context_rows", "fpd_draft_block",
+                  "fpd_constrain_argmax", "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_sd_advance",
+                  "fpd_device_status"):
             getattr(l, f).restype = ctypes.c_int
         _lib = l
     return _lib
@@ -141,6 +145,19 @@ def fpd_prepare_context(model, batch, total_rows, row_off, pos_start, feats, kv_
     arr = (ctypes.c_void_p * len(feats))(*[_ptr(f) for f in feats])
     _check(lib().fpd_prepare_context(model, batch, total_rows, _ptr(row_off), _ptr(pos_start), arr, _ptr(kv_store),
                                      t_cap, _ptr(workspace), workspace_bytes, _stream(stream)), "fpd_prepare_context")
+
+
+def fpd_prepare_context_rows(model, batch, total_rows, row_off, row_cnt, pos_start, feats, kv_store, t_cap, workspace,
+                             workspace_bytes, stream=None):
+    arr = (ctypes.c_void_p * len(feats))(*[_ptr(f) for f in feats])
+    _check(lib().fpd_prepare_context_rows(model, batch, total_rows, _ptr(row_off), _ptr(row_cnt), _ptr(pos_start),
+                                          arr, _ptr(kv_store), t_cap, _ptr(workspace), workspace_bytes,
+                                          _stream(stream)), "fpd_prepare_context_rows")
+
+
+def fpd_sd_advance(batch, block_len, t_cap, accept_len, committed, ctx_len, pos_start, anchor, stream=None):
+    _check(lib().fpd_sd_advance(batch, block_len, t_cap, _ptr(accept_len), _ptr(committed), _ptr(ctx_len),
+                                _ptr(pos_start), _ptr(anchor), _stream(stream)), "fpd_sd_advance")
 
 
 def fpd_draft_block(model, batch, block_len, kv_store, t_cap, ctx_len, anchor, mask_id, hidden_out,

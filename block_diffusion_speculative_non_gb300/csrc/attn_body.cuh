@@ -171,7 +171,7 @@ __device__ __forceinline__ void attn_tile(const AttnArgs& a, bf16* __restrict__ 
   const int b = bg / a.nkv, g = bg % a.nkv;
   const int grp = a.nq / a.nkv, nrows = a.L * grp;
   int T = a.ctx_len[b];
-  T = T < 0 ? 0 : (T > a.t_cap ? a.t_cap : T);
+  T = clamp_ctx(T, a.t_cap);
   const int n_keys = T + a.L;
   const int k_begin = split * a.chunk, k_end = min(n_keys, k_begin + a.chunk);
   const float sl2 = rsqrtf((float)H) * 1.4426950408889634f;   // 1/sqrt(h) * log2(e): softmax in base 2

@@ -326,6 +326,8 @@ fpd_status fpd_model_create(const fpd_model_desc* desc, const fpd_weights* w, fp
   if (d.head_dim != 64 && d.head_dim != 128) return fail(FPD_ERR_UNSUPPORTED, "head_dim %d (64 or 128)", d.head_dim);
   if (d.d_model < 64 || d.d_model % 64 || d.d_ff < 64 || d.d_ff % 64)
     return fail(FPD_ERR_UNSUPPORTED, "d_model %d / d_ff %d must be positive multiples of 64", d.d_model, d.d_ff);
+  if (d.d_model > 16384)   // the row kernels hold one row per CTA of at most 1024 threads x 16 values
+    return fail(FPD_ERR_UNSUPPORTED, "d_model %d exceeds 16384", d.d_model);
   if (d.n_kv_heads < 1 || d.n_q_heads < d.n_kv_heads || d.n_q_heads % d.n_kv_heads)
     return fail(FPD_ERR_UNSUPPORTED, "n_q_heads %d must be a multiple of n_kv_heads %d", d.n_q_heads, d.n_kv_heads);
   if ((d.n_q_heads * d.head_dim) % 64) return fail(FPD_ERR_UNSUPPORTED, "n_q_heads * head_dim must be a multiple of 64");
@@ -413,6 +415,13 @@ size_t fpd_workspace_bytes(const fpd_model* m, int batch, int max_block_len, int
 fpd_status fpd_prepare_context(fpd_model* m, int batch, int total_rows, const int32_t* row_off,
                                const int32_t* pos_start, const void* const* feats, void* kv_store, int t_cap,
                                void* workspace, size_t ws_bytes, void* stream) {
+  return fpd_prepare_context_rows(m, batch, total_rows, row_off, nullptr, pos_start, feats, kv_store, t_cap, workspace,
+                                  ws_bytes, stream);
+}
+
+fpd_status fpd_prepare_context_rows(fpd_model* m, int batch, int total_rows, const int32_t* row_off,
+                                    const int32_t* row_cnt, const int32_t* pos_start, const void* const* feats,
+                                    void* kv_store, int t_cap, void* workspace, size_t ws_bytes, void* stream) {
   if (!m) return fail(FPD_ERR_INVALID_ARG, "model is null");
   const auto& d = m->d;
   if (batch < 1 || total_rows < 0 || t_cap < 1) return fail(FPD_ERR_SHAPE, "batch %d, total_rows %d, t_cap %d", batch, total_rows, t_cap);
@@ -468,7 +477,7 @@ fpd_status fpd_prepare_context(fpd_model* m, int batch, int total_rows, const in
       k.k_split = pk.k_split;
       FPD_CUDA(launch_tc_gemm(k, pk, st), "context K/V GEMM");
       FPD_CUDA(launch_kv_post((bf16*)kv_store, w.part, pk.splits, k.c_split_stride, (const bf16*)m->w.k_norm[l],
-                              m->rope, row_off, pos_start, batch, l, t_cap, r0, R, nkv, h, d.rms_eps, st),
+                              m->rope, row_off, row_cnt, pos_start, batch, l, t_cap, r0, R, nkv, h, d.rms_eps, st),
                "context K/V epilogue");
     }
   }
@@ -801,6 +810,15 @@ fpd_status fpd_verify(int mode, int batch, int L, const int32_t* draft, const in
   FPD_CUDA(launch_verify(mode, batch, L, draft, target, tb, layout ? layout->pos_class : nullptr, rule, pad_id,
                          accept_len, committed, valid_out, (cudaStream_t)stream),
            "verify");
+  return FPD_OK;
+}
+
+fpd_status fpd_sd_advance(int batch, int L, int t_cap, int32_t* accept_len, const int32_t* committed,
+                          int32_t* ctx_len, int32_t* pos_start, int32_t* anchor, void* stream) {
+  if (batch < 1 || L < 2 || t_cap < 1) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d, t_cap %d", batch, L, t_cap);
+  if (!accept_len || !committed || !ctx_len || !pos_start || !anchor) return fail(FPD_ERR_INVALID_ARG, "null pointer argument");
+  FPD_CUDA(launch_sd_advance(batch, L, t_cap, accept_len, committed, ctx_len, pos_start, anchor, (cudaStream_t)stream),
+           "speculative-step advance");
   return FPD_OK;
 }
 

@@ -22,10 +22,21 @@ enum DeviceCheck : int32_t {
   kCheckWaitTimeout = 2,     // an mbarrier / flag wait exceeded its limit
   kCheckNoLegalId = 3,       // a position's class had no legal id (empty argmax)
   kCheckBadClass = 4,        // pos_class outside [0, n_class)
+  kCheckBadContext = 5,      // a ctx_len outside [0, t_cap] (clamped)
+  kCheckBadPosition = 6,     // a context row's position outside [0, t_cap) (row skipped)
+  kCheckCtxOverflow = 7,     // an accepted append would pass t_cap (count capped)
 };
 extern __device__ int32_t g_device_check;
 
 __device__ __forceinline__ void record_check(int32_t code) { atomicCAS(&g_device_check, 0, code); }
+// ctx_len of a request, clamped to [0, t_cap]; a value outside is the caller's contract broken: recorded.
+__device__ __forceinline__ int clamp_ctx(int cl, int t_cap) {
+  if (cl < 0 || cl > t_cap) {
+    record_check(kCheckBadContext);
+    cl = cl < 0 ? 0 : t_cap;
+  }
+  return cl;
+}
 
 // ---- host-side bookkeeping ---------------------------------------------------------------------------------
 extern std::atomic<uint64_t> g_launches;

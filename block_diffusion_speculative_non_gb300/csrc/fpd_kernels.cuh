@@ -92,6 +92,7 @@ struct StreamGemm {
   bf16* hmid;                     // SEPI_SWIGLU output [M][N]
   unsigned long long* slots;      // SEPI_ARGMAX: [grid][16][2]
   float* logits;                  // SEPI_ARGMAX: [M][N] or null
+  uint32_t test_extra_tx = 0;     // test hook only: bytes the first weight stage expects beyond what arrives
 };
 bool stream_shape_ok(const fpd_model_desc& d);
 StreamPlan stream_plan(int tiles, int K, int num_sms, bool split_ok);
@@ -110,8 +111,9 @@ cudaError_t launch_qkv_post(bf16* q, bf16* kblk, bf16* vblk, const float* part, 
                             const bf16* q_norm, const bf16* k_norm, const float2* rope, const int32_t* ctx_len,
                             int t_cap, int B, int L, int nq, int nkv, int h, float eps, cudaStream_t st);
 cudaError_t launch_kv_post(bf16* store, const float* part, int nsplit, size_t split_stride, const bf16* k_norm,
-                           const float2* rope, const int32_t* row_off, const int32_t* pos_start, int batch, int layer,
-                           int t_cap, int row0, int rows, int nkv, int h, float eps, cudaStream_t st);
+                           const float2* rope, const int32_t* row_off, const int32_t* row_cnt, const int32_t* pos_start,
+                           int batch, int layer, int t_cap, int row0, int rows, int nkv, int h, float eps,
+                           cudaStream_t st);
 cudaError_t launch_residual_norm(bf16* x, bf16* xn, const float* part, int nsplit, size_t split_stride, const bf16* g,
                                  int rows, int d, float eps, cudaStream_t st);
 cudaError_t launch_embed_norm(bf16* x, bf16* xn, const bf16* embed, const int32_t* anchor, int32_t mask_id,
@@ -177,5 +179,7 @@ struct VerifyTables {
 cudaError_t launch_verify(int mode, int B, int L, const int32_t* draft, const int32_t* target, const VerifyTables& tb,
                           const int16_t* pos_class, const int8_t* rule, int32_t pad_id, int32_t* accept,
                           int32_t* committed, int32_t* valid, cudaStream_t st);
+cudaError_t launch_sd_advance(int B, int L, int t_cap, int32_t* accept, const int32_t* committed, int32_t* ctx_len,
+                              int32_t* pos_start, int32_t* anchor, cudaStream_t st);
 
 }  // namespace fpd

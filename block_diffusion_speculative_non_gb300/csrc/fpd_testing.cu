@@ -17,6 +17,8 @@ bool attributes_ready() {
     cudaError_t r = tc_init_attributes();
     if (r == cudaSuccess) r = attn_init_attributes();
     if (r == cudaSuccess) r = attn_tc_init_attributes();
+    if (r == cudaSuccess) r = attn_short_init_attributes();
+    if (r == cudaSuccess) r = stream_init_attributes();
     return r;
   }();
   return e == cudaSuccess;
@@ -28,9 +30,72 @@ void attn_test_plan(int impl, int batch, int L, int nq, int nkv, int t_cap, int 
   else
     attn_plan(batch, L, nq, nkv, t_cap, sms, splits, chunk);
 }
+// The "lowbias32" integer hash (C. Wellons, "Prospecting for Hash Functions", 2018): a counter-based source of
+// the synthetic target's pseudo-random ids.
+__device__ __forceinline__ uint32_t lowbias32(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7feb352du;
+  x ^= x >> 15;
+  x *= 0x846ca68bu;
+  x ^= x >> 16;
+  return x;
+}
+
+// target[b][i], i < L: the draft's id for i < g, at i = g (< L - 1) an id != draft (draft + 1 + u mod (V - 1)),
+// past it (and at i = L - 1 when every draft id agrees) u mod V, u = lowbias32(salt * 0x9E3779B9 + b * L + i).
+__global__ void synthetic_target_kernel(int B, int L, int V, const int32_t* __restrict__ draft,
+                                        const int32_t* __restrict__ agree, uint32_t salt, int32_t* __restrict__ target) {
+  const int b = blockIdx.x, i = threadIdx.x;
+  if (i >= L) return;
+  int g = agree[b];
+  g = g < 0 ? 0 : (g > L - 1 ? L - 1 : g);
+  const uint32_t u = lowbias32(salt * 0x9E3779B9u + (uint32_t)(b * L + i));
+  int t;
+  if (i < g) t = draft[(size_t)b * (L - 1) + i];
+  else if (i == g && i < L - 1) t = (int)(((uint32_t)draft[(size_t)b * (L - 1) + i] + 1u + u % (uint32_t)(V - 1)) % (uint32_t)V);
+  else t = (int)(u % (uint32_t)V);
+  target[(size_t)b * L + i] = t;
+}
 }  // namespace
 
 extern "C" {
+
+fpd_status fpd_test_synthetic_target(int batch, int block_len, int vocab, const int32_t* draft, const int32_t* agree,
+                                     uint32_t salt, int32_t* target, void* stream) {
+  if (batch < 1 || block_len < 2 || block_len > 1024 || vocab < 2) return FPD_ERR_SHAPE;
+  if (!draft || !agree || !target) return FPD_ERR_INVALID_ARG;
+  synthetic_target_kernel<<<batch, ((block_len + 31) / 32) * 32, 0, (cudaStream_t)stream>>>(batch, block_len, vocab,
+                                                                                           draft, agree, salt, target);
+  return cudaGetLastError() == cudaSuccess ? FPD_OK : FPD_ERR_CUDA;
+}
+
+size_t fpd_test_stream_timeout_workspace_bytes(void) { return 64 * 1024; }
+
+fpd_status fpd_test_stream_timeout(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < fpd_test_stream_timeout_workspace_bytes()) return FPD_ERR_CAPACITY;
+  const int sms = current_sms();
+  if (!sms || !attributes_ready()) return FPD_ERR_CUDA;
+  char* base = (char*)workspace;
+  StreamGemm g{};
+  g.epi = SEPI_RESID;
+  g.M = 16;
+  g.N = 128;
+  g.K = 64;
+  g.plan = stream_plan(1, g.K, sms, false);
+  g.w = (const bf16*)base;                         // 128 x 64 weights: 16 KB
+  g.x = (const bf16*)(base + 16384);               // 16 x 64 activations: 2 KB
+  g.ldx = g.K;
+  g.xform = XF_COPY;
+  g.xres = (bf16*)(base + 20480);                  // 16 x 128 residual: 4 KB
+  g.ss_out = (float*)(base + 24576);               // 1 x 16
+  g.part = (float*)(base + 32768);
+  g.counters = (int*)(base + 28672);
+  g.test_extra_tx = 16;                            // the first weight stage waits for 16 bytes that never come
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, fpd_test_stream_timeout_workspace_bytes(), st) != cudaSuccess) return FPD_ERR_CUDA;
+  return launch_stream_gemm(g, st) == cudaSuccess ? FPD_OK : FPD_ERR_CUDA;
+}
+
 
 size_t fpd_test_gemm_workspace_bytes(int M, int N, int K) {
   if (M < 1 || N < 1 || K < 64) return 0;
@@ -93,9 +158,10 @@ size_t fpd_test_attention_workspace_bytes(int impl, int batch, int L, int nq, in
 fpd_status fpd_test_attention(int impl, int batch, int L, int nq, int nkv, int head_dim, int t_cap, int layer,
                               const int32_t* ctx_len, const void* q, const void* kblk, const void* vblk,
                               const void* store, void* out, void* workspace, size_t workspace_bytes, void* stream) {
-  if (impl < 0 || impl > 1 || batch < 1 || L < 1 || nkv < 1 || nq % nkv || t_cap < 1 || layer < 0) return FPD_ERR_SHAPE;
+  if (impl < 0 || impl > 2 || batch < 1 || L < 1 || nkv < 1 || nq % nkv || t_cap < 1 || layer < 0) return FPD_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128) return FPD_ERR_UNSUPPORTED;
   if (impl == 1 && !attn_tc_supported(head_dim, L, nq, nkv)) return FPD_ERR_UNSUPPORTED;
+  if (impl == 2 && !attn_short_supported(head_dim, L, nq, nkv)) return FPD_ERR_UNSUPPORTED;
   if (!ctx_len || !q || !kblk || !vblk || !store || !out || !workspace) return FPD_ERR_INVALID_ARG;
   const int sms = current_sms();
   if (!sms || !attributes_ready()) return FPD_ERR_CUDA;
@@ -120,7 +186,9 @@ fpd_status fpd_test_attention(int impl, int batch, int L, int nq, int nkv, int h
   a.o_part = (float*)workspace;
   a.ml = (float2*)((char*)workspace + align_up((size_t)a.splits * rows * nq * head_dim * sizeof(float), 256));
   cudaStream_t st = (cudaStream_t)stream;
-  const cudaError_t e = impl == 1 ? launch_attention_tc(a, (bf16*)out, st) : launch_attention(a, (bf16*)out, st);
+  const cudaError_t e = impl == 2   ? launch_attention_short(a, (bf16*)out, st)
+                        : impl == 1 ? launch_attention_tc(a, (bf16*)out, st)
+                                    : launch_attention(a, (bf16*)out, st);
   return e == cudaSuccess ? FPD_OK : FPD_ERR_CUDA;
 }
 

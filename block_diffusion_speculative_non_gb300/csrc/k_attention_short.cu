@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(NWARP * 32) attn_short_kernel(const __grid_con
   pdl_trigger();
 
   int T = a.ctx_len[b];
-  T = T < 0 ? 0 : (T > a.t_cap ? a.t_cap : T);
+  T = clamp_ctx(T, a.t_cap);
   const int n_keys = T + a.L;
   const int nt = ceil_div(n_keys, KT), tpc = ceil_div(nt, C);
   const int t0 = min(nt, rank * tpc), t1 = min(nt, t0 + tpc), nts = t1 - t0;

@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
   pdl_wait();   // q, block K/V and the context store come from earlier kernels
 
   int T = p.ctx_len[b];
-  T = T < 0 ? 0 : (T > p.t_cap ? p.t_cap : T);
+  T = clamp_ctx(T, p.t_cap);
   const int n_keys = T + p.L;
   TileList tl;
   tl.init(T, min(n_keys, split * p.chunk), min(n_keys, (split + 1) * p.chunk));

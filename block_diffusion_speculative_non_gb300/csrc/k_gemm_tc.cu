@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const bool mok = m < p.M;
         const int b = mok ? m / p.L : 0, j = mok ? m % p.L : 0;
         int cl = mok ? p.ctx_len[b] : 0;
-        cl = cl < 0 ? 0 : (cl > p.t_cap ? p.t_cap : cl);
+        cl = clamp_ctx(cl, p.t_cap);
         const int hh = p.hd / 2;
         const float2* rope_row = p.rope + (size_t)(cl + j) * hh;
 #pragma unroll 1

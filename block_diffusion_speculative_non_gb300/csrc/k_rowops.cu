@@ -81,7 +81,7 @@ __global__ void qkv_post_kernel(bf16* __restrict__ q_out, bf16* __restrict__ kbl
       for (int k = 0; k < NV; k++) v[k] += t[u][k];
   }
   int cl = ctx_len[b];
-  cl = cl < 0 ? 0 : (cl > t_cap ? t_cap : cl);
+  cl = clamp_ctx(cl, t_cap);
   const float2* rope_row = rope + (size_t)(cl + j) * (H / 2);
   bf16* dst;
   if (hd < nq) {
@@ -114,8 +114,9 @@ cudaError_t launch_qkv_post(bf16* q, bf16* kblk, bf16* vblk, const float* part, 
 template <int H>
 __global__ void kv_post_kernel(bf16* __restrict__ store, const float* __restrict__ part, int nsplit,
                                size_t split_stride, const bf16* __restrict__ k_norm, const float2* __restrict__ rope,
-                               const int32_t* __restrict__ row_off, const int32_t* __restrict__ pos_start, int batch,
-                               int layer, int t_cap, int row0, int nkv, float eps) {
+                               const int32_t* __restrict__ row_off, const int32_t* __restrict__ row_cnt,
+                               const int32_t* __restrict__ pos_start, int batch, int layer, int t_cap, int row0, int nkv,
+                               float eps) {
   pdl_trigger();
   pdl_wait();
   constexpr int NV = H / 32;
@@ -127,8 +128,12 @@ __global__ void kv_post_kernel(bf16* __restrict__ store, const float* __restrict
     if (row_off[mid] <= grow) lo = mid; else hi = mid;
   }
   const int b = lo;
+  if (grow >= row_off[batch] || (row_cnt && grow - row_off[b] >= row_cnt[b])) return;   // rows past the count
   const int pos = (pos_start ? pos_start[b] : 0) + grow - row_off[b];
-  if (pos < 0 || pos >= t_cap) return;          // caller contract violated: skip the store
+  if (pos < 0 || pos >= t_cap) {                // caller contract violated: skip the store, record it
+    if (lane == 0 && hd == 0) record_check(kCheckBadPosition);
+    return;
+  }
   const int ncol = 2 * nkv * H;
   float v[NV];
 #pragma unroll
@@ -145,15 +150,16 @@ __global__ void kv_post_kernel(bf16* __restrict__ store, const float* __restrict
 }
 
 cudaError_t launch_kv_post(bf16* store, const float* part, int nsplit, size_t split_stride, const bf16* k_norm,
-                           const float2* rope, const int32_t* row_off, const int32_t* pos_start, int batch, int layer,
-                           int t_cap, int row0, int rows, int nkv, int h, float eps, cudaStream_t st) {
+                           const float2* rope, const int32_t* row_off, const int32_t* row_cnt, const int32_t* pos_start,
+                           int batch, int layer, int t_cap, int row0, int rows, int nkv, int h, float eps,
+                           cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   dim3 grid(rows, 2 * nkv);
   if (h == 128)
     return launch_k(kv_post_kernel<128>, grid, 32, 0, st, store, part, nsplit, split_stride, k_norm, rope, row_off,
-                    pos_start, batch, layer, t_cap, row0, nkv, eps);
+                    row_cnt, pos_start, batch, layer, t_cap, row0, nkv, eps);
   return launch_k(kv_post_kernel<64>, grid, 32, 0, st, store, part, nsplit, split_stride, k_norm, rope, row_off,
-                  pos_start, batch, layer, t_cap, row0, nkv, eps);
+                  row_cnt, pos_start, batch, layer, t_cap, row0, nkv, eps);
 }
 
 // ---- residual add fused with the next RMSNorm: one block per row ------------------------------------------------

@@ -77,6 +77,7 @@ struct StreamParams {
   unsigned long long* slots;   // [gridDim][16][2]
   float* logits;               // [M][N] or null
   int stages;                  // weight ring depth, kMinStages..kMaxStages
+  uint32_t test_extra_tx;      // 0; a test makes the first stage's wait run out with it (bounded-wait check)
 };
 
 template <int EPI>
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       if (t < total) item(t, tile, split, k0, nkb);
       auto issue_w = [&]() {
         const uint32_t fb = full0 + 8 * stage, dst = tc::smem_u32(ring + stage * W_ATOM);
-        tc::mbar_arrive_expect_tx(fb, W_ATOM);
+        tc::mbar_arrive_expect_tx(fb, W_ATOM + (issued == 0 ? p.test_extra_tx : 0u));
         if (EPI == SEPI_SWIGLU) {   // atom = [gate rows f0..f0+63 ; up rows F+f0..F+f0+63]
           tc::tma_load_2d(dst, &p.tm_w, k0 + kb * SBK, tile * 64, fb);
           tc::tma_load_2d(dst + W_ATOM / 2, &p.tm_w, k0 + kb * SBK, p.N + tile * 64, fb);
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
     if (p.xform == XF_NORM) inv_from_partials(p.ss_in, p.n_ss, p.K, p.eps, scratch, s_inv, et);
     if (EPI == SEPI_QKV && et < SBN) {
       int cl = et * p.L < p.M ? p.ctx_len[et] : 0;
-      s_ctx[et] = cl < 0 ? 0 : (cl > p.t_cap ? p.t_cap : cl);
+      s_ctx[et] = clamp_ctx(cl, p.t_cap);
     }
     if (EPI == SEPI_ARGMAX && et < SBN) s_run[2 * et] = s_run[2 * et + 1] = 0ull;
     if (blockIdx.x < total && p.xform != XF_COPY) {
@@ -501,6 +502,7 @@ cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st) {
   p.splits = g.plan.splits;
   p.k_split = g.plan.k_split;
   p.stages = stream_stages(g.plan.k_split / SBK);
+  p.test_extra_tx = g.test_extra_tx;
   p.xform = g.xform;
   p.ss_in = g.ss_in;
   p.n_ss = g.n_ss;

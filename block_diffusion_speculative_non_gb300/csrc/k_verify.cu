@@ -84,4 +84,34 @@ cudaError_t launch_verify(int mode, int B, int L, const int32_t* draft, const in
                   accept, committed, valid);
 }
 
+// ---- the step between a text verification and the next block (one thread per request) ------------------------
+// VFlash blog, "Method": blocks follow one another; FlashDrive §3.2: the target's features at the accepted
+// positions extend the context.  The anchor and the n accepted drafts (accept = n + 1 rows) join the context at
+// ctx_len, and the last committed token (the target's token at the first mismatch) anchors the next block.
+__global__ void sd_advance_kernel(int B, int L, int t_cap, int32_t* __restrict__ accept,
+                                  const int32_t* __restrict__ committed, int32_t* __restrict__ ctx_len,
+                                  int32_t* __restrict__ pos_start, int32_t* __restrict__ anchor) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int cl = clamp_ctx(ctx_len[b], t_cap);
+  int a = accept[b];
+  a = a < 0 ? 0 : (a > L ? L : a);
+  if (cl + a > t_cap) {
+    record_check(kCheckCtxOverflow);
+    a = t_cap - cl;
+  }
+  pos_start[b] = cl;
+  ctx_len[b] = cl + a;
+  accept[b] = a;
+  if (a > 0) anchor[b] = committed[(size_t)b * L + a - 1];
+}
+
+cudaError_t launch_sd_advance(int B, int L, int t_cap, int32_t* accept, const int32_t* committed, int32_t* ctx_len,
+                              int32_t* pos_start, int32_t* anchor, cudaStream_t st) {
+  return launch_k(sd_advance_kernel, ceil_div(B, 128), 128, 0, st, B, L, t_cap, accept, committed, ctx_len, pos_start,
+                  anchor);
+}
+
 }  // namespace fpd

@@ -10,7 +10,7 @@ import torch
 
 from . import (FPD_VERIFY_SCHEMA, FPD_VERIFY_TEXT, MAX_LAYERS, ModelDesc, Weights, fpd_constrain_argmax,
                fpd_draft_block, fpd_kv_store_bytes, fpd_model_create, fpd_model_destroy, fpd_prepare_context,
-               fpd_verify, fpd_workspace_bytes, make_layout)
+               fpd_prepare_context_rows, fpd_sd_advance, fpd_verify, fpd_workspace_bytes, make_layout)
 
 _LAYER_KEYS = ("attn_norm", "wqkv", "q_norm", "k_norm", "wo", "mlp_norm", "w_gate_up", "w_down")
 
@@ -93,6 +93,30 @@ class Drafter:
                              self.ws_bytes, stream, margin_out=margin_out)
         return tokens_out
 
+    def prepare_rows(self, batch, total_rows, row_off_d, row_cnt_d, pos_start_d, feats_d, stream=None):
+        """fpd_prepare_context_rows on device arrays (appends whose row counts live on the device)."""
+        fpd_prepare_context_rows(self.handle, batch, total_rows, row_off_d, row_cnt_d, pos_start_d, feats_d,
+                                 self.kv_store, self.t_cap, self.workspace, self.ws_bytes, stream)
+
+    def spec_state(self, batch, block_len, ctx_len, anchor):
+        """Device buffers of a text speculative loop (see spec_step), starting from ctx_len / anchor."""
+        return SpecState(self, batch, block_len, ctx_len, anchor)
+
+    def spec_step(self, st, feats_d, make_target, mask_id, stream=None, logits_out=None):
+        """One text speculative step on the device, with no host synchronisation (capturable in a CUDA graph):
+        draft block -> unconstrained argmax -> make_target(st.tokens, st.target) (the target model's greedy row for
+        the drafted block; the caller supplies it) -> text verification -> fpd_sd_advance -> append of the target's
+        features at the accepted positions.  feats_d: n_feat device tensors [batch * block_len, d]; row
+        b * block_len + j holds request b's feature at block position j (anchor j = 0)."""
+        B, L = st.batch, st.block_len
+        self.draft_block(B, L, st.ctx_len, st.anchor, mask_id, hidden_out=st.hidden, stream=stream)
+        self.constrain_argmax(B, L, st.hidden, tokens_out=st.tokens, logits_out=logits_out, stream=stream)
+        make_target(st.tokens, st.target)
+        fpd_verify(0, B, L, st.tokens, st.target, None, None, -1, st.accept, st.committed, st.valid, stream)
+        st.after_verify(stream)
+        fpd_sd_advance(B, L, self.t_cap, st.accept, st.committed, st.ctx_len, st.pos_start, st.anchor, stream)
+        self.prepare_rows(B, B * L, st.row_off, st.accept, st.pos_start, feats_d, stream)
+
     @staticmethod
     def layout(layout_np: dict, batch: int, block_len: int, device="cuda"):
         """Device copy of a layout dict (class tables stay on the host)."""
@@ -127,3 +151,28 @@ class Drafter:
         fpd_verify(FPD_VERIFY_SCHEMA, batch, block_len, draft, None, layout, rule, pad_id, accept, committed, valid,
                    stream)
         return accept, committed, valid
+
+
+class SpecState:
+    """Device state of a text speculative loop: context lengths, anchors, the step's outputs, and the fixed
+    row offsets (block_len rows per request) of the feature buffer an append reads."""
+
+    def __init__(self, dr, batch, block_len, ctx_len, anchor):
+        dev = dr.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.batch, self.block_len = batch, block_len
+        self.ctx_len = torch.as_tensor(np.asarray(ctx_len, np.int32), **i32).clone()
+        self.anchor = torch.as_tensor(np.asarray(anchor, np.int32), **i32).clone()
+        self.pos_start = torch.zeros(batch, **i32)
+        self.accept = torch.zeros(batch, **i32)
+        self.committed = torch.zeros(batch, block_len, **i32)
+        self.valid = torch.zeros(batch, **i32)
+        self.tokens = torch.zeros(batch, block_len - 1, **i32)
+        self.target = torch.zeros(batch, block_len, **i32)
+        self.hidden = torch.empty(batch * block_len, dr.shape.d_model, dtype=torch.bfloat16, device=dev)
+        self.row_off = torch.arange(0, (batch + 1) * block_len, block_len, **i32)
+        self.hooks = []
+
+    def after_verify(self, stream=None):
+        for h in self.hooks:   # callers record per-step results here (e.g. copies into a history buffer)
+            h(self)

@@ -56,6 +56,18 @@ typedef enum {
   FPD_ERR_DEVICE_CHECK = 6   /* a kernel reported a failed device-side check (see fpd_device_status) */
 } fpd_status;
 
+/* Codes of the device-side check word (fpd_device_status): the first failure a kernel recorded.  Kernels never
+ * trap; they record the code and skip or clamp the offending access. */
+enum {
+  FPD_CHECK_BAD_TOKEN = 1,      /* an id outside [0, V) reached the embedding gather (row zeroed) */
+  FPD_CHECK_WAIT_TIMEOUT = 2,   /* an mbarrier / flag wait exceeded its 1 s limit (the kernel abandoned its loop) */
+  FPD_CHECK_NO_LEGAL_ID = 3,    /* a position's vocabulary class admits no id (token -1) */
+  FPD_CHECK_BAD_CLASS = 4,      /* a pos_class entry outside [0, n_class) */
+  FPD_CHECK_BAD_CONTEXT = 5,    /* a ctx_len outside [0, t_cap] (clamped) */
+  FPD_CHECK_BAD_POSITION = 6,   /* a context row's position pos_start[b] + i outside [0, t_cap) (row skipped) */
+  FPD_CHECK_CTX_OVERFLOW = 7    /* fpd_sd_advance: ctx_len + accepted rows would pass t_cap (rows capped) */
+};
+
 /* Drafter shape.  The layer form is a pre-norm transformer layer with per-head q/k RMSNorm, rotate-half
  * RoPE, grouped-query attention without any mask (bidirectional over context + block) and a SwiGLU MLP;
  * an untied LM head follows a final RMSNorm.  Supported: head_dim in {64, 128}; d_model, d_ff multiples of
@@ -151,11 +163,22 @@ fpd_status fpd_prepare_context(fpd_model* model, int batch, int total_rows, cons
                                const int32_t* pos_start, const void* const* feats, void* kv_store,
                                int t_cap, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same with per-request row counts, for appends whose sizes are known only on the device (the accepted
+ * counts of a speculative step, e.g. in a captured CUDA graph).  Rows [row_off[b], row_off[b] + row_cnt[b]) of
+ * request b are written at positions pos_start[b] + i; rows past row_cnt[b] inside [row_off[b], row_off[b+1])
+ * and rows past row_off[batch] are read but not written.  Here row_off[batch] <= total_rows (total_rows sizes
+ * the launch) and row_cnt[b] <= row_off[b+1] - row_off[b].
+ *   row_cnt    device [batch] int32, or NULL for row_off[b+1] - row_off[b] */
+fpd_status fpd_prepare_context_rows(fpd_model* model, int batch, int total_rows, const int32_t* row_off,
+                                    const int32_t* row_cnt, const int32_t* pos_start, const void* const* feats,
+                                    void* kv_store, int t_cap, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- a3..a7: one bidirectional drafter pass over a block --------------------------------------------------
  * Block of request b: position 0 holds anchor[b], positions 1..L-1 hold mask_id (VFlash (zh) §2.2).
  * Block position j sits at RoPE position ctx_len[b] + j.  Every layer attends, without a mask, over the
  * request's ctx_len[b] context keys/values of that layer followed by the L block keys/values.
- *   ctx_len       device [batch], 0 <= ctx_len[b] <= t_cap (caller guarantees; kernels clamp)
+ *   ctx_len       device [batch], 0 <= ctx_len[b] <= t_cap (caller guarantees; kernels clamp and record
+ *                 FPD_CHECK_BAD_CONTEXT)
  *   anchor        device [batch] token ids in [0, V)
  *   hidden_out    device [batch * L, d] bf16: residual stream after the last layer (before final norm)
  *   layer_hidden  device [n_layers, batch * L, d] bf16 or NULL: residual stream after every layer */
@@ -212,6 +235,24 @@ fpd_status fpd_constrain_argmax_noalloc(fpd_model* model, int batch, int block_l
 fpd_status fpd_verify(int mode, int batch, int block_len, const int32_t* draft, const int32_t* target,
                       const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id,
                       int32_t* accept_len, int32_t* committed, int32_t* valid_out, void* stream);
+
+/* ---- multi-block speculative loop: the step between verification and the next block ----------------------
+ * VFlash blog, "Method" (blocks are drafted and verified one after another until the sequence ends);
+ * FlashDrive §3.2 (the target's features at the accepted positions extend the drafter's context).  After a
+ * text verification of the block [anchor, d_1..d_{L-1}] at positions ctx_len[b] .. ctx_len[b] + L - 1 with
+ * accept_len[b] = n + 1 committed tokens (d_1..d_n and the target's token at the first mismatch):
+ *   pos_start[b] = ctx_len[b]                     where the target's features of the anchor and the n accepted
+ *                                                 draft positions (accept_len[b] rows) are appended
+ *   ctx_len[b]  += accept_len[b]                  the next block's context
+ *   anchor[b]    = committed[b][accept_len[b] - 1]  the next block's anchor: the last committed token
+ * accept_len[b] itself is the row count of that append (fpd_prepare_context_rows row_cnt).  One kernel; no host
+ * synchronisation, so a draft -> argmax -> verify -> advance -> append sequence can be captured in a graph.
+ * When ctx_len[b] + accept_len[b] would exceed t_cap the count is capped (accept_len[b] is lowered in place),
+ * FPD_CHECK_CTX_OVERFLOW is recorded and the anchor is the last committed token that still fits.
+ *   accept_len  device [batch] int32 (in/out), committed device [batch, L] int32
+ *   ctx_len     device [batch] int32 (in/out), pos_start, anchor device [batch] int32 (out) */
+fpd_status fpd_sd_advance(int batch, int block_len, int t_cap, int32_t* accept_len, const int32_t* committed,
+                          int32_t* ctx_len, int32_t* pos_start, int32_t* anchor, void* stream);
 
 /* ---- diagnostics ---------------------------------------------------------------------------------------- */
 const char* fpd_last_error(void);          /* thread-local message of the last failing call */

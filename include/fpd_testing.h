@@ -28,12 +28,32 @@ fpd_status fpd_test_swiglu(int M, int F, int K, const void* X, const void* W, vo
  * softmax(q . [K_ctx ; K_blk]^T / sqrt(h)) [V_ctx ; V_blk] per request and q head (kv head = q head / group), with
  * q [batch * L, nq, h], k_blk / v_blk [batch, nkv, L, h], the context of layer `layer` in store
  * ([n_layers >= layer + 1][batch][K|V][nkv][t_cap][h]) and ctx_len [batch] (all device).  impl 0: the mma.sync
- * kernel (64-row tiles); impl 1: the tcgen05 kernel (128-row tiles, head_dim 128 and L * group >= 128 only).
+ * kernel (64-row tiles); impl 1: the tcgen05 kernel (128-row tiles, head_dim 128 and L * group >= 128 only);
+ * impl 2: the few-token cluster kernel (L * group <= 64; needs no workspace).
  * workspace: fpd_test_attention_workspace_bytes bytes.  Asynchronous on stream. */
 fpd_status fpd_test_attention(int impl, int batch, int L, int nq, int nkv, int head_dim, int t_cap, int layer,
                               const int32_t* ctx_len, const void* q, const void* kblk, const void* vblk,
                               const void* store, void* out, void* workspace, size_t workspace_bytes, void* stream);
 size_t fpd_test_attention_workspace_bytes(int impl, int batch, int L, int nq, int nkv, int head_dim, int t_cap);
+
+/* The synthetic target row of a text speculative step (a stand-in for the target model's greedy ids, which the
+ * pages' workloads would supply): target [batch, block_len] int32 from draft [batch, block_len - 1] and agree
+ * [batch] (g, the number of leading positions on which the target agrees with the draft):
+ *   target[b][i] = draft[b][i]                          for i < g
+ *   target[b][g] = (draft[b][g] + 1 + u mod (V - 1)) mod V   when g < block_len - 1 (never the draft's id)
+ *   target[b][i] = u mod V                              otherwise (past g, and the bonus position when g = L - 1)
+ * with u = lowbias32(salt * 0x9E3779B9 + b * block_len + i) (C. Wellons' "lowbias32" integer hash, uint32
+ * arithmetic).  Asynchronous on stream. */
+fpd_status fpd_test_synthetic_target(int batch, int block_len, int vocab, const int32_t* draft, const int32_t* agree,
+                                     uint32_t salt, int32_t* target, void* stream);
+
+/* Failure detection without a fault: runs one 16 x 128 x 64 weight-streaming GEMM whose first weight stage is
+ * declared 16 bytes larger than its copy, so the MMA warp's bounded mbarrier wait runs out after 1 s.  The kernel
+ * records FPD_CHECK_WAIT_TIMEOUT, abandons its loops and returns normally (its TMEM freed); fpd_device_status then
+ * reports the code and the context stays usable.  workspace: fpd_test_stream_timeout_workspace_bytes() bytes of
+ * device memory (zeroed by the call).  Asynchronous on stream. */
+fpd_status fpd_test_stream_timeout(void* workspace, size_t workspace_bytes, void* stream);
+size_t fpd_test_stream_timeout_workspace_bytes(void);
 
 #ifdef __cplusplus
 }

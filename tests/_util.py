@@ -123,3 +123,33 @@ def assert_margin(gpu_margin, gpu_logits, ref_margin, ref_logits, what="margin",
             continue
         scale = np.max(np.abs(ref_logits[r, ids])) if len(ids) >= few else block_scale
         assert abs(float(gpu_margin[r]) - ref_margin[r]) <= 2 * REL_TOL * scale, (what, r, gpu_margin[r], ref_margin[r])
+
+
+def lowbias32(x: np.ndarray) -> np.ndarray:
+    """C. Wellons' "lowbias32" integer hash on uint32 arrays (wrapping arithmetic)."""
+    x = np.asarray(x, dtype=np.uint32).copy()
+    with np.errstate(over="ignore"):
+        x ^= x >> np.uint32(16)
+        x *= np.uint32(0x7feb352d)
+        x ^= x >> np.uint32(15)
+        x *= np.uint32(0x846ca68b)
+        x ^= x >> np.uint32(16)
+    return x
+
+
+def synthetic_target(draft: np.ndarray, agree: np.ndarray, salt: int, vocab: int) -> np.ndarray:
+    """The target row of a text speculative step, as fpd_test_synthetic_target defines it: the draft's ids before
+    position g = agree[b], a different id at g (when g < L - 1), hash ids after it (and at the bonus position)."""
+    draft = np.asarray(draft, np.int64)
+    B, P = draft.shape
+    L = P + 1
+    idx = np.arange(B, dtype=np.uint64)[:, None] * L + np.arange(L, dtype=np.uint64)[None, :]
+    key = ((np.uint64(salt) * np.uint64(0x9E3779B9)) + idx) & np.uint64(0xFFFFFFFF)
+    u = lowbias32(key.astype(np.uint32)).astype(np.int64)
+    out = u % vocab
+    for b in range(B):
+        g = int(min(max(int(agree[b]), 0), L - 1))
+        out[b, :g] = draft[b, :g]
+        if g < L - 1:
+            out[b, g] = (draft[b, g] + 1 + u[b, g] % (vocab - 1)) % vocab
+    return out.astype(np.int32)

@@ -18,3 +18,10 @@ def oracle_lib():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def full_weights():
+    """The 4B-shape drafter's synthetic weights (seed 2000), drawn once per session (tens of seconds)."""
+    import synth
+    return synth.make_weights(synth.FULL, 2000)

@@ -55,7 +55,7 @@ def _weights(fpd, null=None):
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=96), 4), (dict(n_layers=0), 4), (dict(n_layers=9), 4), (dict(d_model=500), 4),
     (dict(n_q_heads=6, n_kv_heads=4), 4), (dict(n_feat=0), 4), (dict(vocab=1), 2), (dict(max_pos=1), 2),
-    (dict(rms_eps=0.0), 2),
+    (dict(rms_eps=0.0), 2), (dict(d_model=16448, d_ff=64), 4),
 ])
 def test_model_create_rejects_bad_shapes(fpd, kw, status):
     h = ctypes.c_void_p()
@@ -135,3 +135,15 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pkg, "_lib", None)
     with pytest.raises(RuntimeError):
         pkg.lib()
+
+
+def test_speculative_step_calls_reject_bad_arguments(fpd):
+    """fpd_sd_advance and fpd_prepare_context_rows validate on the host before launching anything."""
+    lib = fpd.lib()
+    a = 1 << 20
+    assert lib.fpd_sd_advance(0, 16, 64, a, a, a, a, a, None) == 2
+    assert lib.fpd_sd_advance(1, 1, 64, a, a, a, a, a, None) == 2
+    assert lib.fpd_sd_advance(1, 16, 64, None, a, a, a, a, None) == 1
+    assert lib.fpd_sd_advance(1, 16, 64, a, a, a, None, a, None) == 1
+    feats = (ctypes.c_void_p * 1)(a)
+    assert lib.fpd_prepare_context_rows(None, 1, 4, a, a, None, feats, a, 64, a, 1 << 20, None) == 1

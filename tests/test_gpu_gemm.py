@@ -136,8 +136,9 @@ def run_attention(lib, impl, B, L, nq, nkv, h, t_cap, ctx, seed):
 @pytest.mark.parametrize("B,L,nq,nkv,h,t_cap,ctx", ATTN_CASES)
 def test_attention_kernels_agree_with_fp32(lib, B, L, nq, nkv, h, t_cap, ctx):
     """Both attention kernels against a plain fp32 softmax attention of the same bf16 inputs.  Each stores bf16
-    (half an ulp: 2e-3 of the row's largest value) after a second product on fp16 P, so the row error stays
-    within a few bf16 rounding steps; the tcgen05 kernel must be as accurate as the mma.sync one."""
+    (half an ulp: 2e-3 of the row's largest value) after a second product on P split into bf16 hi + lo terms, so
+    the row error stays within a few bf16 rounding steps; the tcgen05 kernel must be as accurate as the mma.sync
+    one."""
     errs = [run_attention(lib, impl, B, L, nq, nkv, h, t_cap, ctx, seed=B * 1000 + L) for impl in (0, 1)]
     print(f"attention row error: mma.sync {errs[0]:.3e}, tcgen05 {errs[1]:.3e}")
     assert errs[0] < 6e-3 and errs[1] < 6e-3, errs
@@ -147,6 +148,29 @@ def test_attention_kernels_agree_with_fp32(lib, B, L, nq, nkv, h, t_cap, ctx):
 @pytest.mark.parametrize("B,L,nq,nkv,h,t_cap,ctx", [(1, 16, 32, 8, 128, 2048, [2048]), (2, 33, 8, 2, 64, 96, [96, 5])])
 def test_attention_mma_sync_small_blocks(lib, B, L, nq, nkv, h, t_cap, ctx):
     assert run_attention(lib, 0, B, L, nq, nkv, h, t_cap, ctx, seed=7) < 6e-3
+
+
+SHORT_CASES = [
+    # few-token blocks: at most 64 query rows per (request, kv head)
+    (1, 16, 32, 8, 128, 2048, [2048]),       # the batch-1 text workload
+    (1, 16, 32, 8, 128, 16384, [16384]),     # the longest context of the sweep
+    (1, 16, 32, 8, 128, 300, [0]),           # no context: block keys only
+    (1, 2, 32, 8, 128, 130, [1]),            # two positions, one context key
+    (2, 5, 8, 2, 64, 96, [96, 5]),           # tiny drafter shape, ragged
+]
+
+
+@pytest.mark.parametrize("B,L,nq,nkv,h,t_cap,ctx", SHORT_CASES)
+def test_attention_short_cluster_kernel(lib, B, L, nq, nkv, h, t_cap, ctx):
+    """The few-token cluster kernel against fp32, as accurate as the mma.sync tiles (same per-tile math)."""
+    errs = [run_attention(lib, impl, B, L, nq, nkv, h, t_cap, ctx, seed=B * 100 + L) for impl in (0, 2)]
+    print(f"short attention row error: mma.sync {errs[0]:.3e}, cluster {errs[1]:.3e}")
+    assert errs[1] < 6e-3 and errs[1] < 1.5 * errs[0] + 1e-3, errs
+
+
+@pytest.mark.parametrize("B,L,nq,nkv,h,t_cap,ctx", SHORT_CASES)
+def test_attention_short_covers_every_key_once(lib, B, L, nq, nkv, h, t_cap, ctx):
+    test_attention_covers_every_key_once(lib, 2, B, L, nq, nkv, h, t_cap, ctx)
 
 
 @pytest.mark.parametrize("impl", [0, 1])

@@ -58,7 +58,8 @@ def _compare_store(dr, kv_ref, ctx_len, batch):
 
 def _draft_and_compare(pkg, orc, dr, om, kv_ref, t_cap, ctx_len, anchor, mask_id, L, batch, layout=None,
                        requests=None):
-    """GPU draft + argmax over the whole batch; oracle on `requests` (default all); returns gpu tokens."""
+    """GPU draft + argmax over the whole batch; oracle on `requests` (default all); returns gpu tokens.  kv_ref is
+    the oracle's store [layer][b][...] or a function b -> that request's store [layer][1][...]."""
     s = dr.shape
     lh = torch.empty(s.n_layers, batch * L, s.d_model, dtype=torch.bfloat16, device=DEV)
     hid = dr.draft_block(batch, L, dev_i32(ctx_len), dev_i32(anchor), mask_id, layer_hidden=lh)
@@ -69,23 +70,24 @@ def _draft_and_compare(pkg, orc, dr, om, kv_ref, t_cap, ctx_len, anchor, mask_id
     toks = dr.constrain_argmax(batch, L, hid, layout=lay_d, logits_out=logits)
     torch.cuda.synchronize()
     assert pkg.fpd_device_status() == 0
-    g_hid, g_lh, g_tok, g_log = bits_of(hid), bits_of(lh), toks.cpu().numpy(), logits.cpu().numpy()
+    g_tok = toks.cpu().numpy()
     reqs = range(batch) if requests is None else requests
     for b in reqs:
         sl = slice(b * L, (b + 1) * L)
-        kv_b = kv_ref[:, b:b + 1] if kv_ref.shape[1] > 1 else kv_ref
+        g_hid_b, g_lh_b = bits_of(hid[sl]), bits_of(lh[:, sl])   # only the checked requests leave the GPU
+        kv_b = kv_ref(b) if callable(kv_ref) else (kv_ref[:, b:b + 1] if kv_ref.shape[1] > 1 else kv_ref)
         o_hid, o_lh = orc.draft_block(om, kv_b, t_cap, ctx_len[b:b + 1], anchor[b:b + 1], mask_id, L,
                                       want_layers=True)
         for l in range(s.n_layers):
-            assert_rows_close(g_lh[l, sl], o_lh[l], f"request {b} layer {l} hidden")
-        assert_rows_close(g_hid[sl], o_hid, f"request {b} hidden")
+            assert_rows_close(g_lh_b[l], o_lh[l], f"request {b} layer {l} hidden")
+        assert_rows_close(g_hid_b, o_hid, f"request {b} hidden")
         lay_b = None
         if layout is not None:
             lay_b = dict(layout)
             pc = np.asarray(layout["pos_class"])
             lay_b["pos_class"] = pc if pc.ndim == 1 else pc[b]
         o_tok, o_margin, o_log = orc.constrain_argmax(om, o_hid, 1, L, layout=lay_b, want_logits=True)
-        g_log_b = g_log[b * (L - 1):(b + 1) * (L - 1)]
+        g_log_b = logits[b * (L - 1):(b + 1) * (L - 1)].cpu().numpy()
         assert_logits(g_log_b, o_log, f"request {b} logits")
         assert_tokens_chain(g_tok[b], o_tok[0], o_margin, g_log_b, o_log, f"request {b} tokens")
         # the LM head + argmax stage alone, given the oracle's hidden states: the strict id rule
@@ -290,11 +292,6 @@ def test_verify_schema_exhaustive_field(pkg, orc):
 
 # ---- 4B-shape drafter at full sizes ------------------------------------------------------------------------------
 
-@pytest.fixture(scope="module")
-def full_weights():
-    return synth.make_weights(synth.FULL, 2000)
-
-
 def test_full_text_block(pkg, orc, full_weights):
     """Text mode at the 4B shape: context 2048 (random context K/V), block 16, unconstrained vocabulary."""
     wl = synth.make_workload("text_4b_b1")
@@ -362,4 +359,92 @@ def test_full_fixed_width_batch_sampled_requests(pkg, orc, full_weights):
     oacc, ocom, oval = orc.verify(1, toks, layout=lay, rule=lay["rule"], pad_id=lay["pad_id"])
     np.testing.assert_array_equal(acc.cpu().numpy(), oacc)
     np.testing.assert_array_equal(com.cpu().numpy(), ocom)
+    dr.close()
+
+
+# ---- 4B shape: the context preparation chained into the block pass ----------------------------------------------
+
+def test_full_prepare_then_draft_ragged_append(pkg, orc, full_weights):
+    """Context preparation chained into the block pass at the 4B shape: four requests with ragged contexts (one
+    empty before its append, one receiving nothing in the second), written in two appends, then one 16-position
+    text block per request (64 block rows: the token-tile path).  Each stage is checked against the oracle given
+    the same input: the store against the oracle's preparation from the same features, the block pass (every
+    request) against the oracle run on the GPU's store, then the greedy verification."""
+    s = synth.FULL
+    lens1 = np.array([200, 0, 500, 13], np.int32)
+    lens2 = np.array([56, 40, 0, 3], np.int32)
+    ctx_len = lens1 + lens2
+    t_cap = int(ctx_len.max())
+    B, L = 4, 16
+    off1 = np.concatenate([[0], np.cumsum(lens1)]).astype(np.int32)
+    off2 = np.concatenate([[0], np.cumsum(lens2)]).astype(np.int32)
+    dr, om, kv, _ = _prepare_both(pkg, orc, s, full_weights, off1, t_cap, L, B, 3101)
+    f2 = synth.make_features(s, int(off2[-1]), 3102)
+    dr.prepare_context(B, off2, f2, pos_start=lens1)
+    kv = orc.prepare_context(om, off2, f2, t_cap, batch=B, pos_start=lens1, kv_store=kv)
+    assert _compare_store(dr, kv, ctx_len, B) == 4
+    anchor = np.array([11, 150000, 77777, 151934], np.int32)
+    # stage by stage (reading R21): the block pass against the oracle run on the store the GPU prepared
+    toks, _ = _draft_and_compare(pkg, orc, dr, om, bits_of(dr.kv_view(B)), t_cap, ctx_len, anchor, s.vocab - 1, L, B)
+    target, g = synth.make_target_rows(toks, s.vocab, 0.25, 3103)
+    acc, com, val = dr.verify_text(B, L, dev_i32(toks), dev_i32(target))
+    oacc, ocom, oval = orc.verify(0, toks, target)
+    np.testing.assert_array_equal(acc.cpu().numpy(), oacc)
+    np.testing.assert_array_equal(com.cpu().numpy(), ocom)
+    np.testing.assert_array_equal(oacc, 1 + np.minimum(g, L - 1))
+    dr.close()
+
+
+def test_full_prepare_then_draft_few_token(pkg, orc, full_weights):
+    """The batch-1 text workload with a prepared context instead of a random store: 2048 rows written in two
+    appends (1500 + 548), then one 16-position block on the few-token path (stream GEMMs, cluster attention)."""
+    s = synth.FULL
+    lens1, lens2 = np.array([1500], np.int32), np.array([548], np.int32)
+    T = 2048
+    dr, om, kv, _ = _prepare_both(pkg, orc, s, full_weights, np.array([0, 1500], np.int32), T, 16, 1, 3201)
+    f2 = synth.make_features(s, 548, 3202)
+    dr.prepare_context(1, np.array([0, 548], np.int32), f2, pos_start=lens1)
+    kv = orc.prepare_context(om, np.array([0, 548], np.int32), f2, T, batch=1, pos_start=lens1, kv_store=kv)
+    ctx_len = lens1 + lens2
+    assert _compare_store(dr, kv, ctx_len, 1) == 1
+    _draft_and_compare(pkg, orc, dr, om, bits_of(dr.kv_view(1)), T, ctx_len, np.array([4242], np.int32),
+                       s.vocab - 1, 16, 1)
+    dr.close()
+
+
+# ---- 4B shape: corner points of the throughput sweep --------------------------------------------------------------
+
+@pytest.mark.parametrize("B,T,L", [(1, 512, 16), (64, 16384, 16), (64, 16384, 385)])
+def test_sweep_corner(pkg, orc, full_weights, B, T, L):
+    """Corners of the sweep (batch {1, 64} x context {512, 16384} x block {16 text, 385 special-token}) at full
+    size.  Requests 0 and B - 1 take their context K/V from the seeded host generator and are checked end to end
+    by the oracle (requests are independent); the others are drawn on the device and only run."""
+    base = "text_4b_b1" if L == 16 else "primitive_special_b1"
+    wl = synth.make_workload(base, batch=B, t_ctx=T, seed=5100 + B + L)
+    s = wl.shape
+    dr = pkg.Drafter(s, full_weights, B, wl.block_len, T, device=DEV)
+    kv_dev = dr.kv_view(B)
+    gen = torch.Generator(device=DEV).manual_seed(5200 + B + L)
+    for layer in range(s.n_layers):
+        kv_dev[layer].normal_(generator=gen)
+    host = {}
+    for b in sorted({0, B - 1}):
+        kvb = synth.make_kv_store(s, 1, T, 5300 + b)
+        kv_dev[:, b:b + 1].copy_(torch.from_numpy(kvb.view(np.int16)).view(torch.bfloat16))
+        host[b] = kvb
+    om = orc.Model(s, full_weights)
+    toks, _ = _draft_and_compare(pkg, orc, dr, om, lambda b: host[b], T, wl.ctx_len, wl.anchor, wl.mask_id,
+                                 wl.block_len, B, layout=wl.layout, requests=sorted(host))
+    if wl.layout is None:
+        target, _ = synth.make_target_rows(toks, s.vocab, 0.25, 5400)
+        acc, com, val = dr.verify_text(B, wl.block_len, dev_i32(toks), dev_i32(target))
+        oacc, ocom, oval = orc.verify(0, toks, target)
+    else:
+        lay = wl.layout
+        lay_d, rule_d = pkg.Drafter.layout(lay, B, wl.block_len, DEV)
+        acc, com, val = dr.verify_schema(B, wl.block_len, dev_i32(toks), lay_d, rule_d, lay["pad_id"])
+        oacc, ocom, oval = orc.verify(1, toks, layout=lay, rule=lay["rule"], pad_id=lay["pad_id"])
+    np.testing.assert_array_equal(acc.cpu().numpy(), oacc)
+    np.testing.assert_array_equal(com.cpu().numpy(), ocom)
+    np.testing.assert_array_equal(val.cpu().numpy(), oval)
     dr.close()
