@@ -14,7 +14,8 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libfpd.so")
+# FPD_LIBRARY=debug selects the FPD_DEBUG build (every call waits for its kernels and reports their errors)
+LIB_PATH = os.path.join(_HERE, "libfpd_debug.so" if os.environ.get("FPD_LIBRARY") == "debug" else "libfpd.so")
 MAX_LAYERS = 8
 
 FPD_OK = 0

@@ -2,6 +2,7 @@
 // carving, and the order of kernel launches of each call.  Every entry point validates all of its arguments
 // before it launches anything and returns an fpd_status; nothing here synchronises, allocates or copies
 // between host and device except fpd_model_create / fpd_model_destroy / fpd_device_status.
+#include <nvtx3/nvToolsExt.h>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -298,6 +299,28 @@ fpd_status set_last_error(fpd_status s, const char* msg) {
   return s;
 }
 size_t argmax_scratch_bytes(const fpd_model* m, int batch, int block_len) { return ws_argmax_bytes(*m, batch, block_len); }
+
+// NVTX range over one entry point; with FPD_DEBUG the call's kernels are also waited for and checked.
+struct ApiScope {
+  const char* name;
+  cudaStream_t st;
+  ApiScope(const char* n, void* s) : name(n), st((cudaStream_t)s) { nvtxRangePushA(n); }
+  ~ApiScope() { nvtxRangePop(); }
+  fpd_status done(fpd_status r) const {
+#ifdef FPD_DEBUG
+    if (r != FPD_OK) return r;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return r;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return set_last_error(FPD_ERR_CUDA, (std::string(name) + ": " + cudaGetErrorString(e)).c_str());
+    int32_t code = 0;
+    if (cudaMemcpyFromSymbol(&code, g_device_check, sizeof(code)) == cudaSuccess && code != 0)
+      return set_last_error(FPD_ERR_DEVICE_CHECK, (std::string(name) + ": device check " + std::to_string(code)).c_str());
+#endif
+    return r;
+  }
+};
 }  // namespace fpd
 
 extern "C" {
@@ -419,7 +442,7 @@ fpd_status fpd_prepare_context(fpd_model* m, int batch, int total_rows, const in
                                   ws_bytes, stream);
 }
 
-fpd_status fpd_prepare_context_rows(fpd_model* m, int batch, int total_rows, const int32_t* row_off,
+static fpd_status prepare_rows_impl(fpd_model* m, int batch, int total_rows, const int32_t* row_off,
                                     const int32_t* row_cnt, const int32_t* pos_start, const void* const* feats,
                                     void* kv_store, int t_cap, void* workspace, size_t ws_bytes, void* stream) {
   if (!m) return fail(FPD_ERR_INVALID_ARG, "model is null");
@@ -485,9 +508,9 @@ fpd_status fpd_prepare_context_rows(fpd_model* m, int batch, int total_rows, con
 }
 
 // ---- a3..a7 -------------------------------------------------------------------------------------------------
-fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store, int t_cap, const int32_t* ctx_len,
-                           const int32_t* anchor, int32_t mask_id, void* hidden_out, void* layer_hidden,
-                           void* workspace, size_t ws_bytes, void* stream) {
+static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* kv_store, int t_cap,
+                                   const int32_t* ctx_len, const int32_t* anchor, int32_t mask_id, void* hidden_out,
+                                   void* layer_hidden, void* workspace, size_t ws_bytes, void* stream) {
   if (!m) return fail(FPD_ERR_INVALID_ARG, "model is null");
   const auto& d = m->d;
   if (batch < 1 || L < 2 || t_cap < 1) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d, t_cap %d", batch, L, t_cap);
@@ -710,9 +733,9 @@ fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store,
 }
 
 // ---- a8 -----------------------------------------------------------------------------------------------------
-fpd_status fpd_constrain_argmax(fpd_model* m, int batch, int L, const void* hidden, const fpd_vocab_layout* layout,
-                                int32_t* tokens_out, float* logits_out, float* margin_out, void* workspace,
-                                size_t ws_bytes, void* stream) {
+static fpd_status constrain_argmax_impl(fpd_model* m, int batch, int L, const void* hidden,
+                                        const fpd_vocab_layout* layout, int32_t* tokens_out, float* logits_out,
+                                        float* margin_out, void* workspace, size_t ws_bytes, void* stream) {
   if (!m) return fail(FPD_ERR_INVALID_ARG, "model is null");
   const auto& d = m->d;
   if (batch < 1 || L < 2) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d", batch, L);
@@ -787,9 +810,9 @@ fpd_status fpd_constrain_argmax(fpd_model* m, int batch, int L, const void* hidd
 }
 
 // ---- a9 -----------------------------------------------------------------------------------------------------
-fpd_status fpd_verify(int mode, int batch, int L, const int32_t* draft, const int32_t* target,
-                      const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id, int32_t* accept_len,
-                      int32_t* committed, int32_t* valid_out, void* stream) {
+static fpd_status verify_impl(int mode, int batch, int L, const int32_t* draft, const int32_t* target,
+                              const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id, int32_t* accept_len,
+                              int32_t* committed, int32_t* valid_out, void* stream) {
   if (mode != FPD_VERIFY_TEXT && mode != FPD_VERIFY_SCHEMA) return fail(FPD_ERR_INVALID_ARG, "mode %d", mode);
   if (batch < 1 || L < 2) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d", batch, L);
   if (!draft || !accept_len || !committed) return fail(FPD_ERR_INVALID_ARG, "null pointer argument");
@@ -813,13 +836,54 @@ fpd_status fpd_verify(int mode, int batch, int L, const int32_t* draft, const in
   return FPD_OK;
 }
 
-fpd_status fpd_sd_advance(int batch, int L, int t_cap, int32_t* accept_len, const int32_t* committed,
-                          int32_t* ctx_len, int32_t* pos_start, int32_t* anchor, void* stream) {
+static fpd_status sd_advance_impl(int batch, int L, int t_cap, int32_t* accept_len, const int32_t* committed,
+                                  int32_t* ctx_len, int32_t* pos_start, int32_t* anchor, void* stream) {
   if (batch < 1 || L < 2 || t_cap < 1) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d, t_cap %d", batch, L, t_cap);
   if (!accept_len || !committed || !ctx_len || !pos_start || !anchor) return fail(FPD_ERR_INVALID_ARG, "null pointer argument");
   FPD_CUDA(launch_sd_advance(batch, L, t_cap, accept_len, committed, ctx_len, pos_start, anchor, (cudaStream_t)stream),
            "speculative-step advance");
   return FPD_OK;
+}
+
+// ---- exported entry points: an NVTX range around each call; in a build with FPD_DEBUG defined, every call
+// that is not being captured into a graph also synchronises its stream and returns the first CUDA error or
+// device-side check of its kernels as its own status ---------------------------------------------------------
+fpd_status fpd_prepare_context_rows(fpd_model* m, int batch, int total_rows, const int32_t* row_off,
+                                    const int32_t* row_cnt, const int32_t* pos_start, const void* const* feats,
+                                    void* kv_store, int t_cap, void* workspace, size_t ws_bytes, void* stream) {
+  ApiScope scope("fpd_prepare_context", stream);
+  return scope.done(prepare_rows_impl(m, batch, total_rows, row_off, row_cnt, pos_start, feats, kv_store, t_cap,
+                                      workspace, ws_bytes, stream));
+}
+
+fpd_status fpd_draft_block(fpd_model* m, int batch, int L, const void* kv_store, int t_cap, const int32_t* ctx_len,
+                           const int32_t* anchor, int32_t mask_id, void* hidden_out, void* layer_hidden,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  ApiScope scope("fpd_draft_block", stream);
+  return scope.done(draft_block_impl(m, batch, L, kv_store, t_cap, ctx_len, anchor, mask_id, hidden_out, layer_hidden,
+                                     workspace, ws_bytes, stream));
+}
+
+fpd_status fpd_constrain_argmax(fpd_model* m, int batch, int L, const void* hidden, const fpd_vocab_layout* layout,
+                                int32_t* tokens_out, float* logits_out, float* margin_out, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  ApiScope scope("fpd_constrain_argmax", stream);
+  return scope.done(constrain_argmax_impl(m, batch, L, hidden, layout, tokens_out, logits_out, margin_out, workspace,
+                                          ws_bytes, stream));
+}
+
+fpd_status fpd_verify(int mode, int batch, int L, const int32_t* draft, const int32_t* target,
+                      const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id, int32_t* accept_len,
+                      int32_t* committed, int32_t* valid_out, void* stream) {
+  ApiScope scope("fpd_verify", stream);
+  return scope.done(verify_impl(mode, batch, L, draft, target, layout, rule, pad_id, accept_len, committed, valid_out,
+                                stream));
+}
+
+fpd_status fpd_sd_advance(int batch, int L, int t_cap, int32_t* accept_len, const int32_t* committed,
+                          int32_t* ctx_len, int32_t* pos_start, int32_t* anchor, void* stream) {
+  ApiScope scope("fpd_sd_advance", stream);
+  return scope.done(sd_advance_impl(batch, L, t_cap, accept_len, committed, ctx_len, pos_start, anchor, stream));
 }
 
 }  // extern "C"
