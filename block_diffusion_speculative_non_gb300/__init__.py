@@ -25,6 +25,12 @@ FPD_VERIFY_TEXT, FPD_VERIFY_SCHEMA = 0, 1
 FPD_RULE_NONE, FPD_RULE_MEMBER, FPD_RULE_DIGIT, FPD_RULE_DIGIT_LAST = 0, 1, 2, 3
 
 
+class GridFormat(ctypes.Structure):
+    _fields_ = [("digit_id", ctypes.c_int32 * 10), ("plus_id", ctypes.c_int32), ("minus_id", ctypes.c_int32),
+                ("pad_id", ctypes.c_int32), ("n_axes", ctypes.c_int32), ("width", ctypes.c_int32),
+                ("axis_sep", ctypes.c_char), ("point_sep", ctypes.c_char)]
+
+
 class FpdError(RuntimeError):
     def __init__(self, status: int, where: str, msg: str):
         super().__init__(f"{where}: {STATUS.get(status, status)}: {msg}")
@@ -53,7 +59,7 @@ class VocabLayout(ctypes.Structure):
 _lib = None
 _EXPORTS = ["fpd_model_create", "fpd_model_destroy", "fpd_kv_store_bytes", "fpd_workspace_bytes",
             "fpd_prepare_context", "fpd_prepare_context_rows", "fpd_draft_block", "fpd_constrain_argmax",
-            "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_sd_advance", "fpd_last_error",
+            "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_sd_advance", "fpd_grid_to_text", "fpd_last_error",
             "fpd_kernel_launches", "fpd_device_status"]
 
 
@@ -77,6 +83,8 @@ def lib():
         l.fpd_prepare_context_rows.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.POINTER(vp), vp,
                                                ctypes.c_int, vp, sz, vp]
         l.fpd_sd_advance.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp]
+        l.fpd_grid_to_text.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, ctypes.POINTER(GridFormat), ctypes.c_char_p,
+                                       sz, ctypes.POINTER(sz)]
         l.fpd_draft_block.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, i32, vp, vp, vp,
                                       sz, vp]
         l.fpd_constrain_argmax.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.POINTER(VocabLayout), vp, vp,
@@ -90,6 +98,7 @@ def lib():
         l.fpd_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         for f in ("fpd_model_create", "fpd_prepare_context", "fpd_prepare_context_rows", "fpd_draft_block",
                   "fpd_constrain_argmax", "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_sd_advance",
+                  "fpd_grid_to_text",
                   "fpd_device_status"):
             getattr(l, f).restype = ctypes.c_int
         _lib = l
@@ -201,6 +210,29 @@ def fpd_verify(mode, batch, block_len, draft, target, layout, rule, pad_id, acce
     _check(lib().fpd_verify(mode, batch, block_len, _ptr(draft), _ptr(target),
                             ctypes.byref(layout) if layout is not None else None, _ptr(rule), int(pad_id),
                             _ptr(accept_len), _ptr(committed), _ptr(valid_out), _stream(stream)), "fpd_verify")
+
+
+def grid_format(digit_ids, plus_id, minus_id, pad_id, n_axes=3, width=5, axis_sep=",", point_sep=";") -> GridFormat:
+    f = GridFormat()
+    for k, t in enumerate(digit_ids):
+        f.digit_id[k] = int(t)
+    f.plus_id, f.minus_id, f.pad_id, f.n_axes, f.width = int(plus_id), int(minus_id), int(pad_id), n_axes, width
+    f.axis_sep, f.point_sep = axis_sep.encode(), point_sep.encode()
+    return f
+
+
+def fpd_grid_to_text(committed, accept, fmt: GridFormat) -> list:
+    """Host arrays (numpy int32 [B, L] committed tokens, [B] accepted positions) -> one text per request."""
+    import numpy as np
+    cm = np.ascontiguousarray(committed, dtype=np.int32)
+    acc = np.ascontiguousarray(accept, dtype=np.int32)
+    B, L = cm.shape
+    cap = B * (L * 4 + 16)
+    out = ctypes.create_string_buffer(cap)
+    offs = (ctypes.c_size_t * (B + 1))()
+    _check(lib().fpd_grid_to_text(B, L, cm.ctypes.data, acc.ctypes.data, ctypes.byref(fmt), out, cap, offs),
+           "fpd_grid_to_text")
+    return [ctypes.string_at(ctypes.addressof(out) + offs[b]).decode() for b in range(B)]
 
 
 def fpd_kernel_launches() -> int:

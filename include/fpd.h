@@ -254,6 +254,33 @@ fpd_status fpd_verify(int mode, int batch, int block_len, const int32_t* draft, 
 fpd_status fpd_sd_advance(int batch, int block_len, int t_cap, int32_t* accept_len, const int32_t* committed,
                           int32_t* ctx_len, int32_t* pos_start, int32_t* anchor, void* stream);
 
+/* ---- f4: fixed-width grid -> the target's text format (host-side) ----------------------------------------
+ * VFlash paper (zh) §2.3: for targets that tokenise numbers as text, every coordinate gets one sign slot and
+ * `width` digit slots with unused HIGH digits filled by the mask (pad) token; the grid keeps each position's
+ * role and is converted back to the target's text format afterwards, its separators marking block boundaries.
+ * Block layout (request b, block position j = 0..L-1; j = 0 is the start token): waypoint w occupies positions
+ * 1 + w * (n_axes * (1 + width) + 1) onwards: n_axes fields [sign][d_1..d_width], then one separator.
+ * The text of request b is the values of its first complete waypoints among the accepted positions 1..accept[b]
+ * (a waypoint counts when all its n_axes fields lie inside the accepted prefix): each field's value as a decimal
+ * integer (leading zeros dropped, "-" only for a negative non-zero value), axes joined by axis_sep, waypoints by
+ * point_sep.  A field that breaks the schema (a sign slot that is neither plus nor minus, a pad after a real digit,
+ * a pad or a non-digit in the last slot) ends the request's text there.
+ *   committed  HOST [batch, block_len] int32: fpd_verify's committed tokens (block positions 1..L-1 at 0..L-2)
+ *   accept     HOST [batch] int32: accepted positions
+ *   out        HOST buffer of out_bytes; request b's NUL-terminated text starts at out + offsets[b]
+ *   offsets    HOST [batch + 1]: offsets[batch] = total bytes written (FPD_ERR_CAPACITY when out is too small)
+ * Pure host code: needs no GPU. */
+typedef struct fpd_grid_format {
+  int32_t digit_id[10];   /* token ids of the digits 0..9 */
+  int32_t plus_id, minus_id, pad_id;
+  int32_t n_axes;         /* fields per waypoint */
+  int32_t width;          /* digit slots per field (>= 1) */
+  char axis_sep, point_sep;
+} fpd_grid_format;
+
+fpd_status fpd_grid_to_text(int batch, int block_len, const int32_t* committed, const int32_t* accept,
+                            const fpd_grid_format* fmt, char* out, size_t out_bytes, size_t* offsets);
+
 /* ---- diagnostics ---------------------------------------------------------------------------------------- */
 const char* fpd_last_error(void);          /* thread-local message of the last failing call */
 uint64_t fpd_kernel_launches(void);        /* kernels launched by this library since load (all threads) */

@@ -288,3 +288,56 @@ def verify(mode, draft, target=None, layout=None, rule=None, pad_id=-1):
     if rc:
         raise ValueError("oracle_verify: bad arguments")
     return acc, com, val
+
+
+def grid_field_value(tokens, digit_ids, plus_id, minus_id, pad_id):
+    """VFlash paper (zh) §2.3: one fixed-width field [sign][d_1..d_w] -> its integer value, or None when the field
+    is not a well-formed numeral (sign not + or -, a pad after a real digit, a pad or non-digit in the last slot).
+    Unused HIGH digits hold the pad (mask) token, so the digits read most significant first."""
+    sign, digits = int(tokens[0]), [int(t) for t in tokens[1:]]
+    if sign not in (plus_id, minus_id):
+        return None
+    value, seen_real = 0, False
+    for i, t in enumerate(digits):
+        if t == pad_id:
+            if seen_real or i == len(digits) - 1:
+                return None
+            continue
+        if t not in digit_ids:
+            return None
+        seen_real = True
+        value = 10 * value + digit_ids.index(t)
+    return -value if sign == minus_id else value
+
+
+def grid_to_text(committed, accept, digit_ids, plus_id, minus_id, pad_id, n_axes=3, width=5, axis_sep=",",
+                 point_sep=";"):
+    """VFlash paper (zh) §2.3: the fixed-width grid converted back to the target's text format.  committed[b][i]
+    holds block position i + 1 (position 0 is the start token); waypoint w starts at block position
+    1 + w * (n_axes * (1 + width) + 1) with n_axes fields and one separator.  Request b's text lists its complete
+    waypoints inside the accepted positions 1..accept[b], stopping at the first malformed field."""
+    digit_ids = [int(t) for t in digit_ids]
+    per_wp = n_axes * (1 + width) + 1
+    texts = []
+    for row, acc in zip(np.asarray(committed), np.asarray(accept)):
+        L = len(row) + 0
+        acc = max(0, min(int(acc), L - 1))
+        points = []
+        w = 0
+        while True:
+            first = 1 + w * per_wp
+            if first + n_axes * (1 + width) - 1 > acc:
+                break
+            vals = []
+            for a in range(n_axes):
+                p0 = first + a * (1 + width)
+                v = grid_field_value(row[p0 - 1:p0 - 1 + 1 + width], digit_ids, plus_id, minus_id, pad_id)
+                if v is None:
+                    break
+                vals.append(str(v))
+            if len(vals) < n_axes:
+                break
+            points.append(axis_sep.join(vals))
+            w += 1
+        texts.append(point_sep.join(points))
+    return texts
