@@ -22,7 +22,7 @@ FPD_OK = 0
 STATUS = {0: "FPD_OK", 1: "FPD_ERR_INVALID_ARG", 2: "FPD_ERR_SHAPE", 3: "FPD_ERR_CAPACITY",
           4: "FPD_ERR_UNSUPPORTED", 5: "FPD_ERR_CUDA", 6: "FPD_ERR_DEVICE_CHECK"}
 FPD_VERIFY_TEXT, FPD_VERIFY_SCHEMA = 0, 1
-FPD_RULE_NONE, FPD_RULE_MEMBER, FPD_RULE_DIGIT, FPD_RULE_DIGIT_LAST = 0, 1, 2, 3
+FPD_RULE_NONE, FPD_RULE_MEMBER, FPD_RULE_DIGIT, FPD_RULE_DIGIT_LAST, FPD_RULE_CONFIDENT = 0, 1, 2, 3, 4
 
 
 class GridFormat(ctypes.Structure):
@@ -53,13 +53,15 @@ class Weights(ctypes.Structure):
 
 class VocabLayout(ctypes.Structure):
     _fields_ = [("n_class", ctypes.c_int32), ("class_off", ctypes.POINTER(ctypes.c_int32)),
-                ("class_ranges", ctypes.POINTER(ctypes.c_int32)), ("pos_class", ctypes.c_void_p)]
+                ("class_ranges", ctypes.POINTER(ctypes.c_int32)), ("pos_class", ctypes.c_void_p),
+                ("n_pairs", ctypes.c_int32), ("pairs", ctypes.POINTER(ctypes.c_int16)), ("off_id", ctypes.c_int32)]
 
 
 _lib = None
 _EXPORTS = ["fpd_model_create", "fpd_model_destroy", "fpd_kv_store_bytes", "fpd_workspace_bytes",
             "fpd_prepare_context", "fpd_prepare_context_rows", "fpd_draft_block", "fpd_constrain_argmax",
-            "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_sd_advance", "fpd_grid_to_text", "fpd_last_error",
+            "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_verify_prefix", "fpd_sd_advance", "fpd_grid_to_text",
+            "fpd_last_error",
             "fpd_kernel_launches", "fpd_device_status"]
 
 
@@ -83,6 +85,8 @@ def lib():
         l.fpd_prepare_context_rows.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.POINTER(vp), vp,
                                                ctypes.c_int, vp, sz, vp]
         l.fpd_sd_advance.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp]
+        l.fpd_verify_prefix.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, ctypes.c_float, ctypes.POINTER(VocabLayout),
+                                        vp, i32, vp, vp, vp, vp]
         l.fpd_grid_to_text.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, ctypes.POINTER(GridFormat), ctypes.c_char_p,
                                        sz, ctypes.POINTER(sz)]
         l.fpd_draft_block.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, i32, vp, vp, vp,
@@ -98,7 +102,7 @@ def lib():
         l.fpd_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         for f in ("fpd_model_create", "fpd_prepare_context", "fpd_prepare_context_rows", "fpd_draft_block",
                   "fpd_constrain_argmax", "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_sd_advance",
-                  "fpd_grid_to_text",
+                  "fpd_grid_to_text", "fpd_verify_prefix",
                   "fpd_device_status"):
             getattr(l, f).restype = ctypes.c_int
         _lib = l
@@ -177,14 +181,17 @@ def fpd_draft_block(model, batch, block_len, kv_store, t_cap, ctx_len, anchor, m
                                  workspace_bytes, _stream(stream)), "fpd_draft_block")
 
 
-def make_layout(class_off, class_ranges, pos_class_dev) -> VocabLayout:
-    """Build an fpd_vocab_layout: class tables from host sequences, pos_class a device tensor (int16)."""
+def make_layout(class_off, class_ranges, pos_class_dev, pairs=None, off_id=0) -> VocabLayout:
+    """Build an fpd_vocab_layout: class tables from host sequences, pos_class a device tensor (int16); pairs an
+    optional host sequence of (p, q) block positions of the off-screen pairing rule with its off_id."""
     import numpy as np
     co = np.ascontiguousarray(class_off, dtype=np.int32)
     cr = np.ascontiguousarray(class_ranges, dtype=np.int32)
+    pr = np.ascontiguousarray(np.zeros((0, 2)) if pairs is None else pairs, dtype=np.int16).reshape(-1)
     lay = VocabLayout(len(co) - 1, co.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-                      cr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(pos_class_dev))
-    lay._keep = (co, cr, pos_class_dev)
+                      cr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(pos_class_dev), len(pr) // 2,
+                      pr.ctypes.data_as(ctypes.POINTER(ctypes.c_int16)) if len(pr) else None, int(off_id))
+    lay._keep = (co, cr, pos_class_dev, pr)
     return lay
 
 
@@ -210,6 +217,13 @@ def fpd_verify(mode, batch, block_len, draft, target, layout, rule, pad_id, acce
     _check(lib().fpd_verify(mode, batch, block_len, _ptr(draft), _ptr(target),
                             ctypes.byref(layout) if layout is not None else None, _ptr(rule), int(pad_id),
                             _ptr(accept_len), _ptr(committed), _ptr(valid_out), _stream(stream)), "fpd_verify")
+
+
+def fpd_verify_prefix(batch, block_len, draft, margin, tau, layout, rule, pad_id, accept_len, committed, valid_out,
+                      stream=None):
+    _check(lib().fpd_verify_prefix(batch, block_len, _ptr(draft), _ptr(margin), float(tau), ctypes.byref(layout),
+                                   _ptr(rule), int(pad_id), _ptr(accept_len), _ptr(committed), _ptr(valid_out),
+                                   _stream(stream)), "fpd_verify_prefix")
 
 
 def grid_format(digit_ids, plus_id, minus_id, pad_id, n_axes=3, width=5, axis_sep=",", point_sep=";") -> GridFormat:

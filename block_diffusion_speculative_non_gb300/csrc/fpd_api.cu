@@ -741,9 +741,23 @@ static fpd_status constrain_argmax_impl(fpd_model* m, int batch, int L, const vo
   if (batch < 1 || L < 2) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d", batch, L);
   if (!hidden || !tokens_out || !workspace) return fail(FPD_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(hidden) || !aligned16(workspace)) return fail(FPD_ERR_INVALID_ARG, "hidden/workspace not 16-byte aligned");
+  PairTable pt{};
   if (layout) {
     fpd_status s = check_layout(layout, d.vocab);
     if (s) return s;
+    if (layout->n_pairs < 0 || layout->n_pairs > FPD_MAX_PAIRS || (layout->n_pairs > 0 && !layout->pairs))
+      return fail(FPD_ERR_INVALID_ARG, "n_pairs %d (0..%d) or null pairs", layout->n_pairs, FPD_MAX_PAIRS);
+    if (layout->n_pairs > 0 && (layout->off_id < 0 || layout->off_id >= d.vocab))
+      return fail(FPD_ERR_SHAPE, "off_id %d outside [0, %d)", layout->off_id, d.vocab);
+    pt.n = layout->n_pairs;
+    pt.off_id = layout->off_id;
+    for (int k = 0; k < pt.n; k++) {
+      const int pp = layout->pairs[2 * k], qq = layout->pairs[2 * k + 1];
+      if (pp < 1 || pp >= L || qq < 1 || qq >= L || pp == qq)
+        return fail(FPD_ERR_SHAPE, "pair %d = (%d, %d) outside block positions 1..%d", k, pp, qq, L - 1);
+      pt.p[k] = (int16_t)pp;
+      pt.q[k] = (int16_t)qq;
+    }
   }
   fpd_status ds = check_device(*m);
   if (ds) return ds;
@@ -802,17 +816,21 @@ static fpd_status constrain_argmax_impl(fpd_model* m, int batch, int L, const vo
                                  d.d_model, d.rms_eps, L, st),
            "final norm");
   FPD_CUDA(launch_tc_lmhead(p, w.z, n_rows, (const bf16*)m->w.lm_head, d.d_model, d.vocab, w.items, w.n_items,
-                            w.max_items, w.packed, margin_out ? w.packed2 : nullptr, w.rows_sorted, logits_out,
+                            w.max_items, w.packed, (margin_out || pt.n) ? w.packed2 : nullptr, w.rows_sorted, logits_out,
                             m->num_sms, layout == nullptr, st),
            "LM head + argmax");
   FPD_CUDA(launch_lm_decode(tokens_out, margin_out, w.packed, w.packed2, w.inv_sorted, n_rows, st), "argmax decode");
+  FPD_CUDA(launch_pair_offscreen(tokens_out, margin_out, w.packed, w.packed2, w.inv_sorted, w.z,
+                                 (const bf16*)m->w.lm_head, d.d_model, L, batch, pt, st),
+           "off-screen pairs");
   return FPD_OK;
 }
 
 // ---- a9 -----------------------------------------------------------------------------------------------------
 static fpd_status verify_impl(int mode, int batch, int L, const int32_t* draft, const int32_t* target,
                               const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id, int32_t* accept_len,
-                              int32_t* committed, int32_t* valid_out, void* stream) {
+                              int32_t* committed, int32_t* valid_out, void* stream, const float* margin = nullptr,
+                              float tau = 0.f) {
   if (mode != FPD_VERIFY_TEXT && mode != FPD_VERIFY_SCHEMA) return fail(FPD_ERR_INVALID_ARG, "mode %d", mode);
   if (batch < 1 || L < 2) return fail(FPD_ERR_SHAPE, "batch %d, block_len %d", batch, L);
   if (!draft || !accept_len || !committed) return fail(FPD_ERR_INVALID_ARG, "null pointer argument");
@@ -831,7 +849,7 @@ static fpd_status verify_impl(int mode, int batch, int L, const int32_t* draft, 
     }
   }
   FPD_CUDA(launch_verify(mode, batch, L, draft, target, tb, layout ? layout->pos_class : nullptr, rule, pad_id,
-                         accept_len, committed, valid_out, (cudaStream_t)stream),
+                         accept_len, committed, valid_out, margin, tau, (cudaStream_t)stream),
            "verify");
   return FPD_OK;
 }
@@ -878,6 +896,16 @@ fpd_status fpd_verify(int mode, int batch, int L, const int32_t* draft, const in
   ApiScope scope("fpd_verify", stream);
   return scope.done(verify_impl(mode, batch, L, draft, target, layout, rule, pad_id, accept_len, committed, valid_out,
                                 stream));
+}
+
+fpd_status fpd_verify_prefix(int batch, int L, const int32_t* draft, const float* margin, float tau,
+                             const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id, int32_t* accept_len,
+                             int32_t* committed, int32_t* valid_out, void* stream) {
+  ApiScope scope("fpd_verify_prefix", stream);
+  if (!margin) return fail(FPD_ERR_INVALID_ARG, "prefix verification needs the margins");
+  if (!(tau >= 0.f)) return fail(FPD_ERR_SHAPE, "tau must be a non-negative number");
+  return scope.done(verify_impl(FPD_VERIFY_SCHEMA, batch, L, draft, nullptr, layout, rule, pad_id, accept_len,
+                                committed, valid_out, stream, margin, tau));
 }
 
 fpd_status fpd_sd_advance(int batch, int L, int t_cap, int32_t* accept_len, const int32_t* committed,

@@ -164,6 +164,13 @@ cudaError_t launch_tc_lmhead(const LmPlan& lp, const bf16* z_sorted, int n_rows,
                              unsigned long long* packed2, const int* rows_sorted, float* logits, int num_sms,
                              bool unconstrained, cudaStream_t st);
 // tokens[r] = argmax id; margin[r] (optional) = top-1 minus top-2 fp32 logit (+inf with one legal id)
+struct PairTable {
+  int n, off_id;
+  int16_t p[FPD_MAX_PAIRS], q[FPD_MAX_PAIRS];
+};
+cudaError_t launch_pair_offscreen(int32_t* tokens, float* margin, const unsigned long long* packed,
+                                  const unsigned long long* packed2, const int* inv_sorted, const bf16* z,
+                                  const bf16* w_lm, int d, int L, int B, const PairTable& pt, cudaStream_t st);
 cudaError_t launch_lm_decode(int32_t* tokens, float* margin, const unsigned long long* packed,
                              const unsigned long long* packed2, const int* inv_sorted, int n, cudaStream_t st);
 // RMSNorm of block rows into sorted order: out[i] = norm(hidden[map(rows_sorted[i])]), map drops anchors.
@@ -178,7 +185,7 @@ struct VerifyTables {
 };
 cudaError_t launch_verify(int mode, int B, int L, const int32_t* draft, const int32_t* target, const VerifyTables& tb,
                           const int16_t* pos_class, const int8_t* rule, int32_t pad_id, int32_t* accept,
-                          int32_t* committed, int32_t* valid, cudaStream_t st);
+                          int32_t* committed, int32_t* valid, const float* margin, float tau, cudaStream_t st);
 cudaError_t launch_sd_advance(int B, int L, int t_cap, int32_t* accept, const int32_t* committed, int32_t* ctx_len,
                               int32_t* pos_start, int32_t* anchor, cudaStream_t st);
 

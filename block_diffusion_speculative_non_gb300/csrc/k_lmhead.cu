@@ -196,6 +196,72 @@ __global__ void lm_decode_kernel(int32_t* __restrict__ tokens, float* __restrict
   }
 }
 
+// ---- cross-position rule (f3): off-screen coordinates in pairs -----------------------------------------------
+// VFlash paper (zh) §2.5: a cross-position rule pairs off-screen coordinates, on the computed logits.  One warp per
+// (request, pair): o_x = z_x . W[off_id] (fp32, fixed order) for both positions, a_x = the best legal logit other
+// than off_id (the top-1 word, or the top-2 word when the top-1 is off_id); both positions take off_id when
+// o_p + o_q > a_p + a_q, else their best other id.  The margin of both becomes the smaller of their own and
+// |(o_p + o_q) - (a_p + a_q)|.
+__global__ void pair_offscreen_kernel(int32_t* __restrict__ tokens, float* __restrict__ margin,
+                                      const unsigned long long* __restrict__ packed,
+                                      const unsigned long long* __restrict__ packed2,
+                                      const int* __restrict__ inv_sorted, const bf16* __restrict__ z,
+                                      const bf16* __restrict__ w_lm, int d, int L, int B, PairTable pt) {
+  pdl_trigger();
+  pdl_wait();
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (gw >= B * pt.n) return;
+  const int b = gw / pt.n, k = gw % pt.n;
+  const int rp = b * (L - 1) + pt.p[k] - 1, rq = b * (L - 1) + pt.q[k] - 1;
+  const int ip = inv_sorted[rp], iq = inv_sorted[rq];
+  if (ip < 0 || iq < 0) return;
+  const bf16* wo = w_lm + (size_t)pt.off_id * d;
+  const bf16* zp = z + (size_t)ip * d;
+  const bf16* zq = z + (size_t)iq * d;
+  float op = 0.f, oq = 0.f;
+  for (int c = lane * 8; c < d; c += 256) {
+    const uint4 uw = *reinterpret_cast<const uint4*>(wo + c), up = *reinterpret_cast<const uint4*>(zp + c),
+                uq = *reinterpret_cast<const uint4*>(zq + c);
+    const __nv_bfloat162* ew = reinterpret_cast<const __nv_bfloat162*>(&uw);
+    const __nv_bfloat162* ep = reinterpret_cast<const __nv_bfloat162*>(&up);
+    const __nv_bfloat162* eq = reinterpret_cast<const __nv_bfloat162*>(&uq);
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const float2 fw = __bfloat1622float2(ew[e]), fp = __bfloat1622float2(ep[e]), fq = __bfloat1622float2(eq[e]);
+      op = fmaf(fp.x, fw.x, fmaf(fp.y, fw.y, op));
+      oq = fmaf(fq.x, fw.x, fmaf(fq.y, fw.y, oq));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    op += __shfl_xor_sync(0xffffffffu, op, o);
+    oq += __shfl_xor_sync(0xffffffffu, oq, o);
+  }
+  if (lane != 0) return;
+  unsigned long long bp = packed[ip], bq = packed[iq];
+  if (bp && unpack_argmax_id(bp) == pt.off_id) bp = packed2[ip];
+  if (bq && unpack_argmax_id(bq) == pt.off_id) bq = packed2[iq];
+  if (!bp || !bq) return;   // a position whose only legal id is off_id keeps it
+  const float on = unpack_value(bp) + unpack_value(bq), off = op + oq;
+  const bool take_off = off > on;
+  tokens[rp] = take_off ? pt.off_id : unpack_argmax_id(bp);
+  tokens[rq] = take_off ? pt.off_id : unpack_argmax_id(bq);
+  if (margin) {
+    const float gap = fabsf(off - on);
+    margin[rp] = fminf(margin[rp], gap);
+    margin[rq] = fminf(margin[rq], gap);
+  }
+}
+
+cudaError_t launch_pair_offscreen(int32_t* tokens, float* margin, const unsigned long long* packed,
+                                  const unsigned long long* packed2, const int* inv_sorted, const bf16* z,
+                                  const bf16* w_lm, int d, int L, int B, const PairTable& pt, cudaStream_t st) {
+  if (pt.n <= 0) return cudaSuccess;
+  const int warps = B * pt.n;
+  return launch_k(pair_offscreen_kernel, ceil_div(warps, 8), 256, 0, st, tokens, margin, packed, packed2, inv_sorted,
+                  z, w_lm, d, L, B, pt);
+}
+
 cudaError_t launch_lm_decode(int32_t* tokens, float* margin, const unsigned long long* packed,
                              const unsigned long long* packed2, const int* inv_sorted, int n, cudaStream_t st) {
   const int grid = std::min(ceil_div(n, 256), 1024);

@@ -20,7 +20,7 @@ __global__ void verify_kernel(int mode, int B, int L, const int32_t* __restrict_
                               const int32_t* __restrict__ target, VerifyTables tb,
                               const int16_t* __restrict__ pos_class, const int8_t* __restrict__ rule, int32_t pad_id,
                               int32_t* __restrict__ accept, int32_t* __restrict__ committed,
-                              int32_t* __restrict__ valid) {
+                              int32_t* __restrict__ valid, const float* __restrict__ margin, float tau) {
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -58,6 +58,8 @@ __global__ void verify_kernel(int mode, int B, int L, const int32_t* __restrict_
             fail = true;
           }
         }
+        // f3 (VFlash paper (zh) §2.5): an uncertain coordinate ends the kept prefix like a failing rule
+        if (r == FPD_RULE_CONFIDENT && margin && !(margin[(size_t)b * (L - 1) + j - 1] >= tau)) fail = true;
         if (r == FPD_RULE_DIGIT || r == FPD_RULE_DIGIT_LAST) {
           const int pr = rl[j - 1];
           const bool prev_real = j >= 2 && (pr == FPD_RULE_DIGIT || pr == FPD_RULE_DIGIT_LAST) && dr[j - 2] != pad_id;
@@ -79,9 +81,9 @@ __global__ void verify_kernel(int mode, int B, int L, const int32_t* __restrict_
 
 cudaError_t launch_verify(int mode, int B, int L, const int32_t* draft, const int32_t* target, const VerifyTables& tb,
                           const int16_t* pos_class, const int8_t* rule, int32_t pad_id, int32_t* accept,
-                          int32_t* committed, int32_t* valid, cudaStream_t st) {
+                          int32_t* committed, int32_t* valid, const float* margin, float tau, cudaStream_t st) {
   return launch_k(verify_kernel, ceil_div(B, 4), 128, 0, st, mode, B, L, draft, target, tb, pos_class, rule, pad_id,
-                  accept, committed, valid);
+                  accept, committed, valid, margin, tau);
 }
 
 // ---- the step between a text verification and the next block (one thread per request) ------------------------

@@ -10,7 +10,8 @@ import torch
 
 from . import (FPD_VERIFY_SCHEMA, FPD_VERIFY_TEXT, MAX_LAYERS, ModelDesc, Weights, fpd_constrain_argmax,
                fpd_draft_block, fpd_kv_store_bytes, fpd_model_create, fpd_model_destroy, fpd_prepare_context,
-               fpd_prepare_context_rows, fpd_sd_advance, fpd_verify, fpd_workspace_bytes, make_layout)
+               fpd_prepare_context_rows, fpd_sd_advance, fpd_verify, fpd_verify_prefix, fpd_workspace_bytes,
+               make_layout)
 
 _LAYER_KEYS = ("attn_norm", "wqkv", "q_norm", "k_norm", "wo", "mlp_norm", "w_gate_up", "w_down")
 
@@ -98,6 +99,15 @@ class Drafter:
         fpd_prepare_context_rows(self.handle, batch, total_rows, row_off_d, row_cnt_d, pos_start_d, feats_d,
                                  self.kv_store, self.t_cap, self.workspace, self.ws_bytes, stream)
 
+    def verify_prefix(self, batch, block_len, draft, margin, tau, layout, rule, pad_id, stream=None):
+        """Primitive acceptance keeping the prefix before the first failing or uncertain position."""
+        dev = self.device
+        accept = torch.empty(batch, dtype=torch.int32, device=dev)
+        committed = torch.empty(batch, block_len, dtype=torch.int32, device=dev)
+        valid = torch.empty(batch, dtype=torch.int32, device=dev)
+        fpd_verify_prefix(batch, block_len, draft, margin, tau, layout, rule, pad_id, accept, committed, valid, stream)
+        return accept, committed, valid
+
     def spec_state(self, batch, block_len, ctx_len, anchor):
         """Device buffers of a text speculative loop (see spec_step), starting from ctx_len / anchor."""
         return SpecState(self, batch, block_len, ctx_len, anchor)
@@ -124,7 +134,8 @@ class Drafter:
         if pc.ndim == 1:
             pc = np.broadcast_to(pc, (batch, block_len))
         pc_d = torch.from_numpy(np.array(pc, dtype=np.int16, order="C", copy=True)).to(device)
-        lay = make_layout(layout_np["class_off"], layout_np["class_ranges"], pc_d)
+        lay = make_layout(layout_np["class_off"], layout_np["class_ranges"], pc_d, pairs=layout_np.get("pairs"),
+                          off_id=layout_np.get("off_id", 0))
         rule = layout_np.get("rule")
         rule_d = None
         if rule is not None:

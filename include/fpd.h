@@ -45,6 +45,7 @@ extern "C" {
 #define FPD_MAX_LAYERS 8
 #define FPD_MAX_CLASSES 32   /* vocabulary classes in one layout */
 #define FPD_MAX_RANGES 64    /* [lo,hi) id ranges over all classes of one layout */
+#define FPD_MAX_PAIRS 128    /* cross-position pairs of one layout */
 
 typedef enum {
   FPD_OK = 0,
@@ -116,6 +117,14 @@ typedef struct fpd_vocab_layout {
   const int32_t* class_off;      /* host [n_class + 1], class_off[0] = 0, total ranges <= FPD_MAX_RANGES */
   const int32_t* class_ranges;   /* host [2 * class_off[n_class]] (lo, hi) pairs */
   const int16_t* pos_class;      /* device [B * L] */
+  /* Cross-position rule (f3; VFlash paper (zh) §2.5: a cross-position rule pairs off-screen coordinates, acting on
+   * the computed logits).  For every declared pair (p, q) of block positions and every request, both positions
+   * take off_id or neither does: with a_x the largest logit of x's legal ids other than off_id and o_x the logit
+   * of off_id at x, both take off_id when o_p + o_q > a_p + a_q (fp32 sums), else both take their best other
+   * id.  off_id must be legal at both positions.  n_pairs = 0 (zero-initialised struct) disables the rule. */
+  int32_t n_pairs;               /* 0..FPD_MAX_PAIRS */
+  const int16_t* pairs;          /* host [2 * n_pairs]: (p, q), 1 <= p, q < L, p != q */
+  int32_t off_id;
 } fpd_vocab_layout;
 
 /* Schema rules for primitive-mode acceptance, one int8 per block position (device [B*L]).
@@ -126,8 +135,10 @@ enum {
   FPD_RULE_MEMBER = 1,      /* token must lie in its position's class */
   FPD_RULE_DIGIT = 2,       /* digit slot, not the last of its field: member; pad_id allowed only while the
                                previous slot is not a digit slot holding a real digit */
-  FPD_RULE_DIGIT_LAST = 3   /* last digit slot of a field: member, must be a real digit (!= pad_id), and
+  FPD_RULE_DIGIT_LAST = 3,  /* last digit slot of a field: member, must be a real digit (!= pad_id), and
                                the same ordering rule as FPD_RULE_DIGIT */
+  FPD_RULE_CONFIDENT = 4    /* member, and the drafter's top-2 margin at the position is at least tau
+                               (fpd_verify_prefix; fails like a schema rule otherwise) */
 };
 
 enum { FPD_VERIFY_TEXT = 0, FPD_VERIFY_SCHEMA = 1 };
@@ -235,6 +246,19 @@ fpd_status fpd_constrain_argmax_noalloc(fpd_model* model, int batch, int block_l
 fpd_status fpd_verify(int mode, int batch, int block_len, const int32_t* draft, const int32_t* target,
                       const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id,
                       int32_t* accept_len, int32_t* committed, int32_t* valid_out, void* stream);
+
+/* ---- f3: primitive acceptance that keeps a prefix up to the first uncertain coordinate ----------------------
+ * VFlash paper (zh) §2.5: the prediction passes an acceptance test (the schema validator and, for bounding boxes,
+ * a spatial confidence check); the first k draft positions are kept, and for bounding boxes k stops before the
+ * first uncertain coordinate.  Reading: a coordinate is uncertain when the drafter's own top-2 logit margin there
+ * (fpd_constrain_argmax's margin_out) is below tau.  Position j = 1..L-1 fails when its rule (FPD_RULE_*) fails,
+ * FPD_RULE_CONFIDENT also failing when margin[b][j-1] < tau; with p the first failing position, accept_len = p - 1
+ * (all L - 1 when none fails), committed = d_1..d_accept, valid = (p == L).
+ *   margin  device [B, L-1] float (the margins of the drafted positions); other arguments as fpd_verify's schema
+ *           mode */
+fpd_status fpd_verify_prefix(int batch, int block_len, const int32_t* draft, const float* margin, float tau,
+                             const fpd_vocab_layout* layout, const int8_t* rule, int32_t pad_id, int32_t* accept_len,
+                             int32_t* committed, int32_t* valid_out, void* stream);
 
 /* ---- multi-block speculative loop: the step between verification and the next block ----------------------
  * VFlash blog, "Method" (blocks are drafted and verified one after another until the sequence ends);

@@ -261,11 +261,49 @@ def constrain_argmax(model: Model, hidden, batch, block_len, layout=None, want_l
                                        _p(logits, _f64p), _p(margin, _f64p))
     if rc:
         raise ValueError("oracle_constrain_argmax: bad layout")
+    if layout is not None and len(layout.get("pairs", ())) and logits is None:
+        return constrain_argmax(model, hidden, batch, block_len, layout, want_logits=True)[:2] + (None,)
+    if layout is not None and len(layout.get("pairs", ())):
+        _pair_offscreen(tokens, margin, logits, block_len, layout["pairs"], int(layout["off_id"]))
     return tokens, margin, logits
 
 
-def verify(mode, draft, target=None, layout=None, rule=None, pad_id=-1):
-    """mode 0 = text, 1 = schema.  Returns (accept_len [B], committed [B, L], valid [B])."""
+def _pair_offscreen(tokens, margin, logits, block_len, pairs, off_id):
+    """VFlash paper (zh) §2.5, the cross-position rule on the computed logits: the two positions of a pair take the
+    off-screen id together or not at all.  The decision compares o_p + o_q with a_p + a_q (a = the best legal logit
+    other than off_id, o = off_id's logit), taken like the argmax in fp32 (reading R16); ties stay on screen."""
+    P = block_len - 1
+    f32 = np.float32
+    for b in range(tokens.shape[0]):
+        for p, q in np.asarray(pairs).reshape(-1, 2):
+            rows = (b * P + int(p) - 1, b * P + int(q) - 1)
+            best, offl = [], []
+            for r in rows:
+                lg = logits[r].astype(np.float32)          # fp32 decision values; illegal ids are NaN
+                o = lg[off_id]
+                lg = lg.copy()
+                lg[off_id] = np.nan
+                if np.all(np.isnan(lg)):
+                    best = None
+                    break
+                i = int(np.nanargmax(lg))                  # the lowest id among equal maxima
+                best.append((i, lg[i]))
+                offl.append(o)
+            if best is None:
+                continue
+            on = f32(f32(best[0][1]) + f32(best[1][1]))
+            off = f32(f32(offl[0]) + f32(offl[1]))
+            take_off = bool(off > on)
+            for k, r in enumerate(rows):
+                tokens.reshape(-1)[r] = off_id if take_off else best[k][0]
+                margin[r] = min(margin[r], abs(float(off) - float(on)))
+
+
+def verify(mode, draft, target=None, layout=None, rule=None, pad_id=-1, margin=None, tau=None):
+    """mode 0 = text, 1 = schema, 2 = schema + confidence (prefix-k).  Returns (accept_len [B], committed [B, L],
+    valid [B])."""
+    if mode == 2:
+        return _verify_prefix(draft, layout, rule, pad_id, margin, tau)
     draft = _c(draft, np.int32)
     B, P = draft.shape
     L = P + 1
@@ -341,3 +379,27 @@ def grid_to_text(committed, accept, digit_ids, plus_id, minus_id, pad_id, n_axes
             w += 1
         texts.append(point_sep.join(points))
     return texts
+
+
+def _verify_prefix(draft, layout, rule, pad_id, margin, tau):
+    """VFlash paper (zh) §2.5: the first k draft positions are kept; for bounding boxes k stops before the first
+    uncertain coordinate.  Reading: a position whose rule is 4 (confident) is uncertain when the drafter's top-2
+    margin there is below tau.  The first failing position p is the earlier of the schema's (mode 1) and the first
+    uncertain one; k = p - 1."""
+    draft = _c(draft, np.int32)
+    B, P = draft.shape
+    L = P + 1
+    rl = np.broadcast_to(rule, (B, L)) if np.asarray(rule).ndim == 1 else np.asarray(rule)
+    acc, com, val = verify(1, draft, layout=layout, rule=rl, pad_id=pad_id)
+    mg = np.asarray(margin, dtype=np.float64).reshape(B, P)
+    for b in range(B):
+        p = int(acc[b]) + 1                       # the schema's first failing position (L when none)
+        for j in range(1, p):
+            if rl[b, j] == 4 and not (mg[b, j - 1] >= tau):
+                p = j
+                break
+        acc[b] = p - 1
+        com[b, :p - 1] = draft[b, :p - 1]
+        com[b, p - 1:] = -1
+        val[b] = int(p == L)
+    return acc, com, val

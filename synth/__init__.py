@@ -29,7 +29,7 @@ import numpy as np
 
 __all__ = [
     "ModelShape", "CONFIGS", "f32_to_bf16_bits", "bf16_bits_to_f32", "make_weights", "make_features",
-    "make_kv_store", "layout_special_tokens", "layout_fixed_width", "make_target_rows", "Workload",
+    "make_kv_store", "layout_special_tokens", "layout_fixed_width", "layout_bbox", "make_target_rows", "Workload",
     "make_workload",
 ]
 
@@ -165,7 +165,7 @@ def make_kv_store(shape: ModelShape, batch: int, t_cap: int, seed: int) -> np.nd
 
 
 def layout_special_tokens(vocab: int, n_waypoints: int = 64, coord_lo: int = 150000, n_coord: int = 1001,
-                          delim_id: int = 151100, start_id: int = 151101) -> dict:
+                          delim_id: int = 151100, start_id: int = 151101, off_id: int | None = None) -> dict:
     """Primitive block with dedicated coordinate tokens: start token, then per waypoint
     [u, v (image), X, Y, Z (metric), delimiter].  All five coordinates share one contiguous slice of
     n_coord ids; the delimiter slot admits one id.  Class 0 = coordinate slice, class 1 = delimiter,
@@ -179,6 +179,38 @@ def layout_special_tokens(vocab: int, n_waypoints: int = 64, coord_lo: int = 150
         pos_class[base:base + 5] = 0
         pos_class[base + 5] = 1
         rule[base:base + 6] = 1
+    pos_class[0] = 2
+    class_off = np.array([0, 1, 2, 3], dtype=np.int32)
+    class_ranges = np.array([coord_lo, coord_lo + n_coord, delim_id, delim_id + 1, 0, vocab], dtype=np.int32)
+    lay = dict(block_len=L, pos_class=pos_class, rule=rule, class_off=class_off, class_ranges=class_ranges,
+               pad_id=-1, start_id=start_id)
+    if off_id is not None:
+        # the image coordinates (u, v) of every waypoint may also be off screen, together (class 3 = slice + off)
+        assert off_id >= coord_lo + n_coord
+        for w in range(n_waypoints):
+            pos_class[1 + 6 * w:3 + 6 * w] = 3
+        lay["class_off"] = np.array([0, 1, 2, 3, 5], dtype=np.int32)
+        lay["class_ranges"] = np.concatenate([class_ranges, [coord_lo, coord_lo + n_coord, off_id, off_id + 1]]
+                                             ).astype(np.int32)
+        lay["pairs"] = np.array([(1 + 6 * w, 2 + 6 * w) for w in range(n_waypoints)], dtype=np.int16)
+        lay["off_id"] = int(off_id)
+    return lay
+
+
+def layout_bbox(vocab: int, n_boxes: int = 16, coord_lo: int = 150000, n_coord: int = 1001, delim_id: int = 151100,
+                start_id: int = 151101) -> dict:
+    """Bounding-box primitive: start token, then per box [x1, y1, x2, y2, delimiter], coordinates from the
+    n_coord-id slice.  Coordinates carry the confidence rule (4): prefix acceptance stops before the first
+    coordinate the drafter is unsure of; delimiters must be members."""
+    L = 1 + 5 * n_boxes
+    pos_class = np.zeros(L, dtype=np.int16)
+    rule = np.zeros(L, dtype=np.int8)
+    for k in range(n_boxes):
+        base = 1 + 5 * k
+        pos_class[base:base + 4] = 0
+        rule[base:base + 4] = 4
+        pos_class[base + 4] = 1
+        rule[base + 4] = 1
     pos_class[0] = 2
     class_off = np.array([0, 1, 2, 3], dtype=np.int32)
     class_ranges = np.array([coord_lo, coord_lo + n_coord, delim_id, delim_id + 1, 0, vocab], dtype=np.int32)
