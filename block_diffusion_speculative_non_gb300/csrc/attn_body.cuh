@@ -55,6 +55,14 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// 2^x on the special-function unit (ex2.approx, flush-to-zero): relative error near 2^-22 for the arguments used
+// here (<= 0), and 2^-inf = 0 for masked keys.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Tile of rows x H bf16 in shared memory; 16-byte chunk c of row r lives at chunk c ^ (r & 7).
 template <int H>
 __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
@@ -95,34 +103,39 @@ __device__ __forceinline__ void attn_tile_math(uint32_t ks, uint32_t vs, const u
     }
   }
   // ---- online softmax (base 2) ----
-  float mx0 = -INFINITY, mx1 = -INFINITY;
+  if (k0 + KT > k_end) {   // a partial tile (warp-uniform): keys past the end get 2^-inf = 0
+#pragma unroll
+    for (int n = 0; n < KT / 8; n++) {
+      const int key = k0 + n * 8 + (lane & 3) * 2;
+      if (key >= k_end) s[n][0] = s[n][2] = -INFINITY;
+      if (key + 1 >= k_end) s[n][1] = s[n][3] = -INFINITY;
+    }
+  }
+  float mx0 = -INFINITY, mx1 = -INFINITY;   // raw maxima, scaled once below (sl2 > 0)
 #pragma unroll
   for (int n = 0; n < KT / 8; n++) {
-    const int key = k0 + n * 8 + (lane & 3) * 2;
-    const bool v0 = key < k_end, v1 = key + 1 < k_end;
-    s[n][0] = v0 ? s[n][0] * sl2 : -INFINITY;
-    s[n][1] = v1 ? s[n][1] * sl2 : -INFINITY;
-    s[n][2] = v0 ? s[n][2] * sl2 : -INFINITY;
-    s[n][3] = v1 ? s[n][3] * sl2 : -INFINITY;
     mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
     mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
   }
+  mx0 *= sl2;
+  mx1 *= sl2;
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
   const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: every tile holds at least one valid key
-  const float c0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mn0);
-  const float c1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mn1);
+  const float c0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mn0);
+  const float c1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mn1);
   m0 = mn0;
   m1 = mn1;
   float ps0 = 0.f, ps1 = 0.f;
+  const float n0 = -mn0, n1 = -mn1;
 #pragma unroll
   for (int n = 0; n < KT / 8; n++) {
-    s[n][0] = exp2f(s[n][0] - mn0);
-    s[n][1] = exp2f(s[n][1] - mn0);
-    s[n][2] = exp2f(s[n][2] - mn1);
-    s[n][3] = exp2f(s[n][3] - mn1);
+    s[n][0] = ex2_approx(fmaf(s[n][0], sl2, n0));
+    s[n][1] = ex2_approx(fmaf(s[n][1], sl2, n0));
+    s[n][2] = ex2_approx(fmaf(s[n][2], sl2, n1));
+    s[n][3] = ex2_approx(fmaf(s[n][3], sl2, n1));
     ps0 += s[n][0] + s[n][1];
     ps1 += s[n][2] + s[n][3];
   }

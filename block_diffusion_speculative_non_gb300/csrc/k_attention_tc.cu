@@ -322,12 +322,16 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
 #pragma unroll
       for (int c0 = 0; c0 < AKT; c0 += 32) tmem_ld32_nowait(st + c0, sv + c0);
       tmem_wait_ld();
-      float mx = -INFINITY;
+      if (valid < AKT) {   // a partial tile (warp-uniform): keys past the last valid one get 2^-inf = 0
 #pragma unroll
-      for (int e = 0; e < AKT; e++) {
-        sv[e] = e < valid ? sv[e] * sl2 : -INFINITY;
-        mx = fmaxf(mx, sv[e]);
+        for (int e = 0; e < AKT; e++)
+          if (e >= valid) sv[e] = -INFINITY;
       }
+      // raw row maximum in four independent chains, scaled once (sl2 > 0)
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int e = 0; e < AKT; e++) mq[e & 3] = fmaxf(mq[e & 3], sv[e]);
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
       const bool need = mx > m_ref + kRescaleLog2;
       if (__any_sync(0xffffffffu, need)) {   // tcgen05.ld/st are warp-wide: every lane takes part
         // O may only be rescaled once every product into it (up to tile i - 1) has finished
@@ -350,18 +354,22 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
       }
       // p = 2^(s - m_ref) (0 for masked keys) as hi + lo bf16 terms over the S columns just read:
       // hi at columns [0, 64), lo at [64, 128) of the buffer, two keys per 32-bit column
+      const float nm = -m_ref;
+      float lq[2] = {0.f, 0.f};   // two chains of the running sum, combined in a fixed order
 #pragma unroll
       for (int c0 = 0; c0 < AKT; c0 += 32) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2(sv[c0 + e] - m_ref), p1 = ex2(sv[c0 + e + 1] - m_ref);
-          l += p0 + p1;
+          const float p0 = ex2(fmaf(sv[c0 + e], sl2, nm)), p1 = ex2(fmaf(sv[c0 + e + 1], sl2, nm));
+          lq[0] += p0;
+          lq[1] += p1;
           split_bf16x2(p0, p1, hi[e / 2], lo[e / 2]);
         }
         tmem_st16(st + c0 / 2, hi);
         tmem_st16(st + AKT / 2 + c0 / 2, lo);
       }
+      l += lq[0] + lq[1];
       tmem_wait_st();
       tc::tc_fence_before();
       __syncwarp();

@@ -56,6 +56,13 @@ def _compare_store(dr, kv_ref, ctx_len, batch):
     return n
 
 
+def _stagewise(dr, kv_ref, ctx_len, batch):
+    """Reading R21: the store the GPU prepared is checked against the oracle's preparation, and the block pass is
+    then compared with the oracle run on the GPU's store (each call given the same inputs)."""
+    _compare_store(dr, kv_ref, ctx_len, batch)
+    return bits_of(dr.kv_view(batch))
+
+
 def _draft_and_compare(pkg, orc, dr, om, kv_ref, t_cap, ctx_len, anchor, mask_id, L, batch, layout=None,
                        requests=None):
     """GPU draft + argmax over the whole batch; oracle on `requests` (default all); returns gpu tokens.  kv_ref is
@@ -113,7 +120,8 @@ def test_tiny_text_end_to_end(pkg, orc):
     w = synth.make_weights(s, wl.seed)
     dr, om, kv, _ = _prepare_both(pkg, orc, s, w, wl.row_off, wl.t_cap, wl.block_len, wl.batch, wl.seed + 1)
     assert _compare_store(dr, kv, wl.ctx_len, wl.batch) == 1
-    toks, _ = _draft_and_compare(pkg, orc, dr, om, kv, wl.t_cap, wl.ctx_len, wl.anchor, wl.mask_id, wl.block_len,
+    kv_g = _stagewise(dr, kv, wl.ctx_len, wl.batch)
+    toks, _ = _draft_and_compare(pkg, orc, dr, om, kv_g, wl.t_cap, wl.ctx_len, wl.anchor, wl.mask_id, wl.block_len,
                                  wl.batch)
     # verify against geometric target rows built from the GPU ids; bit-exact given the ids
     target, g = synth.make_target_rows(toks, s.vocab, wl.geo_p, wl.seed + 2)
@@ -143,7 +151,8 @@ def test_tiny_ragged_batch_with_append(pkg, orc):
     kv = orc.prepare_context(om, off2, f2, t_cap, batch=B, pos_start=lens1, kv_store=kv)
     _compare_store(dr, kv, ctx_len, B)
     anchor = np.array([5, 6, 7, 4000], np.int32)
-    _draft_and_compare(pkg, orc, dr, om, kv, t_cap, ctx_len, anchor, s.vocab - 1, L, B)
+    kv_g = _stagewise(dr, kv, ctx_len, B)
+    _draft_and_compare(pkg, orc, dr, om, kv_g, t_cap, ctx_len, anchor, s.vocab - 1, L, B)
     dr.close()
 
 
@@ -155,7 +164,8 @@ def test_tiny_few_token_batch_ragged(pkg, orc):
     off = np.concatenate([[0], np.cumsum(ctx_len)]).astype(np.int32)
     B, L = 3, 5
     dr, om, kv, _ = _prepare_both(pkg, orc, s, w, off, int(ctx_len.max()), L, B, 4243)
-    _draft_and_compare(pkg, orc, dr, om, kv, int(ctx_len.max()), ctx_len, np.array([3, 4000, 77], np.int32),
+    kv_g = _stagewise(dr, kv, ctx_len, B)
+    _draft_and_compare(pkg, orc, dr, om, kv_g, int(ctx_len.max()), ctx_len, np.array([3, 4000, 77], np.int32),
                        s.vocab - 1, L, B)
     dr.close()
 
@@ -168,7 +178,8 @@ def test_tiny_degenerate_blocks(pkg, orc, L, ctx):
     t_cap = max(ctx, 1)
     off = np.array([0, ctx], np.int32)
     dr, om, kv, _ = _prepare_both(pkg, orc, s, w, off, t_cap, L, 1, 98)
-    _draft_and_compare(pkg, orc, dr, om, kv, t_cap, np.array([ctx], np.int32), np.array([17], np.int32),
+    kv_g = _stagewise(dr, kv, np.array([ctx], np.int32), 1)
+    _draft_and_compare(pkg, orc, dr, om, kv_g, t_cap, np.array([ctx], np.int32), np.array([17], np.int32),
                        s.vocab - 1, L, 1)
     dr.close()
 
@@ -182,7 +193,8 @@ def test_tiny_special_token_primitive(pkg, orc):
     L = lay["block_len"]
     T = 200
     dr, om, kv, _ = _prepare_both(pkg, orc, s, w, np.array([0, T], np.int32), T, L, 1, 556)
-    toks, _ = _draft_and_compare(pkg, orc, dr, om, kv, T, np.array([T], np.int32), np.array([3101], np.int32),
+    kv_g = _stagewise(dr, kv, np.array([T], np.int32), 1)
+    toks, _ = _draft_and_compare(pkg, orc, dr, om, kv_g, T, np.array([T], np.int32), np.array([3101], np.int32),
                                  s.vocab - 1, L, 1, layout=lay)
     lay_d, rule_d = pkg.Drafter.layout(lay, 1, L, DEV)
     acc, com, val = dr.verify_schema(1, L, dev_i32(toks), lay_d, rule_d, -1)
@@ -201,7 +213,8 @@ def test_tiny_fixed_width_primitive_batch(pkg, orc):
     B = 4
     dr, om, kv, _ = _prepare_both(pkg, orc, s, w, off, int(ctx_len.max()), L, B, 778)
     anchor = np.full(B, lay["start_id"], np.int32)
-    toks, _ = _draft_and_compare(pkg, orc, dr, om, kv, int(ctx_len.max()), ctx_len, anchor, s.vocab - 1, L, B,
+    kv_g = _stagewise(dr, kv, ctx_len, B)
+    toks, _ = _draft_and_compare(pkg, orc, dr, om, kv_g, int(ctx_len.max()), ctx_len, anchor, s.vocab - 1, L, B,
                                  layout=lay)
     lay_d, rule_d = pkg.Drafter.layout(lay, B, L, DEV)
     acc, com, val = dr.verify_schema(B, L, dev_i32(toks), lay_d, rule_d, lay["pad_id"])
