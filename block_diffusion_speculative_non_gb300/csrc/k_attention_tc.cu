@@ -1,25 +1,28 @@
 // k_attention_tc.cu — a5 for long blocks on the 5th-generation tensor cores: bidirectional grouped-query attention
-// of 128 query rows of one (request, kv head) over [context K/V ; block K/V], head dim 128.
+// of query tiles of one (request, kv head) over [context K/V ; block K/V], head dim 128.
 //
 // VFlash paper (zh) §2.1: the fused target features enter every drafter layer as keys and values and the block is
 // predicted in one bidirectional pass, so there is no mask inside a request.  At primitive lengths (L = 381, 385)
 // the attention is a dense contraction: 4 (T + L) L h flops per head, about a quarter of the block's flops, so it
 // runs on tcgen05 with the accumulators in tensor memory.
 //
-// One CTA = 128 query rows (L positions x the q heads of one kv head, row r = position * group + head) x one KV
-// split.  Warps:
-//   0      TMA producer: K and V tiles of 128 keys (two 64-dim boxes each, 128-byte swizzle) into 3-slot rings;
-//   1      MMA issuer: S_i = Q K_i^T (M = 128 rows, N = 128 keys, bf16, fp32 into one of two TMEM buffers), then
-//          O += P_{i-1} V_{i-1} with P read from tensor memory and V as an MN-major shared-memory operand;
-//   2..5   softmax, one thread per query row (= TMEM lane): the whole S row in registers, row maximum,
-//          p = 2^(s log2e/sqrt(h) - m), written back over its own S buffer as two bf16 terms p = hi + lo
-//          (split_bf16x2); both terms multiply V, so the second product sees p to about 2^-17 relative instead
-//          of bf16's 2^-9 and needs no operand conversion.  O in TMEM is rescaled only when
-//          the row maximum rises by more than 2^8 over the reference (p then stays below 2^8), so O / l is exact;
-//   6      clears the V rows past the last valid key of a partial tile (p = 0 there, and 0 x a stale non-finite
+// One CTA = two query tiles of 128 rows (row r of a tile = position * group + head within the kv head's rows) x
+// one KV split; both tiles share every K/V tile.  Warps:
+//   0      TMA producer: K and V tiles of 128 keys (two 64-dim boxes each, 128-byte swizzle) into 2-slot rings;
+//   1      MMA issuer: S_t = Q_t K_i^T for tile t = 0, 1 (M = 128 rows, N = 128 keys, fp32 into t's TMEM buffer),
+//          and O_t += (P_hi + P_lo)_t V_i with P read from tensor memory and V as an MN-major shared-memory operand;
+//          it issues S_t for the next key tile right after O_t's product, so each warpgroup waits only for its
+//          own tile's MMAs;
+//   2..5   softmax of tile 0, 6..9 softmax of tile 1, one thread per query row (= TMEM lane): the row maximum from
+//          a first pass over S, then p = 2^(s log2e/sqrt(h) - m) written back over S 32 keys at a time as two bf16
+//          terms (split_bf16x2; hi at columns [32c, 32c + 16), lo at [32c + 16, 32c + 32) for keys 32c..32c + 31,
+//          so each chunk overwrites only the S columns it has just read); O in TMEM is rescaled only when the row
+//          maximum rises by more than 2^8 over the reference (p then stays below 2^8), so O / l is exact;
+//   10     clears the V rows past the last valid key of a partial tile (p = 0 there, and 0 x a stale non-finite
 //          value would still be NaN).
-// The tensor core runs the products of one thread in issue order, so S_{i+2} may overwrite P_i's buffer as soon as
-// O += P_i V_i has been issued: no barrier guards that reuse.
+// Two softmax warps share each SM sub-partition, so one hides the other's load and exponent latency, and each
+// K/V tile is loaded once for 256 query rows.  The tensor core runs one thread's products in issue order, so
+// S_t for key tile i + 1 may overwrite P_t of tile i as soon as that product has been issued.
 // With one split the CTA writes O / l as bf16; with several it writes the unnormalised partial (o, m, l) that the
 // merge kernel of k_attention.cu combines in split order.  Every mbarrier wait is bounded (tc::mbar_wait).
 #include <cstring>
@@ -32,29 +35,30 @@ namespace fpd {
 namespace {
 
 constexpr int AQ = 128, AKT = 128, AH = 128;
-constexpr int kAThreads = 224;
-constexpr int NSTAGE = 3;
+constexpr int NQT = 2;                     // query tiles per CTA, one softmax warpgroup each
+constexpr int kAThreads = 11 * 32;
+constexpr int NSTAGE = 2;
 constexpr int TILE_BYTES = AKT * AH * 2;   // 32 KB: 128 rows x 128 dims, two 64-dim swizzle atoms
 constexpr int ATOM_BYTES = TILE_BYTES / 2;
-// shared memory: Q | K[3] | V[3] | barriers
-constexpr int SM_Q = 0, SM_K = TILE_BYTES, SM_V = (1 + NSTAGE) * TILE_BYTES, SM_BAR = (1 + 2 * NSTAGE) * TILE_BYTES;
-// barriers: q_ready, k_full[3], k_empty[3], v_full[3], v_empty[3], v_ready[3] (stale rows cleared), s_full[2],
-// p_full[2], pv_done[2] (the O += P V that read TMEM buffer b)
+// shared memory: Q[2] | K[2] | V[2] | barriers
+constexpr int SM_Q = 0, SM_K = NQT * TILE_BYTES, SM_V = SM_K + NSTAGE * TILE_BYTES, SM_BAR = SM_V + NSTAGE * TILE_BYTES;
+// barriers: q_ready[tile], k_full[slot], k_empty[slot], v_full[slot], v_empty[slot], v_ready[slot] (stale rows
+// cleared), s_full[tile], p_full[tile], pv_done[tile]
 enum {
   B_Q = 0,
-  B_KF = 1,
+  B_KF = B_Q + NQT,
   B_KE = B_KF + NSTAGE,
   B_VF = B_KE + NSTAGE,
   B_VE = B_VF + NSTAGE,
   B_VR = B_VE + NSTAGE,
   B_SF = B_VR + NSTAGE,
-  B_PF = B_SF + 2,
-  B_PV = B_PF + 2,
-  B_N = B_PV + 2
+  B_PF = B_SF + NQT,
+  B_PV = B_PF + NQT,
+  B_N = B_PV + NQT
 };
-constexpr size_t kASmem = 1024 + (1 + 2 * NSTAGE) * TILE_BYTES + 8 * B_N + 16;
+constexpr size_t kASmem = 1024 + (size_t)SM_BAR + 8 * B_N + 16;
 static_assert(kASmem <= 232448, "attention tile set exceeds the shared memory of one CTA");
-constexpr int kTmemCols = 512;   // S/P[0] at 0, S/P[1] at 128, O at 256
+constexpr int kTmemCols = 512;   // S/P of tile t at 128 t, O of tile t at 256 + 128 t
 constexpr uint32_t kTmemO = 256;
 constexpr float kRescaleLog2 = 8.f;
 
@@ -170,23 +174,23 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
   const uint32_t bar0 = tc::smem_u32(bars);
   auto bar = [&](int i) { return bar0 + 8 * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, bg = blockIdx.y, split = blockIdx.z;
+  const int qp = blockIdx.x, bg = blockIdx.y, split = blockIdx.z;
   const int b = bg / p.nkv, g = bg % p.nkv, grp = p.nq / p.nkv, nrows = p.L * grp;
 
   pdl_trigger();
   if (threadIdx.x == 0) {
-    tc::mbar_init(bar(B_Q), 1);
+    for (int t = 0; t < NQT; t++) {
+      tc::mbar_init(bar(B_Q + t), 1);
+      tc::mbar_init(bar(B_SF + t), 1);
+      tc::mbar_init(bar(B_PF + t), 4);
+      tc::mbar_init(bar(B_PV + t), 1);
+    }
     for (int s = 0; s < NSTAGE; s++) {
       tc::mbar_init(bar(B_KF + s), 1);
       tc::mbar_init(bar(B_KE + s), 1);
       tc::mbar_init(bar(B_VF + s), 1);
       tc::mbar_init(bar(B_VE + s), 1);
       tc::mbar_init(bar(B_VR + s), 1);
-    }
-    for (int s = 0; s < 2; s++) {
-      tc::mbar_init(bar(B_SF + s), 1);
-      tc::mbar_init(bar(B_PF + s), 4);
-      tc::mbar_init(bar(B_PV + s), 1);
     }
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -204,8 +208,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
   pdl_wait();   // q, block K/V and the context store come from earlier kernels
 
-  int T = p.ctx_len[b];
-  T = clamp_ctx(T, p.t_cap);
+  const int T = clamp_ctx(p.ctx_len[b], p.t_cap);
   const int n_keys = T + p.L;
   TileList tl;
   tl.init(T, min(n_keys, split * p.chunk), min(n_keys, (split + 1) * p.chunk));
@@ -246,96 +249,116 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(AQ, AKT, 0);   // Q x K, both K-major in shared memory
       constexpr uint32_t id_o = idesc_bf16(AQ, AH, 1);    // P (TMEM) x V (MN-major in shared memory)
-      const uint32_t qs = tc::smem_u32(smem + SM_Q);
-      if (!tc::mbar_wait(bar(B_Q), 0)) *abort_flag = 1;
+      for (int t = 0; t < NQT; t++)
+        if (!tc::mbar_wait(bar(B_Q + t), 0)) *abort_flag = 1;
       tc::tc_fence_after();
-      auto pv = [&](int i) {   // O += (P_hi + P_lo)_i V_i
-        const int s = i % NSTAGE, pb = i & 1;
-        const uint32_t ph = (i / NSTAGE) & 1;
-        if (!tc::mbar_wait(bar(B_PF + pb), (i >> 1) & 1) || !tc::mbar_wait(bar(B_VF + s), ph) ||
-            !tc::mbar_wait(bar(B_VR + s), ph)) {
-          *abort_flag = 1;
-          return;
-        }
-        tc::tc_fence_after();
-        const uint32_t vs = tc::smem_u32(smem + SM_V + s * TILE_BYTES);
-        const uint32_t pt = tmem + pb * AKT;
-#pragma unroll
-        for (int kk = 0; kk < AKT / 16; kk++) {
-          const uint64_t db = sw128_mn_desc(vs + kk * 16 * 128, ATOM_BYTES);
-          umma_ts_bf16(tmem + kTmemO, pt + kk * 8, db, id_o, (i > 0 || kk > 0) ? 1u : 0u);
-          umma_ts_bf16(tmem + kTmemO, pt + AKT / 2 + kk * 8, db, id_o, 1u);
-        }
-        tc::umma_commit(bar(B_PV + pb));
-        tc::umma_commit(bar(B_VE + s));
-      };
-      for (int i = 0; i < n_tiles && !*abort_flag; i++) {
-        const int s = i % NSTAGE, sb = i & 1;
-        if (!tc::mbar_wait(bar(B_KF + s), (i / NSTAGE) & 1)) { *abort_flag = 1; break; }
-        tc::tc_fence_after();
-        // buffer sb last held P_{i-2}, whose product was issued before this one
-        const uint32_t ks = tc::smem_u32(smem + SM_K + s * TILE_BYTES);
+      auto issue_s = [&](int t, int i) {   // S_t = Q_t K_i^T into tile t's buffer
+        const uint32_t qs = tc::smem_u32(smem + SM_Q + t * TILE_BYTES);
+        const uint32_t ks = tc::smem_u32(smem + SM_K + (i % NSTAGE) * TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < AH / 16; kk++) {
           const uint64_t da = tc::sw128_kmajor_desc(qs + (kk >> 2) * ATOM_BYTES + (kk & 3) * 32);
           const uint64_t db = tc::sw128_kmajor_desc(ks + (kk >> 2) * ATOM_BYTES + (kk & 3) * 32);
-          tc::umma_bf16(tmem + sb * AKT, da, db, id_s, kk > 0 ? 1u : 0u);
+          tc::umma_bf16(tmem + t * AKT, da, db, id_s, kk > 0 ? 1u : 0u);
         }
-        tc::umma_commit(bar(B_SF + sb));
-        tc::umma_commit(bar(B_KE + s));
-        if (i >= 1) pv(i - 1);
+        tc::umma_commit(bar(B_SF + t));
+      };
+      auto wait_k = [&](int i) {
+        if (!tc::mbar_wait(bar(B_KF + i % NSTAGE), (i / NSTAGE) & 1)) { *abort_flag = 1; return false; }
+        tc::tc_fence_after();
+        return true;
+      };
+      auto issue_pv = [&](int t, int i) {   // O_t += (P_hi + P_lo)_t V_i
+        const int s = i % NSTAGE;
+        const uint32_t ph = (i / NSTAGE) & 1;
+        if (!tc::mbar_wait(bar(B_PF + t), i & 1) || !tc::mbar_wait(bar(B_VF + s), ph) ||
+            !tc::mbar_wait(bar(B_VR + s), ph)) {
+          *abort_flag = 1;
+          return false;
+        }
+        tc::tc_fence_after();
+        const uint32_t vs = tc::smem_u32(smem + SM_V + s * TILE_BYTES);
+        const uint32_t pt = tmem + t * AKT;
+#pragma unroll
+        for (int kk = 0; kk < AKT / 16; kk++) {
+          // keys 16 kk .. 16 kk + 15: chunk kk / 2, half kk % 2 -> hi at 32 c + 8 h, lo at 32 c + 16 + 8 h
+          const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+          const uint64_t db = sw128_mn_desc(vs + kk * 16 * 128, ATOM_BYTES);
+          umma_ts_bf16(tmem + kTmemO + t * AH, pt + col, db, id_o, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_bf16(tmem + kTmemO + t * AH, pt + col + 16, db, id_o, 1u);
+        }
+        tc::umma_commit(bar(B_PV + t));
+        if (t == NQT - 1) tc::umma_commit(bar(B_VE + s));
+        return true;
+      };
+      if (n_tiles > 0 && wait_k(0)) {
+        for (int t = 0; t < NQT; t++) issue_s(t, 0);
+        tc::umma_commit(bar(B_KE + 0));
       }
-      if (n_tiles > 0 && !*abort_flag) pv(n_tiles - 1);
+      // each tile's next S follows its own product, so one warpgroup never waits for the other's softmax
+      for (int i = 0; i < n_tiles && !*abort_flag; i++) {
+        const bool more = i + 1 < n_tiles;
+        if (!issue_pv(0, i)) break;
+        if (more && !wait_k(i + 1)) break;
+        if (more) issue_s(0, i + 1);
+        if (!issue_pv(1, i)) break;
+        if (more) {
+          issue_s(1, i + 1);
+          tc::umma_commit(bar(B_KE + (i + 1) % NSTAGE));
+        }
+      }
     }
-  } else if (warp < 6) {
-    // ---------------- softmax: thread = query row = TMEM lane ----------------
-    const int quarter = warp & 3, r = quarter * 32 + lane;
-    const int qi = qt * AQ + r;
+  } else if (warp < 2 + 4 * NQT) {
+    // ---------------- softmax of tile t: thread = query row = TMEM lane ----------------
+    const int t = (warp - 2) >> 2, quarter = warp & 3, r = quarter * 32 + lane;
+    const int qi = (qp * NQT + t) * AQ + r;
     const bool row_ok = qi < nrows;
     const int j = row_ok ? qi / grp : 0, head = g * grp + (row_ok ? qi % grp : 0);
     // Q row r -> shared memory (K-major, 128-byte swizzle: chunk c of row r at c ^ (r & 7))
     {
+      uint8_t* qs = smem + SM_Q + t * TILE_BYTES;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.L + j) * p.nq + head) * AH);
       uint4 u[16];
 #pragma unroll
       for (int c = 0; c < 16; c++) u[c] = row_ok ? src[c] : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int c = 0; c < 16; c++)
-        *reinterpret_cast<uint4*>(smem + SM_Q + (c >> 3) * ATOM_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = u[c];
+        *reinterpret_cast<uint4*>(qs + (c >> 3) * ATOM_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = u[c];
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      named_bar(1, 128);
-      if (r == 0) tc::mbar_arrive(bar(B_Q));
+      named_bar(1 + t, 128);
+      if (r == 0) tc::mbar_arrive(bar(B_Q + t));
     }
     const float sl2 = rsqrtf((float)AH) * 1.4426950408889634f;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t st = tmem + lane_off + t * AKT, ot = tmem + lane_off + kTmemO + t * AH;
     float m_ref = -INFINITY, l = 0.f;
     for (int i = 0; i < n_tiles && !*abort_flag; i++) {
-      const int sb = i & 1;
       int first, valid;
       bool ctx;
       tl.tile(i, first, valid, ctx);
-      if (!tc::mbar_wait(bar(B_SF + sb), (i >> 1) & 1)) *abort_flag = 1;
+      if (!tc::mbar_wait(bar(B_SF + t), i & 1)) *abort_flag = 1;
       tc::tc_fence_after();
-      // the whole S row in registers (four 32-column loads, one wait)
-      const uint32_t st = tmem + lane_off + sb * AKT;
-      float sv[AKT];
-#pragma unroll
-      for (int c0 = 0; c0 < AKT; c0 += 32) tmem_ld32_nowait(st + c0, sv + c0);
-      tmem_wait_ld();
-      if (valid < AKT) {   // a partial tile (warp-uniform): keys past the last valid one get 2^-inf = 0
-#pragma unroll
-        for (int e = 0; e < AKT; e++)
-          if (e >= valid) sv[e] = -INFINITY;
-      }
-      // raw row maximum in four independent chains, scaled once (sl2 > 0)
+      // pass 1: the row maximum of the raw scores (keys past `valid` excluded), scaled once (sl2 > 0)
       float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < AKT; e++) mq[e & 3] = fmaxf(mq[e & 3], sv[e]);
+      for (int h = 0; h < AKT; h += 64) {
+        float sv[64];
+        tmem_ld32_nowait(st + h, sv);
+        tmem_ld32_nowait(st + h + 32, sv + 32);
+        tmem_wait_ld();
+        if (valid < AKT) {   // a partial tile (warp-uniform)
+#pragma unroll
+          for (int e = 0; e < 64; e++)
+            if (h + e >= valid) sv[e] = -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < 64; e++) mq[e & 3] = fmaxf(mq[e & 3], sv[e]);
+      }
       const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
       const bool need = mx > m_ref + kRescaleLog2;
       if (__any_sync(0xffffffffu, need)) {   // tcgen05.ld/st are warp-wide: every lane takes part
-        // O may only be rescaled once every product into it (up to tile i - 1) has finished
-        if (i >= 1 && !tc::mbar_wait(bar(B_PV + ((i - 1) & 1)), ((i - 1) >> 1) & 1)) *abort_flag = 1;
+        // O_t may only be rescaled once every product into it (up to key tile i - 1) has finished
+        if (i >= 1 && !tc::mbar_wait(bar(B_PV + t), (i - 1) & 1)) *abort_flag = 1;
         tc::tc_fence_after();
         const float m_new = need ? mx : m_ref;
         const float cf = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
@@ -343,47 +366,55 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
 #pragma unroll 1
           for (int c0 = 0; c0 < AH; c0 += 16) {
             float o[16];
-            tc::tmem_ld16(tmem + lane_off + kTmemO + c0, o);
+            tc::tmem_ld16(ot + c0, o);
 #pragma unroll
             for (int e = 0; e < 16; e++) o[e] *= cf;
-            tmem_st16(tmem + lane_off + kTmemO + c0, o);
+            tmem_st16(ot + c0, o);
           }
         }
         l *= cf;
         m_ref = m_new;
       }
-      // p = 2^(s - m_ref) (0 for masked keys) as hi + lo bf16 terms over the S columns just read:
-      // hi at columns [0, 64), lo at [64, 128) of the buffer, two keys per 32-bit column
+      // pass 2, 32 keys at a time: p = 2^(s sl2 - m_ref) (0 past `valid`) as hi + lo bf16 terms over the columns
+      // just read: hi at [32c, 32c + 16), lo at [32c + 16, 32c + 32), two keys per 32-bit column
       const float nm = -m_ref;
       float lq[2] = {0.f, 0.f};   // two chains of the running sum, combined in a fixed order
 #pragma unroll
       for (int c0 = 0; c0 < AKT; c0 += 32) {
+        float sv[32];
+        tmem_ld32_nowait(st + c0, sv);
+        tmem_wait_ld();
+        if (valid < c0 + 32) {
+#pragma unroll
+          for (int e = 0; e < 32; e++)
+            if (c0 + e >= valid) sv[e] = -INFINITY;
+        }
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2(fmaf(sv[c0 + e], sl2, nm)), p1 = ex2(fmaf(sv[c0 + e + 1], sl2, nm));
+          const float p0 = ex2(fmaf(sv[e], sl2, nm)), p1 = ex2(fmaf(sv[e + 1], sl2, nm));
           lq[0] += p0;
           lq[1] += p1;
           split_bf16x2(p0, p1, hi[e / 2], lo[e / 2]);
         }
-        tmem_st16(st + c0 / 2, hi);
-        tmem_st16(st + AKT / 2 + c0 / 2, lo);
+        tmem_st16(st + c0, hi);
+        tmem_st16(st + c0 + 16, lo);
       }
       l += lq[0] + lq[1];
       tmem_wait_st();
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(bar(B_PF + sb));
+      if (lane == 0) tc::mbar_arrive(bar(B_PF + t));
     }
-    // epilogue: O / l (one split) or the partial (o, m, l)
-    if (n_tiles > 0 && !tc::mbar_wait(bar(B_PV + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1)) *abort_flag = 1;
+    // epilogue: O_t / l (one split) or the partial (o, m, l)
+    if (n_tiles > 0 && !tc::mbar_wait(bar(B_PV + t), (n_tiles - 1) & 1)) *abort_flag = 1;
     tc::tc_fence_after();
     const size_t orow = ((size_t)b * p.L + j) * p.nq + head;
 #pragma unroll 1
     for (int c0 = 0; c0 < AH; c0 += 16) {
       float o[16];
       if (n_tiles > 0) {
-        tc::tmem_ld16(tmem + lane_off + kTmemO + c0, o);
+        tc::tmem_ld16(ot + c0, o);
       } else {
 #pragma unroll
         for (int e = 0; e < 16; e++) o[e] = 0.f;
@@ -440,15 +471,27 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_tc_kernel(const __grid_cons
 
 bool attn_tc_supported(int head_dim, int L, int nq, int nkv) { return head_dim == AH && L * (nq / nkv) >= AQ; }
 
-// About one CTA per SM or more: split the keys only when the query tiles alone leave SMs idle.
+// One CTA per SM (the shared memory allows no second): the split count s minimises the waves times the key tiles a
+// CTA walks, ceil(base s / SMs) * ceil(keys / (s AKT)), plus the split's own cost;
+// ties go to fewer splits.  A split adds about two key tiles of work to each CTA: its fp32 partial row out, and the
+// merge pass that reads it back.
 void attn_tc_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* splits, int* chunk) {
-  const int q_tiles = ceil_div(L * (nq / nkv), AQ);
-  const int base = q_tiles * batch * nkv;
+  const int q_pairs = ceil_div(ceil_div(L * (nq / nkv), AQ), NQT);
+  const long base = (long)q_pairs * batch * nkv;
   const int max_keys = t_cap + L;
-  int s = base >= num_sms ? 1 : ceil_div(num_sms, base);
-  s = std::max(1, std::min(s, ceil_div(max_keys, AKT)));
-  s = std::min(s, 128);
-  const int ch = ceil_div(ceil_div(max_keys, s), AKT) * AKT;
+  const int key_tiles = ceil_div(max_keys, AKT);
+  const int s_max = std::max(1, std::min(key_tiles, 128));
+  int best_s = 1;
+  double best = 0.0;
+  for (int s = 1; s <= s_max; s++) {
+    const long waves = (base * s + num_sms - 1) / num_sms;
+    const double cost = (double)waves * (ceil_div(key_tiles, s) + (s > 1 ? 2 : 0));
+    if (s == 1 || cost < best) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  const int ch = ceil_div(key_tiles, best_s) * AKT;
   *chunk = ch;
   *splits = ceil_div(max_keys, ch);
 }
@@ -485,7 +528,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, bf16* out, cudaStream_t st) {
   p.splits = a.splits;
   p.chunk = a.chunk;
   const int grp = a.nq / a.nkv;
-  dim3 grid(ceil_div(a.L * grp, AQ), a.batch * a.nkv, a.splits);
+  dim3 grid(ceil_div(ceil_div(a.L * grp, AQ), NQT), a.batch * a.nkv, a.splits);
   cudaError_t err = launch_k(attn_tc_kernel, grid, kAThreads, kASmem, st, p);
   if (err != cudaSuccess || a.splits == 1) return err;
   return launch_attn_merge(a, out, st);
