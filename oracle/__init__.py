@@ -28,6 +28,7 @@ _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _i16p = ctypes.POINTER(ctypes.c_int16)
 _i8p = ctypes.POINTER(ctypes.c_int8)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 _f64p = ctypes.POINTER(ctypes.c_double)
 
 
@@ -49,6 +50,10 @@ class _OracleModel(ctypes.Structure):
         ("attn_norm", _u16p * _MAX_LAYERS), ("wqkv", _u16p * _MAX_LAYERS), ("q_norm", _u16p * _MAX_LAYERS),
         ("k_norm", _u16p * _MAX_LAYERS), ("wo", _u16p * _MAX_LAYERS), ("mlp_norm", _u16p * _MAX_LAYERS),
         ("w_gate_up", _u16p * _MAX_LAYERS), ("w_down", _u16p * _MAX_LAYERS),
+        ("q_wqkv", _u8p * _MAX_LAYERS), ("q_wo", _u8p * _MAX_LAYERS), ("q_gate_up", _u8p * _MAX_LAYERS),
+        ("q_down", _u8p * _MAX_LAYERS), ("q_lm_head", _u8p),
+        ("e_wqkv", _i8p * _MAX_LAYERS), ("e_wo", _i8p * _MAX_LAYERS), ("e_gate_up", _i8p * _MAX_LAYERS),
+        ("e_down", _i8p * _MAX_LAYERS), ("e_lm_head", _i8p),
     ]
 
 
@@ -72,9 +77,18 @@ def _configure(l):
     l.oracle_prepare_context.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _i32p,
                                          _i32p, ctypes.POINTER(_u16p), _u16p, ctypes.c_int]
     l.oracle_draft_block.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
-                                     ctypes.c_int, _i32p, _i32p, ctypes.c_int32, _u16p, _u16p]
+                                     ctypes.c_int, _i32p, _i32p, ctypes.c_int32, _u16p, _u16p, ctypes.c_int]
     l.oracle_constrain_argmax.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
-                                          ctypes.c_int, _i32p, _i32p, _i16p, _i32p, _f64p, _f64p]
+                                          ctypes.c_int, _i32p, _i32p, _i16p, _i32p, _f64p, _f64p, ctypes.c_int]
+    l.oracle_e4m3_decode.restype = ctypes.c_double
+    l.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    l.oracle_e4m3_encode.restype = ctypes.c_uint8
+    l.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+    l.oracle_block_exponent.restype = ctypes.c_int
+    l.oracle_block_exponent.argtypes = [ctypes.c_double]
+    l.oracle_quantize_fp8.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _u8p, _i8p]
+    l.oracle_quantize_fp8_bf16.argtypes = [ctypes.c_int, ctypes.c_int, _u16p, _u8p, _i8p]
+    l.oracle_linear_fp8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64p, _u8p, _i8p, _f64p]
     l.oracle_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _i32p, ctypes.c_int, _i32p,
                                 _i32p, _i16p, _i8p, ctypes.c_int32, _i32p, _i32p, _i32p]
     return l
@@ -174,14 +188,67 @@ def attention(q, k_ctx_bits, v_ctx_bits, k_blk, v_blk, scale) -> np.ndarray:
     return o
 
 
+# ---- f2: E4M3 and the 128-element group quantisation (fpd_oracle.c, "f2" section) -------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8)
+    f = lib().oracle_e4m3_decode
+    return np.array([f(int(v)) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float64)
+    f = lib().oracle_e4m3_encode
+    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint8).reshape(x.shape)
+
+
+def block_exponent(amax: float) -> int:
+    return int(lib().oracle_block_exponent(float(amax)))
+
+
+def quantize_fp8(X) -> tuple:
+    """Rows of X (float values, or bf16 bit patterns as uint16) -> (codes [N, K] uint8, exponents [N, K/128] int8)."""
+    X = np.asarray(X)
+    N, K = X.shape
+    assert K % 128 == 0
+    codes = np.empty((N, K), dtype=np.uint8)
+    exps = np.empty((N, K // 128), dtype=np.int8)
+    if X.dtype == np.uint16:
+        Xc = _c(X, np.uint16)
+        lib().oracle_quantize_fp8_bf16(N, K, _p(Xc, _u16p), _p(codes, _u8p), _p(exps, _i8p))
+    else:
+        Xc = _c(X, np.float64)
+        lib().oracle_quantize_fp8(N, K, _p(Xc, _f64p), _p(codes, _u8p), _p(exps, _i8p))
+    return codes, exps
+
+
+def dequantize_fp8(codes, exps) -> np.ndarray:
+    """The values the quantised rows stand for: decode(code) * 2^exponent of its group."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    v = e4m3_decode(np.arange(256, dtype=np.uint8))[codes]
+    return v * np.exp2(np.repeat(np.asarray(exps, dtype=np.float64), 128, axis=1))
+
+
+def linear_fp8(X, codes, exps) -> np.ndarray:
+    """X [M, K] float values (quantised here by rows) against quantised weights [N, K]."""
+    X = _c(X, np.float64)
+    M, K = X.shape
+    q = _c(codes, np.uint8)
+    e = _c(exps, np.int8)
+    Y = np.empty((M, q.shape[0]), dtype=np.float64)
+    lib().oracle_linear_fp8(M, q.shape[0], K, _p(X, _f64p), _p(q, _u8p), _p(e, _i8p), _p(Y, _f64p))
+    return Y
+
+
 # ---- the hot path ---------------------------------------------------------------------------------------
 
 class Model:
     """Holds the weights (bf16 bit patterns from synth.make_weights) and the C struct pointing at them."""
 
-    def __init__(self, shape, weights):
+    def __init__(self, shape, weights, fp8=False):
         self.shape = shape
         self.w = weights
+        self.fp8 = bool(fp8)
         s = _OracleModel()
         s.n_layers, s.d, s.nq, s.nkv = shape.n_layers, shape.d_model, shape.n_q_heads, shape.n_kv_heads
         s.h, s.F, s.V, s.nf = shape.head_dim, shape.d_ff, shape.vocab, shape.n_feat
@@ -199,8 +266,35 @@ class Model:
         for l, lw in enumerate(weights["layers"]):
             for name in ("attn_norm", "wqkv", "q_norm", "k_norm", "wo", "mlp_norm", "w_gate_up", "w_down"):
                 getattr(s, name)[l] = ptr(lw[name])
+        if fp8:   # the FP8 copies of the streamed matrices, quantised by this oracle from the bf16 weights
+            def q(a):
+                codes, exps = quantize_fp8(_c(a, np.uint16))
+                keep.extend([codes, exps])
+                return codes.ctypes.data_as(_u8p), exps.ctypes.data_as(_i8p)
+
+            s.q_lm_head, s.e_lm_head = q(weights["lm_head"])
+            for l, lw in enumerate(weights["layers"]):
+                for name, qn, en in (("wqkv", "q_wqkv", "e_wqkv"), ("wo", "q_wo", "e_wo"),
+                                     ("w_gate_up", "q_gate_up", "e_gate_up"), ("w_down", "q_down", "e_down")):
+                    getattr(s, qn)[l], getattr(s, en)[l] = q(lw[name])
         self._keep = keep
         self.c = s
+
+    def fp8_copy(self, name, layer=None):
+        """(codes, exponents) numpy views of one FP8 copy: name in wqkv, wo, w_gate_up, w_down, lm_head."""
+        assert self.fp8
+        sh = self.shape
+        d, F, nqkv = sh.d_model, sh.d_ff, (sh.n_q_heads + 2 * sh.n_kv_heads) * sh.head_dim
+        rows, K = {"wqkv": (nqkv, d), "wo": (d, sh.n_q_heads * sh.head_dim), "w_gate_up": (2 * F, d),
+                   "w_down": (d, F), "lm_head": (sh.vocab, d)}[name]
+        qn, en = {"wqkv": ("q_wqkv", "e_wqkv"), "wo": ("q_wo", "e_wo"), "w_gate_up": ("q_gate_up", "e_gate_up"),
+                  "w_down": ("q_down", "e_down"), "lm_head": ("q_lm_head", "e_lm_head")}[name]
+        qp, ep = getattr(self.c, qn), getattr(self.c, en)
+        if layer is not None:
+            qp, ep = qp[layer], ep[layer]
+        codes = np.ctypeslib.as_array(qp, shape=(rows, K))
+        exps = np.ctypeslib.as_array(ep, shape=(rows, K // 128))
+        return codes, exps
 
 
 def prepare_context(model: Model, row_off, feats, t_cap, batch=None, pos_start=None, kv_store=None):
@@ -222,8 +316,12 @@ def prepare_context(model: Model, row_off, feats, t_cap, batch=None, pos_start=N
     return kv_store
 
 
-def draft_block(model: Model, kv_store, t_cap, ctx_len, anchor, mask_id, block_len, want_layers=False):
-    """Returns hidden [B*L, d] (bf16 bits) and, when asked, the per-layer residual [n_layers, B*L, d]."""
+FEW_TOKENS = 16   # calls with at most this many positions run the weight-streaming (FP8-capable) path
+
+
+def draft_block(model: Model, kv_store, t_cap, ctx_len, anchor, mask_id, block_len, want_layers=False, fp8=None):
+    """Returns hidden [B*L, d] (bf16 bits) and, when asked, the per-layer residual [n_layers, B*L, d].
+    fp8 None: the FP8 projections exactly when the model has FP8 copies and the call has at most 16 positions."""
     sh = model.shape
     ctx_len = _c(ctx_len, np.int32)
     anchor = _c(anchor, np.int32)
@@ -231,17 +329,21 @@ def draft_block(model: Model, kv_store, t_cap, ctx_len, anchor, mask_id, block_l
     kv = _c(kv_store, np.uint16)
     hidden = np.empty((B * block_len, sh.d_model), dtype=np.uint16)
     layers = np.empty((sh.n_layers, B * block_len, sh.d_model), dtype=np.uint16) if want_layers else None
+    if fp8 is None:
+        fp8 = model.fp8 and B * block_len <= FEW_TOKENS
+    assert not fp8 or model.fp8
     rc = lib().oracle_draft_block(ctypes.byref(model.c), B, block_len, _p(kv, _u16p), int(t_cap),
                                   _p(ctx_len, _i32p), _p(anchor, _i32p), int(mask_id), _p(hidden, _u16p),
-                                  _p(layers, _u16p))
+                                  _p(layers, _u16p), int(bool(fp8)))
     if rc:
         raise ValueError("oracle_draft_block: bad arguments")
     return (hidden, layers) if want_layers else hidden
 
 
-def constrain_argmax(model: Model, hidden, batch, block_len, layout=None, want_logits=False):
+def constrain_argmax(model: Model, hidden, batch, block_len, layout=None, want_logits=False, fp8=None):
     """Returns (tokens [B, L-1] int32, margin [B*(L-1)] f64, logits [B*(L-1), V] f64 or None).  Logits of
-    illegal columns are NaN."""
+    illegal columns are NaN.  fp8 None: the FP8 LM head exactly when the model has FP8 copies, there is no
+    layout and at most 16 positions."""
     sh = model.shape
     hid = _c(hidden, np.uint16)
     P = block_len - 1
@@ -256,13 +358,16 @@ def constrain_argmax(model: Model, hidden, batch, block_len, layout=None, want_l
         cr = _c(layout["class_ranges"], np.int32)
         pc = _c(np.broadcast_to(layout["pos_class"], (batch, block_len)) if layout["pos_class"].ndim == 1
                 else layout["pos_class"], np.int16)
+    if fp8 is None:
+        fp8 = model.fp8 and layout is None and batch * P <= FEW_TOKENS
+    assert not fp8 or model.fp8
     rc = lib().oracle_constrain_argmax(ctypes.byref(model.c), batch, block_len, _p(hid, _u16p), n_class,
                                        _p(co, _i32p), _p(cr, _i32p), _p(pc, _i16p), _p(tokens, _i32p),
-                                       _p(logits, _f64p), _p(margin, _f64p))
+                                       _p(logits, _f64p), _p(margin, _f64p), int(bool(fp8)))
     if rc:
         raise ValueError("oracle_constrain_argmax: bad layout")
     if layout is not None and len(layout.get("pairs", ())) and logits is None:
-        return constrain_argmax(model, hidden, batch, block_len, layout, want_logits=True)[:2] + (None,)
+        return constrain_argmax(model, hidden, batch, block_len, layout, want_logits=True, fp8=fp8)[:2] + (None,)
     if layout is not None and len(layout.get("pairs", ())):
         _pair_offscreen(tokens, margin, logits, block_len, layout["pairs"], int(layout["off_id"]))
     return tokens, margin, logits

@@ -44,6 +44,11 @@ typedef struct oracle_model {
   const uint16_t *attn_norm[OR_MAX_LAYERS], *wqkv[OR_MAX_LAYERS], *q_norm[OR_MAX_LAYERS],
       *k_norm[OR_MAX_LAYERS], *wo[OR_MAX_LAYERS], *mlp_norm[OR_MAX_LAYERS], *w_gate_up[OR_MAX_LAYERS],
       *w_down[OR_MAX_LAYERS];
+  /* FP8 copies (E4M3 codes + one power-of-two exponent per 128 elements of a row), or NULL: see the f2 section */
+  const uint8_t *q_wqkv[OR_MAX_LAYERS], *q_wo[OR_MAX_LAYERS], *q_gate_up[OR_MAX_LAYERS], *q_down[OR_MAX_LAYERS],
+      *q_lm_head;
+  const int8_t *e_wqkv[OR_MAX_LAYERS], *e_wo[OR_MAX_LAYERS], *e_gate_up[OR_MAX_LAYERS], *e_down[OR_MAX_LAYERS],
+      *e_lm_head;
 } oracle_model;
 
 /* ------------------------------------------------------------------------------------------------------ */
@@ -151,6 +156,129 @@ void oracle_linear(int M, int N, int K, const double* X, const uint16_t* W, doub
       free(w);
     }
   }
+}
+
+/* ------------------------------------------------------------------------------------------------------ */
+/* f2: 8-bit weights and activations.  FlashDrive §3.4 "Quantization": low-bit weights shrink the bytes a
+ * memory-bound decoding step has to load, and 8-bit activations let the products run on 8-bit matrix units.
+ * The 8-bit type here is E4M3 of the OCP 8-bit floating-point format (OFP8): 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; code (e, m) is (1 + m/8) 2^(e-7) for e >= 1 and (m/8) 2^-6 for e = 0; the code with
+ * e = 15, m = 7 is NaN, so the largest finite magnitude is 448 (e = 15, m = 6).
+ *
+ * Quantisation group: 128 consecutive elements of one row (a weight row, or one token's activation row), with a
+ * power-of-two scale 2^k: k is the smallest integer with amax * 2^-k <= 448 (amax = the group's largest
+ * magnitude), clamped to [-126, 127], and k = 0 for an all-zero group.  Each element becomes the E4M3 code
+ * nearest to x * 2^-k, ties to the even code (mantissa bit 0 clear); a zero result is the +0 code.  The value
+ * the group stands for is decode(code) * 2^k.                                                               */
+
+double oracle_e4m3_decode(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* nearest code, ties to even; magnitudes above 448 saturate to 448 */
+uint8_t oracle_e4m3_encode(double x) {
+  const int neg = x < 0;
+  double a = fabs(x);
+  if (a > 448.0) a = 448.0;
+  int code;
+  if (a < ldexp(1.0, -6)) {
+    code = (int)rint(a * 512.0);                /* subnormal steps of 2^-9; 8 steps = the smallest normal */
+  } else {
+    int E;
+    const double f = frexp(a, &E);             /* a = f 2^E, f in [0.5, 1): exponent e - 7 = E - 1 */
+    const int mant = (int)rint((2.0 * f - 1.0) * 8.0);   /* 0..8; 8 carries into the next exponent */
+    code = ((E - 1 + 7) << 3) + mant;
+  }
+  if (code == 0) return 0;
+  return (uint8_t)(code | (neg ? 0x80 : 0));
+}
+
+int oracle_block_exponent(double amax) {
+  if (!(amax > 0.0)) return 0;
+  int E;
+  const double f = frexp(amax, &E);            /* amax = f 2^E; 448 = 0.875 2^9 */
+  int k = E - 9 + (f > 0.875 ? 1 : 0);
+  if (k < -126) k = -126;
+  if (k > 127) k = 127;
+  return k;
+}
+
+/* one group of 128 values: its exponent, and its codes */
+static int8_t quantize_group(const double* x, uint8_t* codes) {
+  double amax = 0.0;
+  for (int i = 0; i < 128; i++)
+    if (fabs(x[i]) > amax) amax = fabs(x[i]);
+  const int k = oracle_block_exponent(amax);
+  for (int i = 0; i < 128; i++) codes[i] = oracle_e4m3_encode(ldexp(x[i], -k));
+  return (int8_t)k;
+}
+
+/* codes [N, K] and exponents [N, K/128] of the rows of X (K a multiple of 128) */
+void oracle_quantize_fp8(int N, int K, const double* X, uint8_t* codes, int8_t* exps) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; n++)
+    for (int g = 0; g < K / 128; g++)
+      exps[(size_t)n * (K / 128) + g] = quantize_group(X + (size_t)n * K + (size_t)g * 128, codes + (size_t)n * K + (size_t)g * 128);
+}
+
+/* the same for a bf16 matrix (weights) */
+void oracle_quantize_fp8_bf16(int N, int K, const uint16_t* W, uint8_t* codes, int8_t* exps) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; n++) {
+    double x[128];
+    for (int g = 0; g < K / 128; g++) {
+      for (int i = 0; i < 128; i++) x[i] = bf(W[(size_t)n * K + (size_t)g * 128 + i]);
+      exps[(size_t)n * (K / 128) + g] = quantize_group(x, codes + (size_t)n * K + (size_t)g * 128);
+    }
+  }
+}
+
+static void dequant_row(int K, const uint8_t* q, const int8_t* e, double* out) {
+  for (int k = 0; k < K; k++) out[k] = ldexp(oracle_e4m3_decode(q[k]), e[k / 128]);
+}
+
+/* Y[m][n] = sum_k Xq[m][k] Wq[n][k] with both operands in the quantised form above: the activation rows X are
+ * quantised here (the same rule as the weights), the weights come as codes + exponents. */
+void oracle_linear_fp8(int M, int N, int K, const double* X, const uint8_t* Wq, const int8_t* We, double* Y) {
+  uint8_t* xq = (uint8_t*)malloc((size_t)M * K);
+  int8_t* xe = (int8_t*)malloc((size_t)M * (K / 128));
+  double* xd = (double*)malloc(sizeof(double) * (size_t)M * K);
+  oracle_quantize_fp8(M, K, X, xq, xe);
+  for (int m = 0; m < M; m++) dequant_row(K, xq + (size_t)m * K, xe + (size_t)m * (K / 128), xd + (size_t)m * K);
+#pragma omp parallel
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(static)
+    for (int n = 0; n < N; n++) {
+      dequant_row(K, Wq + (size_t)n * K, We + (size_t)n * (K / 128), w);
+      for (int m = 0; m < M; m++) {
+        const double* xr = xd + (size_t)m * K;
+        double acc = 0.0;
+        for (int k = 0; k < K; k++) acc += xr[k] * w[k];
+        Y[(size_t)m * N + n] = acc;
+      }
+    }
+    free(w);
+  }
+  free(xq);
+  free(xe);
+  free(xd);
+}
+
+/* the linear layers of the drafter pass: bf16 weights, or the FP8 copies when fp8 is set */
+static void linear_of(int fp8, int M, int N, int K, const double* X, const uint16_t* W, const uint8_t* Wq,
+                      const int8_t* We, double* Y) {
+  if (fp8)
+    oracle_linear_fp8(M, N, K, X, Wq, We, Y);
+  else
+    oracle_linear(M, N, K, X, W, Y);
 }
 
 /* Softmax attention of nq_rows query rows (each h values) over n_keys keys/values (bf16 rows of h):
@@ -266,10 +394,12 @@ int oracle_prepare_context(const oracle_model* m, int batch, int total_rows, con
  *   o = bf16(softmax(q [Kctx; Kblk]^T / sqrt(h)) [Vctx; Vblk])    (GQA: q head i uses kv head i/(nq/nkv))
  *   x = bf16(x + o . Wo^T)
  *   xn = bf16(RMSNorm_mlp(x)); u = bf16(silu(xn . Wg^T) * (xn . Wu^T)); x = bf16(x + u . Wdown^T)
- * hidden_out [B*L, d] = x after the last layer; layer_hidden (optional) [n_layers, B*L, d]. */
+ * hidden_out [B*L, d] = x after the last layer; layer_hidden (optional) [n_layers, B*L, d].
+ * fp8 != 0: the four projections take the FP8 form of the f2 section (weights from the q_ and e_ copies, the
+ * bf16 activations xn, o, xn, u quantised per 128-element group of each row). */
 int oracle_draft_block(const oracle_model* m, int batch, int L, const uint16_t* kv_store, int t_cap,
                        const int32_t* ctx_len, const int32_t* anchor, int32_t mask_id, uint16_t* hidden_out,
-                       uint16_t* layer_hidden) {
+                       uint16_t* layer_hidden, int fp8) {
   const int d = m->d, h = m->h, nq = m->nq, nkv = m->nkv, F = m->F;
   const int M = batch * L, nqkv = (nq + 2 * nkv) * h, grp = nq / nkv;
   if (L < 1 || batch < 1 || nq % nkv) return -1;
@@ -300,7 +430,7 @@ int oracle_draft_block(const oracle_model* m, int batch, int L, const uint16_t* 
       oracle_rmsnorm(d, x + (size_t)r * d, m->attn_norm[l], m->eps, xn + (size_t)r * d);
       for (int k = 0; k < d; k++) xn[(size_t)r * d + k] = rbf(xn[(size_t)r * d + k]);
     }
-    oracle_linear(M, nqkv, d, xn, m->wqkv[l], qkv);
+    linear_of(fp8, M, nqkv, d, xn, m->wqkv[l], m->q_wqkv[l], m->e_wqkv[l], qkv);
 #pragma omp parallel
     {
       double* t = (double*)malloc(sizeof(double) * (size_t)h);
@@ -347,19 +477,19 @@ int oracle_draft_block(const oracle_model* m, int batch, int L, const uint16_t* 
       free(qh);
       free(oh);
     }
-    oracle_linear(M, d, nq * h, o, m->wo[l], dx);
+    linear_of(fp8, M, d, nq * h, o, m->wo[l], m->q_wo[l], m->e_wo[l], dx);
     for (size_t e = 0; e < (size_t)M * d; e++) x[e] = rbf(x[e] + dx[e]);
     for (int r = 0; r < M; r++) {
       oracle_rmsnorm(d, x + (size_t)r * d, m->mlp_norm[l], m->eps, xn + (size_t)r * d);
       for (int k = 0; k < d; k++) xn[(size_t)r * d + k] = rbf(xn[(size_t)r * d + k]);
     }
-    oracle_linear(M, 2 * F, d, xn, m->w_gate_up[l], dx); /* columns 0..F-1 gate, F..2F-1 up */
+    linear_of(fp8, M, 2 * F, d, xn, m->w_gate_up[l], m->q_gate_up[l], m->e_gate_up[l], dx); /* gate | up */
     for (int r = 0; r < M; r++)
       for (int f = 0; f < F; f++) {
         double gv = dx[(size_t)r * 2 * F + f], uv = dx[(size_t)r * 2 * F + F + f];
         hm[(size_t)r * F + f] = rbf(oracle_silu(gv) * uv);
       }
-    oracle_linear(M, d, F, hm, m->w_down[l], dx);
+    linear_of(fp8, M, d, F, hm, m->w_down[l], m->q_down[l], m->e_down[l], dx);
     for (size_t e = 0; e < (size_t)M * d; e++) x[e] = rbf(x[e] + dx[e]);
     if (layer_hidden)
       for (size_t e = 0; e < (size_t)M * d; e++)
@@ -376,10 +506,11 @@ int oracle_draft_block(const oracle_model* m, int batch, int L, const uint16_t* 
  *   pos_class NULL: every id in [0, V) is legal.  Otherwise class c's ids are the union of ranges
  *   class_ranges[2*class_off[c] ..].
  * Outputs: tokens [B, L-1]; logits (optional) [B*(L-1), V] double, only legal columns written;
- * margin (optional) [B*(L-1)] = top-1 minus top-2 fp32 logit (INFINITY when one id is legal). */
+ * margin (optional) [B*(L-1)] = top-1 minus top-2 fp32 logit (INFINITY when one id is legal).
+ * fp8 != 0: logits from the FP8 LM-head copy and the quantised z (f2 section). */
 int oracle_constrain_argmax(const oracle_model* m, int batch, int L, const uint16_t* hidden, int n_class,
                             const int32_t* class_off, const int32_t* class_ranges, const int16_t* pos_class,
-                            int32_t* tokens, double* logits, double* margin) {
+                            int32_t* tokens, double* logits, double* margin, int fp8) {
   const int d = m->d, V = m->V, P = L - 1;
   if (L < 2) return -1;
   const int all_off[2] = {0, 1};
@@ -422,7 +553,8 @@ int oracle_constrain_argmax(const oracle_model* m, int batch, int L, const uint1
       if (lo < 0 || hi > V || lo >= hi) { rc = -1; break; }
       int n = hi - lo;
       double* lg = (double*)malloc(sizeof(double) * (size_t)nrow * n);
-      oracle_linear(nrow, n, d, zc, m->lm_head + (size_t)lo * d, lg);
+      linear_of(fp8, nrow, n, d, zc, m->lm_head + (size_t)lo * d, fp8 ? m->q_lm_head + (size_t)lo * d : NULL,
+                fp8 ? m->e_lm_head + (size_t)lo * (d / 128) : NULL, lg);
       /* ids ascending within and across ranges (ranges are sorted), so strict '>' keeps the lowest id */
       for (int i = 0; i < nrow; i++)
         for (int v = 0; v < n; v++) {
