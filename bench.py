@@ -71,16 +71,19 @@ def legal_counts(wl):
     return counts, (s.vocab if full else len(rows))
 
 
-def algorithmic_work(wl):
+def algorithmic_work(wl, fp8=False):
     """Minimum bytes and flops of one step (every request's block): drafter layer weights, the LM-head rows some
     position can select, the context K/V reads; 2 flops per multiply-add of the projections, the LM-head columns
-    of the legal ids and the attention (4 (T_b + L) L h per q head and layer)."""
+    of the legal ids and the attention (4 (T_b + L) L h per q head and layer).  fp8: one byte per weight plus one
+    exponent byte per 128 weights for the streamed matrices (the unconstrained LM head included)."""
     s, B, L = wl.shape, wl.batch, wl.block_len
     layer_params = (s.qkv_rows * s.d_model + s.d_model * s.n_q_heads * s.head_dim + 2 * s.d_ff * s.d_model
                     + s.d_model * s.d_ff)
     counts, lm_rows = legal_counts(wl)
     ctx = wl.ctx_len.astype(np.int64)
-    bytes_ = {"layers": s.n_layers * layer_params * 2, "lm_head": lm_rows * s.d_model * 2,
+    wb = 1 + 1 / 128 if fp8 else 2
+    lmb = wb if (fp8 and wl.layout is None) else 2
+    bytes_ = {"layers": int(s.n_layers * layer_params * wb), "lm_head": int(lm_rows * s.d_model * lmb),
               "kv": int(ctx.sum()) * s.n_layers * 2 * s.n_kv_heads * s.head_dim * 2}
     flops = {"layers": 2 * B * L * layer_params * s.n_layers, "lm_head": 2 * B * int(counts.sum()) * s.d_model,
              "attention": 4 * int((ctx + L).sum()) * L * s.head_dim * s.n_q_heads * s.n_layers}
@@ -300,10 +303,10 @@ class StepRunner:
         return t0e.elapsed_time(t1e), draft_ms, lm_ms
 
 
-def roofline_of(wl, ms_per_step, draft_ms, lm_ms, traffic=None):
+def roofline_of(wl, ms_per_step, draft_ms, lm_ms, traffic=None, fp8=False):
     """The step's roofline: HBM-bound when the bytes take longer than the flops at the measured peaks."""
     hbm, tc_burst, tc_sus, kind = peaks()
-    by, fl = algorithmic_work(wl)
+    by, fl = algorithmic_work(wl, fp8)
     B_tot, F_tot = sum(by.values()), sum(fl.values())
     sec = ms_per_step * 1e-3
     lm_bytes = by["lm_head"] + wl.batch * (wl.block_len - 1) * wl.shape.d_model * 2
@@ -359,6 +362,26 @@ def run_batched_extra(pkg, w, dev, steps=10, warmup=3):
     return out
 
 
+def run_fp8_extra(pkg, w, wl, dev, steps=20, warmup=3):
+    """The same workload on the model's 8-bit weight copies (fpd_model_enable_fp8): the streamed GEMMs read E4M3
+    weights and quantise their inputs per 128 elements; the HBM roofline counts the 8-bit bytes."""
+    dr = pkg.Drafter(wl.shape, w, wl.batch, wl.block_len, wl.t_cap, device=dev, fp8=True)
+    r = StepRunner(pkg, dr, wl, dev)
+    r.capture(warmup)
+    ms, dms, lms = r.time_steps(steps)
+    assert pkg.fpd_device_status(r.stream) == 0, "device-side check failed (8-bit run)"
+    rf = roofline_of(wl, ms / steps, dms, lms, fp8=True)
+    out = {"ms_per_step": ms / steps, "value": wl.batch * (wl.block_len - 1) * steps / (ms * 1e-3),
+           "unit": "draft tokens/s", "draft_ms": dms, "lm_head_ms": lms, "bound": rf["bound"],
+           "achieved": rf["achieved"], "unit_roofline": rf["unit"], "frac": rf["frac"], "peak": rf["peak"],
+           "algorithmic_bytes": rf.get("algorithmic_bytes"),
+           "weights": "E4M3 codes + one power-of-two exponent per 128 elements (a different model from the bf16 "
+                      "line: its activations are quantised too)"}
+    del r
+    dr.close()
+    return out
+
+
 def run_sweep(pkg, steps, warmup):
     """The 32-point sweep: batch {1,4,16,64} x context {512,2048,8192,16384} x block {16 text, 385 special}.
     Each point's context K/V is drawn on the device (seed 5000 + point index); the LM head, attention and
@@ -400,6 +423,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-batched", action="store_true", help="skip the batched workload's extra measurement")
     ap.add_argument("--sweep", action="store_true", help="time the 32-point sweep, one line per point")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the 8-bit-weight measurement of the workload")
+    ap.add_argument("--fp8", action="store_true", help="time the workload on the 8-bit weight copies (main line)")
     args = ap.parse_args()
 
     import torch
@@ -425,6 +450,8 @@ def main():
     L, B = wl.block_len, wl.batch
     draft_tokens_per_step = B * (L - 1)
     config = workload_config(args.workload, wl)
+    if args.fp8:
+        config["weights"] = "8-bit E4M3 copies of the streamed matrices (fpd_model_enable_fp8)"
 
     if args.impl == "reference":
         # the CPU oracle, as it stands, on the host cores: rank 0 only
@@ -460,7 +487,7 @@ def main():
     torch.cuda.set_device(dev)
 
     w = synth.make_weights(s, wl.seed)
-    dr = pkg.Drafter(s, w, B, L, wl.t_cap, device=dev)
+    dr = pkg.Drafter(s, w, B, L, wl.t_cap, device=dev, fp8=args.fp8)
     r = StepRunner(pkg, dr, wl, dev)
     r.capture(args.warmup)
 
@@ -501,7 +528,8 @@ def main():
     e2e_s = time.perf_counter() - t0
     e2e_value = world * draft_tokens_per_step * e2e_steps / e2e_s
 
-    roofline = roofline_of(wl, ms_per_step, draft_ms, lm_ms, profiled_traffic(args.workload))
+    roofline = roofline_of(wl, ms_per_step, draft_ms, lm_ms, None if args.fp8 else profiled_traffic(args.workload),
+                           fp8=args.fp8 and B * L <= 16)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -521,6 +549,9 @@ def main():
     prepare_ms = r.prepare_ms
     del r
     dr.close()
+    fp8 = None
+    if rank == 0 and world == 1 and B * L <= 16 and not args.no_fp8 and not args.fp8:
+        fp8 = run_fp8_extra(pkg, w, wl, dev)
     batched = None
     if rank == 0 and world == 1 and B * L < 300 and not args.no_batched:
         batched = run_batched_extra(pkg, w, dev)
@@ -528,12 +559,15 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "draft tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+                "vs_baseline": None, "dtype": "f8e4m3 x f8e4m3 -> f32" if args.fp8 and B * L <= 16 else "bf16",
+                "data": "synthetic", "config": config,
                 "blocks_per_s": world * B * args.steps / (elapsed_ms / 1e3), "prepare_ms": prepare_ms,
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": "draft tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": int(launches), "clocks": cs.summary(local_rank)}
+        if fp8 is not None:
+            line["fp8"] = fp8
         if batched is not None:
             line["batched"] = batched
         print(json.dumps(line), flush=True)

@@ -61,7 +61,7 @@ _lib = None
 _EXPORTS = ["fpd_model_create", "fpd_model_destroy", "fpd_kv_store_bytes", "fpd_workspace_bytes",
             "fpd_prepare_context", "fpd_prepare_context_rows", "fpd_draft_block", "fpd_constrain_argmax",
             "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_verify_prefix", "fpd_sd_advance", "fpd_grid_to_text",
-            "fpd_last_error",
+            "fpd_model_enable_fp8", "fpd_model_fp8_enabled", "fpd_quantize_fp8", "fpd_last_error",
             "fpd_kernel_launches", "fpd_device_status"]
 
 
@@ -100,7 +100,11 @@ def lib():
         l.fpd_last_error.restype = ctypes.c_char_p
         l.fpd_kernel_launches.restype = ctypes.c_uint64
         l.fpd_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
-        for f in ("fpd_model_create", "fpd_prepare_context", "fpd_prepare_context_rows", "fpd_draft_block",
+        l.fpd_model_enable_fp8.argtypes = [vp, vp]
+        l.fpd_model_fp8_enabled.argtypes = [vp]
+        l.fpd_model_fp8_enabled.restype = ctypes.c_int32
+        l.fpd_quantize_fp8.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+        for f in ("fpd_model_create", "fpd_model_enable_fp8", "fpd_quantize_fp8", "fpd_prepare_context", "fpd_prepare_context_rows", "fpd_draft_block",
                   "fpd_constrain_argmax", "fpd_constrain_argmax_noalloc", "fpd_verify", "fpd_sd_advance",
                   "fpd_grid_to_text", "fpd_verify_prefix",
                   "fpd_device_status"):
@@ -144,6 +148,19 @@ def fpd_model_create(desc: ModelDesc, weights: Weights) -> int:
 
 def fpd_model_destroy(model: int) -> None:
     lib().fpd_model_destroy(model)
+
+
+def fpd_model_enable_fp8(model: int, stream=None) -> None:
+    _check(lib().fpd_model_enable_fp8(model, _stream(stream)), "fpd_model_enable_fp8")
+
+
+def fpd_model_fp8_enabled(model: int) -> bool:
+    return bool(lib().fpd_model_fp8_enabled(model))
+
+
+def fpd_quantize_fp8(w, rows, cols, ld, codes, exps, stream=None) -> None:
+    _check(lib().fpd_quantize_fp8(_ptr(w), rows, cols, ld, _ptr(codes), _ptr(exps), _stream(stream)),
+           "fpd_quantize_fp8")
 
 
 def fpd_kv_store_bytes(model: int, batch: int, t_cap: int) -> int:

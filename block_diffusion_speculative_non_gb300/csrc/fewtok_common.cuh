@@ -7,6 +7,8 @@
 #pragma once
 
 #include "fpd_kernels.cuh"
+#include <cuda_fp8.h>
+
 #include "tc_primitives.cuh"
 
 namespace fpd {
@@ -95,6 +97,74 @@ __device__ __forceinline__ void norm_atoms(uint8_t* act, const uint8_t* gbuf, co
       }
       *xp = u;
     }
+  }
+}
+
+// ---- 8-bit operands (E4M3, OCP OFP8) with one power-of-two scale per 128 elements of a row ----------------------
+// The exponent k of a group: the smallest integer with amax 2^-k <= 448 (the largest finite E4M3), clamped to
+// [-126, 127]; 0 for an all-zero group.  From the bits of amax = (1 + m 2^-23) 2^(e - 127): 448 = 1.75 2^8, so
+// k = e - 127 - 8 + (m > 0.75 2^23).  A subnormal amax gives the clamp.
+__device__ __forceinline__ int fp8_group_exponent(float amax) {
+  const uint32_t u = __float_as_uint(amax);
+  const int e = (int)(u >> 23), m = (int)(u & 0x7FFFFFu);
+  if (amax == 0.f) return 0;
+  if (e == 0) return -126;
+  const int k = e - 135 + (m > 0x600000 ? 1 : 0);
+  return k < -126 ? -126 : (k > 127 ? 127 : k);
+}
+__device__ __forceinline__ float exp2_int(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }   // |k| <= 126
+
+// Two E4M3 codes (round to nearest even, saturating) of x0, x1: x0 in the low byte.  A zero result is the +0 code.
+__device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
+  uint32_t c = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+  if ((c & 0x7Fu) == 0) c &= 0xFF00u;
+  if ((c & 0x7F00u) == 0) c &= 0x00FFu;
+  return c;
+}
+
+// The activation slice in 8-bit form, in place: bf16 atoms [a0, a0 + na) (na even, <= 4: 64 K each, 16 token rows,
+// 128-byte swizzle) become E4M3 blocks [a0/2, a0/2 + na/2) (128 K each, same row and swizzle layout, written over
+// the bytes of atoms a0/2 ..), with s_xs[t * xs_ld + block] = 2^k of token t's group.  Thread et: pair = et / 4
+// (token t = pair % 16, block pair / 16), quarter q = et % 4 covers the block's K elements [32q, 32q + 32).  Rows
+// t >= M are zero.  Every read of the group precedes every write (the first blocks overwrite their own source).
+__device__ __forceinline__ void quant_atoms(uint8_t* act, float* s_xs, int xs_ld, int a0, int na, int M, int et) {
+  const int pair = et >> 2, q = et & 3, t = pair & 15, blk = pair >> 4;
+  const bool on = blk < (na >> 1);
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; i++) x[i] = 0.f;
+  if (on && t < M) {
+    const uint8_t* src = act + (a0 + 2 * blk + (q >> 1)) * X_ATOM + t * 128;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+      const int lc = (q & 1) * 4 + c;
+      const uint4 u = *reinterpret_cast<const uint4*>(src + ((lc ^ (t & 7)) << 4));
+      const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const float2 f = __bfloat1622float2(e[k]);
+        x[c * 8 + 2 * k] = f.x;
+        x[c * 8 + 2 * k + 1] = f.y;
+      }
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(x[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int k = fp8_group_exponent(amax);
+  const float sc = exp2_int(-k);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++)
+    w[i] = e4m3x2(x[4 * i] * sc, x[4 * i + 1] * sc) | (e4m3x2(x[4 * i + 2] * sc, x[4 * i + 3] * sc) << 16);
+  epi_bar();   // every thread has read its source chunks
+  if (on) {
+    uint8_t* dst = act + (a0 / 2 + blk) * X_ATOM + t * 128;
+    *reinterpret_cast<uint4*>(dst + (((2 * q) ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ (t & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    if (q == 0) s_xs[t * xs_ld + a0 / 2 + blk] = exp2_int(k);
   }
 }
 

@@ -95,16 +95,21 @@ struct DraftWs {
 // The few-token path takes calls with at most 16 block positions in all.
 bool use_stream(const Model& m, int B, int L) { return B * L <= kStreamMaxTokens && stream_shape_ok(m.d); }
 
-DraftWs carve_draft_stream(const Model& m, Carver& c, int B, int L, int t_cap) {
+// Shapes whose streamed matrices can take the 8-bit form: every K a multiple of the 128-element group.
+bool fp8_shape_ok(const fpd_model_desc& d) {
+  return stream_shape_ok(d) && d.d_model % 128 == 0 && (d.n_q_heads * d.head_dim) % 128 == 0 && d.d_ff % 128 == 0;
+}
+
+DraftWs carve_draft_stream(const Model& m, Carver& c, int B, int L, int t_cap, bool fp8) {
   const auto& d = m.d;
   DraftWs w{};
   w.stream = true;
   const int M = B * L, S = kStreamMaxTokens;
   const int nqkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim, nqh = d.n_q_heads * d.head_dim;
-  w.s_qkv = stream_plan(nqkv / 128, d.d_model, m.num_sms, true);
-  w.s_o = stream_plan(d.d_model / 128, nqh, m.num_sms, true);
-  w.s_sw = stream_plan(d.d_ff / 64, d.d_model, m.num_sms, false);
-  w.s_down = stream_plan(d.d_model / 128, d.d_ff, m.num_sms, true);
+  w.s_qkv = stream_plan(nqkv / 128, d.d_model, m.num_sms, true, fp8);
+  w.s_o = stream_plan(d.d_model / 128, nqh, m.num_sms, true, fp8);
+  w.s_sw = stream_plan(d.d_ff / 64, d.d_model, m.num_sms, false, fp8);
+  w.s_down = stream_plan(d.d_model / 128, d.d_ff, m.num_sms, true, fp8);
   const size_t part = std::max(std::max(stream_part_floats(w.s_qkv), stream_part_floats(w.s_o)),
                                stream_part_floats(w.s_down));
   w.part = c.take<float>(std::max<size_t>(part, 1));
@@ -155,8 +160,8 @@ DraftWs carve_draft_tok(const Model& m, Carver& c, int B, int L, int t_cap) {
   return w;
 }
 
-DraftWs carve_draft(const Model& m, Carver& c, int B, int L, int t_cap) {
-  if (use_stream(m, B, L)) return carve_draft_stream(m, c, B, L, t_cap);
+DraftWs carve_draft(const Model& m, Carver& c, int B, int L, int t_cap, bool fp8) {
+  if (use_stream(m, B, L)) return carve_draft_stream(m, c, B, L, t_cap, fp8);
   if (B * L >= kTokMinRows) return carve_draft_tok(m, c, B, L, t_cap);
   const auto& d = m.d;
   DraftWs w{};
@@ -237,10 +242,12 @@ PrepWs carve_prep(const Model& m, Carver& c, int rows_max) {
   return w;
 }
 
+// Either weight form: the model may switch to 8-bit weights after the caller sized its workspace.
 size_t ws_draft_bytes(const Model& m, int B, int L, int t_cap) {
-  Carver c;
-  carve_draft(m, c, B, L, t_cap);
-  return c.off;
+  Carver c0, c1;
+  carve_draft(m, c0, B, L, t_cap, false);
+  if (fp8_shape_ok(m.d)) carve_draft(m, c1, B, L, t_cap, true);
+  return std::max(c0.off, c1.off);
 }
 size_t ws_argmax_bytes(const Model& m, int B, int L) {
   Carver c0, c1;
@@ -412,8 +419,79 @@ fpd_status fpd_model_create(const fpd_model_desc* desc, const fpd_weights* w, fp
 void fpd_model_destroy(fpd_model* m) {
   if (!m) return;
   if (m->rope) cudaFree(m->rope);
+  if (m->fp8_buf) cudaFree(m->fp8_buf);
   delete m;
 }
+
+fpd_status fpd_model_enable_fp8(fpd_model* m, void* stream) {
+  ApiScope scope("fpd_model_enable_fp8", stream);
+  if (!m) return fail(FPD_ERR_INVALID_ARG, "model must be non-null");
+  if (m->fp8) return FPD_OK;
+  const fpd_model_desc& d = m->d;
+  if (!fp8_shape_ok(d))
+    return fail(FPD_ERR_UNSUPPORTED, "8-bit weights need the few-token path's shapes and d_model, n_q_heads * head_dim "
+                                     "and d_ff multiples of 128");
+  fpd_status ds = check_device(*m);
+  if (ds) return ds;
+  const int nqkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim, nqh = d.n_q_heads * d.head_dim;
+  struct Job {
+    const void* w;
+    int N, K;
+    Model::F8* dst;
+  };
+  std::vector<Job> jobs;
+  for (int l = 0; l < d.n_layers; l++) {
+    jobs.push_back({m->w.wqkv[l], nqkv, d.d_model, &m->f8_qkv[l]});
+    jobs.push_back({m->w.wo[l], d.d_model, nqh, &m->f8_o[l]});
+    jobs.push_back({m->w.w_gate_up[l], 2 * d.d_ff, d.d_model, &m->f8_gu[l]});
+    jobs.push_back({m->w.w_down[l], d.d_model, d.d_ff, &m->f8_down[l]});
+  }
+  jobs.push_back({m->w.lm_head, d.vocab, d.d_model, &m->f8_lm});
+  size_t bytes = 0;
+  for (const Job& j : jobs) bytes = align_up(align_up(bytes, 256) + (size_t)j.N * j.K, 256) + (size_t)j.N * (j.K / 128);
+  void* buf = nullptr;
+  cudaError_t e = cudaMalloc(&buf, bytes + 256);
+  if (e != cudaSuccess) return cuda_fail(e, "8-bit weight copies");
+  cudaStream_t st = (cudaStream_t)stream;
+  size_t off = 0;
+  for (const Job& j : jobs) {
+    off = align_up(off, 256);
+    uint8_t* q = (uint8_t*)buf + off;
+    off = align_up(off + (size_t)j.N * j.K, 256);
+    int8_t* ex = (int8_t*)buf + off;
+    off += (size_t)j.N * (j.K / 128);
+    if (e == cudaSuccess) e = launch_quantize_fp8((const bf16*)j.w, j.N, j.K, j.K, q, ex, m->num_sms, st);
+    j.dst->q = q;
+    j.dst->e = ex;
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    cudaFree(buf);
+    for (const Job& j : jobs) *j.dst = Model::F8{};
+    return cuda_fail(e, "8-bit weight quantisation");
+  }
+  m->fp8_buf = buf;
+  m->fp8 = true;
+  return scope.done(FPD_OK);
+}
+
+fpd_status fpd_quantize_fp8(const void* w, int rows, int cols, int ld, void* codes, void* exps, void* stream) {
+  ApiScope scope("fpd_quantize_fp8", stream);
+  if (!w || !codes || !exps) return fail(FPD_ERR_INVALID_ARG, "w, codes and exps must be non-null");
+  if (rows < 1 || cols < 128 || cols % 128 || ld < cols || ld % 8)
+    return fail(FPD_ERR_SHAPE, "rows %d, cols %d (a positive multiple of 128), ld %d (>= cols, a multiple of 8)", rows,
+                cols, ld);
+  if (!aligned16(w) || !aligned16(codes)) return fail(FPD_ERR_INVALID_ARG, "w and codes must be 16-byte aligned");
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = launch_quantize_fp8((const bf16*)w, rows, cols, ld, (uint8_t*)codes, (int8_t*)exps, sms, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fpd_quantize_fp8");
+  return scope.done(FPD_OK);
+}
+
+int32_t fpd_model_fp8_enabled(const fpd_model* m) { return m && m->fp8 ? 1 : 0; }
 
 size_t fpd_kv_store_bytes(const fpd_model* m, int batch, int t_cap) {
   if (!m || batch < 1 || t_cap < 1) return 0;
@@ -523,7 +601,7 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
   if (ds) return ds;
   Carver c;
   c.base = (char*)workspace;
-  DraftWs w = carve_draft(*m, c, batch, L, t_cap);
+  DraftWs w = carve_draft(*m, c, batch, L, t_cap, m->fp8);
   if (c.off > ws_bytes) return fail(FPD_ERR_CAPACITY, "workspace %zu < %zu bytes", ws_bytes, c.off);
   cudaStream_t st = (cudaStream_t)stream;
   const int M = batch * L, dm = d.d_model, h = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.d_ff;
@@ -563,6 +641,9 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
       g.epi = SEPI_QKV;
       g.plan = w.s_qkv;
       g.w = (const bf16*)m->w.wqkv[l];
+      g.fp8 = m->fp8;
+      g.w8 = m->f8_qkv[l].q;
+      g.w_exp = m->f8_qkv[l].e;
       g.N = nqkv;
       g.K = dm;
       g.x = x;
@@ -592,6 +673,8 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
       o.epi = SEPI_RESID;
       o.plan = w.s_o;
       o.w = (const bf16*)m->w.wo[l];
+      o.w8 = m->f8_o[l].q;
+      o.w_exp = m->f8_o[l].e;
       o.N = dm;
       o.K = nq * h;
       o.x = w.o;
@@ -606,6 +689,8 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
       u.epi = SEPI_SWIGLU;
       u.plan = w.s_sw;
       u.w = (const bf16*)m->w.w_gate_up[l];
+      u.w8 = m->f8_gu[l].q;
+      u.w_exp = m->f8_gu[l].e;
       u.N = F;
       u.K = dm;
       u.x = x;
@@ -620,6 +705,8 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
       StreamGemm dn = o;
       dn.plan = w.s_down;
       dn.w = (const bf16*)m->w.w_down[l];
+      dn.w8 = m->f8_down[l].q;
+      dn.w_exp = m->f8_down[l].e;
       dn.K = F;
       dn.x = w.hmid;
       dn.ldx = F;
@@ -773,6 +860,9 @@ static fpd_status constrain_argmax_impl(fpd_model* m, int batch, int L, const vo
     g.epi = SEPI_ARGMAX;
     g.plan = w.s_lm;
     g.w = (const bf16*)m->w.lm_head;
+    g.fp8 = m->fp8;
+    g.w8 = m->f8_lm.q;
+    g.w_exp = m->f8_lm.e;
     g.M = n_rows;
     g.N = d.vocab;
     g.K = d.d_model;

@@ -75,6 +75,14 @@ struct Model {
   int device = 0;
   int num_sms = 0;
   float2* rope = nullptr;   // [max_pos][head_dim/2] (cos, sin), built in double on the host
+  // 8-bit copies of the weight-streamed matrices (fpd_model_enable_fp8), in one allocation the model owns
+  struct F8 {
+    const uint8_t* q = nullptr;   // E4M3 codes [rows, K]
+    const int8_t* e = nullptr;    // exponents [rows, K / 128]
+  };
+  bool fp8 = false;
+  void* fp8_buf = nullptr;
+  F8 f8_qkv[FPD_MAX_LAYERS], f8_o[FPD_MAX_LAYERS], f8_gu[FPD_MAX_LAYERS], f8_down[FPD_MAX_LAYERS], f8_lm;
 };
 
 // ---- small helpers -----------------------------------------------------------------------------------------

@@ -93,14 +93,20 @@ struct StreamGemm {
   unsigned long long* slots;      // SEPI_ARGMAX: [grid][16][2]
   float* logits;                  // SEPI_ARGMAX: [M][N] or null
   uint32_t test_extra_tx = 0;     // test hook only: bytes the first weight stage expects beyond what arrives
+  // 8-bit weights (E4M3 codes [rows, K] and exponents [rows, K/128], K a multiple of 128) instead of w
+  bool fp8 = false;
+  const uint8_t* w8 = nullptr;
+  const int8_t* w_exp = nullptr;
 };
 bool stream_shape_ok(const fpd_model_desc& d);
-StreamPlan stream_plan(int tiles, int K, int num_sms, bool split_ok);
+StreamPlan stream_plan(int tiles, int K, int num_sms, bool split_ok, bool fp8);
 size_t stream_part_floats(const StreamPlan& pl);
 cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st);
 cudaError_t stream_init_attributes();
 cudaError_t launch_embed_ss(bf16* x, float* ss, int* counters, int n_cnt, const bf16* embed, const int32_t* anchor,
                             int32_t mask_id, int B, int L, int d, int V, cudaStream_t st);
+cudaError_t launch_quantize_fp8(const bf16* w, int N, int K, int ld, uint8_t* codes, int8_t* exps, int num_sms,
+                                cudaStream_t st);
 cudaError_t launch_stream_decode(int32_t* tokens, float* margin, const unsigned long long* slots, int n_slots,
                                  int n_rows, cudaStream_t st);
 

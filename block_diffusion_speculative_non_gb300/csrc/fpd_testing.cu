@@ -81,7 +81,7 @@ fpd_status fpd_test_stream_timeout(void* workspace, size_t workspace_bytes, void
   g.M = 16;
   g.N = 128;
   g.K = 64;
-  g.plan = stream_plan(1, g.K, sms, false);
+  g.plan = stream_plan(1, g.K, sms, false, false);
   g.w = (const bf16*)base;                         // 128 x 64 weights: 16 KB
   g.x = (const bf16*)(base + 16384);               // 16 x 64 activations: 2 KB
   g.ldx = g.K;
@@ -96,6 +96,47 @@ fpd_status fpd_test_stream_timeout(void* workspace, size_t workspace_bytes, void
   return launch_stream_gemm(g, st) == cudaSuccess ? FPD_OK : FPD_ERR_CUDA;
 }
 
+size_t fpd_test_stream_gemm_workspace_bytes(int N, int K, int fp8) {
+  const int sms = current_sms();
+  if (!sms || N < 128 || N % 128 || K < 128 || K % 128) return 0;
+  const StreamPlan pl = stream_plan(N / 128, K, sms, true, fp8 != 0);
+  return 4096 + align_up(stream_part_floats(pl) * sizeof(float), 256) + align_up((size_t)(N / 128) * 16 * 4, 256) +
+         align_up((size_t)(N / 128) * 4, 256);
+}
+
+fpd_status fpd_test_stream_gemm(int fp8, int M, int N, int K, const void* X, const void* W, const void* W8,
+                                const void* Wexp, void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 1 || M > 16 || N < 128 || N % 128 || K < 128 || K % 128) return FPD_ERR_SHAPE;
+  if (!X || !y || !workspace || (fp8 ? (!W8 || !Wexp) : !W)) return FPD_ERR_INVALID_ARG;
+  const size_t need = fpd_test_stream_gemm_workspace_bytes(N, K, fp8);
+  if (!need || workspace_bytes < need) return FPD_ERR_CAPACITY;
+  const int sms = current_sms();
+  if (!sms || !attributes_ready()) return FPD_ERR_CUDA;
+  StreamGemm g{};
+  g.epi = SEPI_RESID;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.plan = stream_plan(N / 128, K, sms, true, fp8 != 0);
+  g.w = (const bf16*)W;
+  g.fp8 = fp8 != 0;
+  g.w8 = (const uint8_t*)W8;
+  g.w_exp = (const int8_t*)Wexp;
+  g.x = (const bf16*)X;
+  g.ldx = K;
+  g.xform = XF_COPY;
+  g.xres = (bf16*)y;
+  char* base = (char*)workspace;
+  size_t off = 0;
+  g.part = (float*)(base + off);
+  off = align_up(off + stream_part_floats(g.plan) * sizeof(float), 256);
+  g.ss_out = (float*)(base + off);
+  off = align_up(off + (size_t)(N / 128) * 16 * 4, 256);
+  g.counters = (int*)(base + off);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, need, st) != cudaSuccess) return FPD_ERR_CUDA;
+  return launch_stream_gemm(g, st) == cudaSuccess ? FPD_OK : FPD_ERR_CUDA;
+}
 
 size_t fpd_test_gemm_workspace_bytes(int M, int N, int K) {
   if (M < 1 || N < 1 || K < 64) return 0;

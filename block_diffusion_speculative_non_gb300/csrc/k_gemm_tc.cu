@@ -589,8 +589,24 @@ cudaError_t make_tmap(CUtensorMap* tm, const void* ptr, int rows, int cols, int 
   return make_tmap_nd(tm, ptr, 2, dims, strides, box);
 }
 
+static cudaError_t make_tmap_typed(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, int rank,
+                                   const uint64_t* dims, const uint64_t* strides, const uint32_t* box);
+
 cudaError_t make_tmap_nd(CUtensorMap* tm, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
                          const uint32_t* box) {
+  return make_tmap_typed(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rank, dims, strides, box);
+}
+
+cudaError_t make_tmap_u8(CUtensorMap* tm, const void* ptr, int rows, int cols, int ld, int box_rows) {
+  if (rows < 1 || cols < 128) return cudaErrorInvalidValue;
+  const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)ld};
+  const uint32_t box[2] = {128u, (uint32_t)box_rows};
+  return make_tmap_typed(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, 2, dims, strides, box);
+}
+
+static cudaError_t make_tmap_typed(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, int rank,
+                                   const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
   auto enc = get_encode();
   if (!enc) return cudaErrorNotSupported;
   if (((uintptr_t)ptr & 15) || rank < 2 || rank > 3) return cudaErrorInvalidValue;
@@ -604,7 +620,7 @@ cudaError_t make_tmap_nd(CUtensorMap* tm, const void* ptr, int rank, const uint6
     if (strides[i] % 16) return cudaErrorInvalidValue;
     st[i] = strides[i];
   }
-  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), d, st, b, estr,
+  CUresult r = enc(tm, dt, rank, const_cast<void*>(ptr), d, st, b, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;

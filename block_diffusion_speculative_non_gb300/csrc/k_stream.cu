@@ -34,18 +34,23 @@ constexpr int kSThreads = 192;
 constexpr int kMinStages = 8;                 // weight ring depth: 8 atoms (128 KB) in flight per CTA; deeper rings
 constexpr int kMaxStages = 8;                 // (10-14 atoms) measured slower on the 4B shape at batch 1
 constexpr int kTmemCols = 32;                 // two 16-column accumulators
+constexpr int kAccSlots = 8;                  // 8-bit weights: one 16-column accumulator per weight atom, 8 in flight
+constexpr int kTmemCols8 = kAccSlots * SBN;
 constexpr int kActGroup = 4;                  // activation atoms per readiness barrier
 constexpr int kMaxActGroups = 12;             // activation slices of up to 48 atoms (K <= 3072)
-// misc region: mbarriers full[S], empty[S], act_tma[G], act_ready[G], tfull[2], tempty[2] | TMEM slot, abort,
-// last-CTA flag | inverse RMS per token [16] | context length per request [16] | running top-2 per token [16][2]
-constexpr int kMiscFlags = 8 * (2 * kMaxStages + 2 * kMaxActGroups + 4);
+constexpr int kXsLd = 2 * kMaxActGroups;      // 8-bit activation scales per token: one per 128-element block
+// misc region: mbarriers full[S], empty[S], act_tma[G], act_ready[G], tfull[8], tempty[8] | TMEM slot, abort,
+// last-CTA flag | inverse RMS per token [16] | context length per request [16] | running top-2 per token [16][2] |
+// 8-bit activation scales [16][kXsLd]
+constexpr int kMiscFlags = 8 * (2 * kMaxStages + 2 * kMaxActGroups + 2 * kAccSlots);
 constexpr int kMiscInv = kMiscFlags + 16;
 constexpr int kMiscCtx = kMiscInv + SBN * 4;
 constexpr int kMiscRun = kMiscCtx + SBN * 4;
-constexpr int kMiscBytes = kMiscRun + SBN * 16;
+constexpr int kMiscXs = kMiscRun + SBN * 16;
+constexpr int kMiscBytes = kMiscXs + SBN * kXsLd * 4;
 
 struct StreamParams {
-  CUtensorMap tm_w;            // weights [rows, K] bf16, box 64 x (128, SwiGLU: 64)
+  CUtensorMap tm_w;            // weights [rows, K] bf16, box 64 x (128, SwiGLU: 64); 8-bit: E4M3 bytes, box 128 x ..
   CUtensorMap tm_x;            // activation source: 2-D [M rows, K] (box 64 x 16) or, for the LM head, 3-D
                                // [B][L-1 rows starting at block position 1][K] (box 64 x (L-1) x B)
   int x_rank;                  // 2 or 3
@@ -76,14 +81,23 @@ struct StreamParams {
   // SEPI_ARGMAX
   unsigned long long* slots;   // [gridDim][16][2]
   float* logits;               // [M][N] or null
+  const int8_t* w_exp;         // 8-bit weights: exponents [rows][K / 128]
+  int w_rows;                  // rows of the weight matrix
   int stages;                  // weight ring depth, kMinStages..kMaxStages
   uint32_t test_extra_tx;      // 0; a test makes the first stage's wait run out with it (bounded-wait check)
 };
 
-template <int EPI>
+// FP8: E4M3 weight atoms of 128 rows x 128 K (16 KB, the same bytes as a bf16 atom), the activation slice
+// quantised in place to E4M3 blocks of 128 K with one scale per (token, block), tcgen05.mma kind::f8f6f4 into one
+// accumulator slot per weight atom, and the epilogue threads adding each atom's product times
+// 2^(k_activation + k_weight) in fp32 registers.
+template <int EPI, bool FP8>
 __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_constant__ StreamParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int KA = FP8 ? 2 : 1;                             // 64-K activation atoms per weight atom
+  constexpr int n_slots = FP8 ? kAccSlots : 2;
+  constexpr uint32_t tmem_cols = FP8 ? kTmemCols8 : kTmemCols;
   const int n_act = p.k_split / SBK;                          // activation atoms of one split (LM head: all K)
   uint8_t* ring = smem;
   const int n_stages = p.stages;
@@ -98,8 +112,10 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
   float* s_inv = reinterpret_cast<float*>(misc + kMiscInv);
   int* s_ctx = reinterpret_cast<int*>(misc + kMiscCtx);
   unsigned long long* s_run = reinterpret_cast<unsigned long long*>(misc + kMiscRun);
+  float* s_xs = reinterpret_cast<float*>(misc + kMiscXs);
   const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kMaxStages, actt0 = empty0 + 8 * kMaxStages,
-                 actr0 = actt0 + 8 * kMaxActGroups, tfull0 = actr0 + 8 * kMaxActGroups, tempty0 = tfull0 + 16;
+                 actr0 = actt0 + 8 * kMaxActGroups, tfull0 = actr0 + 8 * kMaxActGroups,
+                 tempty0 = tfull0 + 8 * kAccSlots;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   pdl_trigger();
@@ -116,7 +132,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       tc::mbar_init(actt0 + 8 * g, 1);
       tc::mbar_init(actr0 + 8 * g, 1);
     }
-    for (int a = 0; a < 2; a++) {
+    for (int a = 0; a < n_slots; a++) {
       tc::mbar_init(tfull0 + 8 * a, 1);
       tc::mbar_init(tempty0 + 8 * a, 4);
     }
@@ -124,7 +140,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
     tc::fence_barrier_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), tmem_cols);
     tc::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -139,15 +155,16 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // work item t -> output tile, K range
+  // work item t -> output tile, K range, weight atoms
   auto item = [&](int t, int& tile, int& split, int& k0, int& nkb) {
     tile = persistent ? t : t % p.tiles;
     split = persistent ? 0 : t / p.tiles;
     k0 = split * p.k_split;
-    nkb = (min(p.K, k0 + p.k_split) - k0) / SBK;
+    nkb = (min(p.K, k0 + p.k_split) - k0) / (SBK * KA);
   };
   int tile0, split0, k00, nkb0;   // the CTA's first item: its K slice is the activation slice
   item(blockIdx.x < total ? blockIdx.x : 0, tile0, split0, k00, nkb0);
+  const int nxa0 = nkb0 * KA;     // its 64-K activation atoms
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -158,11 +175,12 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       auto issue_w = [&]() {
         const uint32_t fb = full0 + 8 * stage, dst = tc::smem_u32(ring + stage * W_ATOM);
         tc::mbar_arrive_expect_tx(fb, W_ATOM + (issued == 0 ? p.test_extra_tx : 0u));
+        const int kx = k0 + kb * SBK * KA;   // element (= byte, 8-bit) column of the atom
         if (EPI == SEPI_SWIGLU) {   // atom = [gate rows f0..f0+63 ; up rows F+f0..F+f0+63]
-          tc::tma_load_2d(dst, &p.tm_w, k0 + kb * SBK, tile * 64, fb);
-          tc::tma_load_2d(dst + W_ATOM / 2, &p.tm_w, k0 + kb * SBK, p.N + tile * 64, fb);
+          tc::tma_load_2d(dst, &p.tm_w, kx, tile * 64, fb);
+          tc::tma_load_2d(dst + W_ATOM / 2, &p.tm_w, kx, p.N + tile * 64, fb);
         } else {
-          tc::tma_load_2d(dst, &p.tm_w, k0 + kb * SBK, tile * SBM, fb);
+          tc::tma_load_2d(dst, &p.tm_w, kx, tile * SBM, fb);
         }
         issued++;
         if (++stage == n_stages) { stage = 0; phase ^= 1; }
@@ -179,8 +197,8 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       pdl_wait();
       if (blockIdx.x < total) {
         const bool gains = p.xform != XF_COPY;
-        for (int g = 0; g * kActGroup < nkb0; g++) {
-          const int a0 = g * kActGroup, na = min(kActGroup, nkb0 - a0);
+        for (int g = 0; g * kActGroup < nxa0; g++) {
+          const int a0 = g * kActGroup, na = min(kActGroup, nxa0 - a0);
           const uint32_t bar = actt0 + 8 * g;
           tc::mbar_arrive_expect_tx(bar, na * p.x_atom_bytes + (gains ? na * G_ATOM : 0));
           for (int a = a0; a < a0 + na; a++) {
@@ -205,12 +223,40 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
           tc::mbar_wait(full0 + 8 * stage, phase);
         }
         if (blockIdx.x < total)
-          for (int g = 0; g * kActGroup < nkb0; g++) tc::mbar_wait(actt0 + 8 * g, 0);
+          for (int g = 0; g * kActGroup < nxa0; g++) tc::mbar_wait(actt0 + 8 * g, 0);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    if (lane == 0 && FP8) {
+      // one accumulator slot per weight atom; the epilogue threads free a slot once they have read it
+      constexpr uint32_t idesc = tc::idesc_e4m3_f32(SBM, SBN);
+      int stage = 0, c = 0;
+      uint32_t phase = 0;
+      const uint32_t xs = tc::smem_u32(act);
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += stride) {
+        int tile, split, k0, nkb;
+        item(t, tile, split, k0, nkb);
+        for (int kb = 0; kb < nkb && !*abort_flag; kb++, c++) {
+          // 8-bit block kb is ready once its activation group has been quantised
+          if ((kb * KA) % kActGroup == 0 && !tc::mbar_wait(actr0 + 8 * (kb * KA / kActGroup), 0)) { *abort_flag = 1; break; }
+          const int slot = c % kAccSlots;
+          if (c >= kAccSlots && !tc::mbar_wait(tempty0 + 8 * slot, ((c / kAccSlots) & 1) ^ 1)) { *abort_flag = 1; break; }
+          if (!tc::mbar_wait(full0 + 8 * stage, phase)) { *abort_flag = 1; break; }
+          tc::tc_fence_after();
+          const uint32_t ws = tc::smem_u32(ring + stage * W_ATOM), d_tmem = tmem_base + slot * SBN;
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++) {   // K = 32 bytes per instruction
+            const uint64_t da = tc::sw128_kmajor_desc(ws + kk * 32);
+            const uint64_t db = tc::sw128_kmajor_desc(xs + kb * X_ATOM + kk * 32);
+            tc::umma_f8(d_tmem, da, db, idesc, kk > 0 ? 1u : 0u);
+          }
+          tc::umma_commit(empty0 + 8 * stage);
+          tc::umma_commit(tfull0 + 8 * slot);
+          if (++stage == n_stages) { stage = 0; phase ^= 1; }
+        }
+      }
+    } else if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(SBM, SBN);
       // activation atoms are ready group by group: straight from TMA, or after the norm transform
       const uint32_t rdy0 = p.xform == XF_COPY ? actt0 : actr0;
@@ -253,40 +299,76 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       s_ctx[et] = clamp_ctx(cl, p.t_cap);
     }
     if (EPI == SEPI_ARGMAX && et < SBN) s_run[2 * et] = s_run[2 * et + 1] = 0ull;
-    if (blockIdx.x < total && p.xform != XF_COPY) {
+    if (blockIdx.x < total && (FP8 || p.xform != XF_COPY)) {
       if (p.xform == XF_NORM_FULL) {   // 1/rms from the whole rows: every group first
-        for (int g = 0; g * kActGroup < nkb0; g++)
+        for (int g = 0; g * kActGroup < nxa0; g++)
           if (!tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
-        inv_from_rows(act, nkb0, p.K, p.eps, s_inv, et);
+        inv_from_rows(act, nxa0, p.K, p.eps, s_inv, et);
       }
       epi_bar();   // s_inv complete
-      for (int g = 0; g * kActGroup < nkb0; g++) {
-        if (p.xform == XF_NORM && !tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
-        norm_atoms(act, gbuf, s_inv, g * kActGroup, min(kActGroup, nkb0 - g * kActGroup), et);
+      for (int g = 0; g * kActGroup < nxa0; g++) {
+        const int a0 = g * kActGroup, na = min(kActGroup, nxa0 - a0);
+        if (p.xform != XF_NORM_FULL && !tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
+        if (p.xform != XF_COPY) norm_atoms(act, gbuf, s_inv, a0, na, et);
+        if (FP8) {
+          epi_bar();   // the normed rows are complete
+          quant_atoms(act, s_xs, kXsLd, a0, na, p.M, et);
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
         epi_bar();
         if (et == 0) tc::mbar_arrive(actr0 + 8 * g);
       }
     }
 
-    int it = 0;
+    int it = 0, c8 = 0;
     for (int t = blockIdx.x; t < total; t += stride, it++) {
       int tile, split, k0, nkb;
       item(t, tile, split, k0, nkb);
-      const int acc = it & 1;
       float xv[16];
       if (EPI == SEPI_RESID) resid_preload(xv, p.xres, p.N, tile, p.M, row_in_tile);
-      if (!tc::mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1)) *abort_flag = 1;
-      tc::tc_fence_after();
       float v[16];
-      tc::tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * SBN, v);
-      if (*abort_flag) {
+      if (FP8) {
+        // v = sum over the item's weight atoms of (block product) 2^(k_token + k_row); this thread's weight row
 #pragma unroll
         for (int j = 0; j < 16; j++) v[j] = 0.f;
+        const int wrow = EPI == SEPI_SWIGLU
+                             ? (row_in_tile < 64 ? tile * 64 + row_in_tile : p.N + tile * 64 + row_in_tile - 64)
+                             : tile * SBM + row_in_tile;
+        const bool wok = wrow < p.w_rows;
+        const int8_t* we = p.w_exp + (size_t)(wok ? wrow : 0) * (p.K / 128) + k0 / 128;
+        int ew = (wok && nkb > 0) ? we[0] : 0;
+        for (int kb = 0; kb < nkb; kb++, c8++) {
+          const int ew_next = (wok && kb + 1 < nkb) ? we[kb + 1] : 0;
+          const int slot = c8 % kAccSlots;
+          if (!*abort_flag && !tc::mbar_wait(tfull0 + 8 * slot, (c8 / kAccSlots) & 1)) *abort_flag = 1;
+          tc::tc_fence_after();
+          float u[16];
+          tc::tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + slot * SBN, u);
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tempty0 + 8 * slot);
+          const float sw = exp2_int(ew);
+#pragma unroll
+          for (int j = 0; j < 16; j++) v[j] = fmaf(u[j], s_xs[j * kXsLd + kb] * sw, v[j]);
+          ew = ew_next;
+        }
+        if (*abort_flag) {
+#pragma unroll
+          for (int j = 0; j < 16; j++) v[j] = 0.f;
+        }
+      } else {
+        const int acc = it & 1;
+        if (!tc::mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1)) *abort_flag = 1;
+        tc::tc_fence_after();
+        tc::tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * SBN, v);
+        if (*abort_flag) {
+#pragma unroll
+          for (int j = 0; j < 16; j++) v[j] = 0.f;
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tempty0 + 8 * acc);
       }
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tempty0 + 8 * acc);
 
       if (EPI == SEPI_QKV || EPI == SEPI_RESID) {
         if (splitk_last(v, p.part, p.counters, split, p.splits, tile, p.tiles, row_in_tile, et, s_flag)) {
@@ -359,7 +441,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, kTmemCols);
+    tc::tmem_dealloc(tmem_base, tmem_cols);
   }
 }
 
@@ -378,9 +460,19 @@ int stream_stages(int act_atoms) {
 }
 
 template <int EPI>
-cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
+cudaError_t launch_stream(const StreamParams& p, int grid, bool fp8, cudaStream_t st) {
   const size_t smem = stream_smem_bytes(p.k_split / SBK, p.stages);
-  return launch_k(stream_gemm_kernel<EPI>, grid, kSThreads, smem, st, p);
+  if (fp8) return launch_k(stream_gemm_kernel<EPI, true>, grid, kSThreads, smem, st, p);
+  return launch_k(stream_gemm_kernel<EPI, false>, grid, kSThreads, smem, st, p);
+}
+
+template <int EPI>
+cudaError_t stream_attr() {
+  cudaError_t e = cudaFuncSetAttribute(stream_gemm_kernel<EPI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       227 * 1024);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_gemm_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  return e;
 }
 
 // ---- embedding gather for the few-token path: x rows + their sums of squares; clears the split-K counters ---------
@@ -453,17 +545,19 @@ bool stream_shape_ok(const fpd_model_desc& d) {
          d.d_model / SBK <= kActGroup * kMaxActGroups;
 }
 
-StreamPlan stream_plan(int tiles, int K, int num_sms, bool split_ok) {
+StreamPlan stream_plan(int tiles, int K, int num_sms, bool split_ok, bool fp8) {
   StreamPlan pl{};
   pl.tiles = tiles;
-  const int nkb = K / SBK;
+  const int gran = fp8 ? 2 : 1;   // 64-K atoms per weight atom (8-bit atoms hold 128 K)
+  const int nu = K / (SBK * gran);
   int splits = 1;
-  if (split_ok && tiles < num_sms) splits = std::max(1, std::min(num_sms / tiles, nkb / 2));
-  int kb_per = ceil_div(nkb, splits);
+  if (split_ok && tiles < num_sms) splits = std::max(1, std::min(num_sms / tiles, nu / 2));
+  int u_per = ceil_div(nu, splits);
   // the activation slice must fit next to the ring
-  while (stream_smem_bytes(kb_per) > 227 * 1024) kb_per = ceil_div(kb_per, 2);
+  while (u_per > 1 && stream_smem_bytes(u_per * gran) > 227 * 1024) u_per = ceil_div(u_per, 2);
+  const int kb_per = u_per * gran;
   pl.k_split = kb_per * SBK;
-  pl.splits = ceil_div(nkb, kb_per);
+  pl.splits = ceil_div(nu, u_per);
   pl.grid = tiles * pl.splits;
   return pl;
 }
@@ -477,7 +571,11 @@ cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st) {
   const int w_rows = g.epi == SEPI_SWIGLU ? 2 * g.N : g.N;
   if (g.M < 1 || g.M > SBN || g.K % SBK || g.plan.k_split / SBK > kActGroup * kMaxActGroups)
     return cudaErrorInvalidValue;
-  cudaError_t e = make_tmap(&p.tm_w, g.w, w_rows, g.K, g.K, box_rows);
+  if (g.fp8 && (g.K % 128 || g.plan.k_split % 128 || !g.w8 || !g.w_exp)) return cudaErrorInvalidValue;
+  cudaError_t e = g.fp8 ? make_tmap_u8(&p.tm_w, g.w8, w_rows, g.K, g.K, box_rows)
+                        : make_tmap(&p.tm_w, g.w, w_rows, g.K, g.K, box_rows);
+  p.w_exp = g.w_exp;
+  p.w_rows = w_rows;
   if (e != cudaSuccess) return e;
   if (g.xform == XF_NORM_FULL) {
     // rows of the LM head are block positions 1..L-1 of every request: a 3-D view [B][L-1][K] of hidden
@@ -528,21 +626,18 @@ cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st) {
   p.slots = g.slots;
   p.logits = g.logits;
   switch (g.epi) {
-    case SEPI_QKV: return launch_stream<SEPI_QKV>(p, g.plan.grid, st);
-    case SEPI_RESID: return launch_stream<SEPI_RESID>(p, g.plan.grid, st);
-    case SEPI_SWIGLU: return launch_stream<SEPI_SWIGLU>(p, g.plan.grid, st);
-    default: return launch_stream<SEPI_ARGMAX>(p, g.plan.grid, st);
+    case SEPI_QKV: return launch_stream<SEPI_QKV>(p, g.plan.grid, g.fp8, st);
+    case SEPI_RESID: return launch_stream<SEPI_RESID>(p, g.plan.grid, g.fp8, st);
+    case SEPI_SWIGLU: return launch_stream<SEPI_SWIGLU>(p, g.plan.grid, g.fp8, st);
+    default: return launch_stream<SEPI_ARGMAX>(p, g.plan.grid, g.fp8, st);
   }
 }
 
 cudaError_t stream_init_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(stream_gemm_kernel<SEPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(stream_gemm_kernel<SEPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(stream_gemm_kernel<SEPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(stream_gemm_kernel<SEPI_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  cudaError_t e = stream_attr<SEPI_QKV>();
+  if (e == cudaSuccess) e = stream_attr<SEPI_RESID>();
+  if (e == cudaSuccess) e = stream_attr<SEPI_SWIGLU>();
+  if (e == cudaSuccess) e = stream_attr<SEPI_ARGMAX>();
   return e;
 }
 

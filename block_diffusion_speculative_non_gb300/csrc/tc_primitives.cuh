@@ -147,6 +147,25 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with E4M3 A and B (K-major, format code 0 for both), fp32
+// accumulator, shape M x N.  One instruction covers K = 32 (32 bytes of each operand row).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                      // accumulator format: f32
+         | (0u << 7)                    // A format: E4M3
+         | (0u << 10)                   // B format: E4M3
+         | ((uint32_t)(N >> 3) << 17)   // N / 8
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on bar when every tcgen05 operation issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -173,4 +192,6 @@ cudaError_t make_tmap(CUtensorMap* tm, const void* ptr, int rows, int cols, int 
 // bf16 tensor of rank 2 or 3 (dims innermost first, byte strides of dims 1.., box in elements), 128-byte swizzle
 cudaError_t make_tmap_nd(CUtensorMap* tm, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
                          const uint32_t* box);
+// byte matrix [rows, cols] (row stride ld bytes), box 128 bytes x box_rows, 128-byte swizzle (E4M3 weight atoms)
+cudaError_t make_tmap_u8(CUtensorMap* tm, const void* ptr, int rows, int cols, int ld, int box_rows);
 }  // namespace fpd

@@ -9,7 +9,8 @@ import numpy as np
 import torch
 
 from . import (FPD_VERIFY_SCHEMA, FPD_VERIFY_TEXT, MAX_LAYERS, ModelDesc, Weights, fpd_constrain_argmax,
-               fpd_draft_block, fpd_kv_store_bytes, fpd_model_create, fpd_model_destroy, fpd_prepare_context,
+               fpd_draft_block, fpd_kv_store_bytes, fpd_model_create, fpd_model_destroy, fpd_model_enable_fp8,
+               fpd_prepare_context,
                fpd_prepare_context_rows, fpd_sd_advance, fpd_verify, fpd_verify_prefix, fpd_workspace_bytes,
                make_layout)
 
@@ -25,9 +26,10 @@ def to_device_bf16(a, device) -> torch.Tensor:
 
 class Drafter:
     """One drafter model on one GPU, sized for up to `max_batch` requests of `t_cap` context positions and
-    blocks of up to `max_block_len` positions."""
+    blocks of up to `max_block_len` positions.  fp8=True adds the 8-bit copies of the streamed matrices
+    (fpd_model_enable_fp8): calls of at most 16 positions then run on them."""
 
-    def __init__(self, shape, weights, max_batch: int, max_block_len: int, t_cap: int, device="cuda"):
+    def __init__(self, shape, weights, max_batch: int, max_block_len: int, t_cap: int, device="cuda", fp8=False):
         self.shape = shape
         self.device = torch.device(device)
         self.max_batch, self.max_block_len, self.t_cap = max_batch, max_block_len, t_cap
@@ -44,6 +46,8 @@ class Drafter:
             for l in range(shape.n_layers):
                 arr[l] = self.layers[l][name].data_ptr()
         self.handle = fpd_model_create(desc, W)
+        if fp8:
+            fpd_model_enable_fp8(self.handle)
         self.kv_bytes = fpd_kv_store_bytes(self.handle, max_batch, t_cap)
         self.ws_bytes = fpd_workspace_bytes(self.handle, max_batch, max_block_len, t_cap)
         self.kv_store = torch.zeros(self.kv_bytes // 2, dtype=torch.bfloat16, device=self.device)

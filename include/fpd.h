@@ -150,6 +150,35 @@ enum { FPD_VERIFY_TEXT = 0, FPD_VERIFY_SCHEMA = 1 };
 fpd_status fpd_model_create(const fpd_model_desc* desc, const fpd_weights* weights, fpd_model** out);
 void fpd_model_destroy(fpd_model* model);
 
+/* ---- f2: 8-bit weights for the weight-streaming calls ----------------------------------------------------------
+ * FlashDrive §3.4 "Quantization": low-bit weights cut the bytes a memory-bound decoding step loads, and 8-bit
+ * activations let the products run on 8-bit matrix units.  Here both operands of the streamed GEMMs take E4M3
+ * (the OCP OFP8 format: bias 7, largest finite 448) with one power-of-two scale per 128 consecutive elements of a
+ * row:
+ *   exponent k = the smallest integer with amax 2^-k <= 448 (amax: the group's largest magnitude; k clamped to
+ *   [-126, 127]; k = 0 for an all-zero group); code = the E4M3 value nearest to x 2^-k, ties to the even code, a
+ *   zero result encoded +0; the group stands for decode(code) 2^k.
+ *
+ * fpd_model_enable_fp8 quantises, once, the model's QKV, O, gate/up and down matrices of every layer and the LM
+ * head into a device allocation the model owns (about half the bytes of the bf16 matrices; freed by
+ * fpd_model_destroy) and synchronises the stream.  From then on the calls that stream these weights use them:
+ *   fpd_draft_block with batch * block_len <= 16, and fpd_constrain_argmax without a layout and with
+ *   batch * (block_len - 1) <= 16.
+ * In those calls each projection quantises its bf16 input rows the same way (per token, per 128 elements) and
+ * computes y = sum over groups of (codes . codes) 2^(k_x + k_w) in fp32.  Every other call (context preparation,
+ * larger blocks, constrained LM heads) keeps the bf16 weights.  The borrowed bf16 weights must stay valid.
+ * Needs d_model, n_q_heads * head_dim and d_ff to be multiples of 128 (FPD_ERR_UNSUPPORTED otherwise); calling it
+ * again is a no-op.  Not capturable in a CUDA graph (it allocates and synchronises). */
+fpd_status fpd_model_enable_fp8(fpd_model* model, void* stream);
+/* 1 after a successful fpd_model_enable_fp8, else 0. */
+int32_t fpd_model_fp8_enabled(const fpd_model* model);
+
+/* The quantisation above on any bf16 matrix, on the device (stream-ordered, asynchronous).
+ *   w      device [rows, ld] bf16, 16-byte aligned; cols a positive multiple of 128, ld >= cols and a multiple of 8
+ *   codes  device [rows, cols] uint8 E4M3 codes, 16-byte aligned
+ *   exps   device [rows, cols / 128] int8 exponents k */
+fpd_status fpd_quantize_fp8(const void* w, int rows, int cols, int ld, void* codes, void* exps, void* stream);
+
 /* Bytes of the caller-allocated context KV store for `batch` requests of at most t_cap context positions.
  * Layout: [layer][request][K|V][kv_head][t_cap][head_dim] bf16. */
 size_t fpd_kv_store_bytes(const fpd_model* model, int batch, int t_cap);

@@ -77,7 +77,8 @@ def _configure(l):
     l.oracle_prepare_context.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _i32p,
                                          _i32p, ctypes.POINTER(_u16p), _u16p, ctypes.c_int]
     l.oracle_draft_block.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
-                                     ctypes.c_int, _i32p, _i32p, ctypes.c_int32, _u16p, _u16p, ctypes.c_int]
+                                     ctypes.c_int, _i32p, _i32p, ctypes.c_int32, _u16p, _u16p, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, _u16p]
     l.oracle_constrain_argmax.argtypes = [ctypes.POINTER(_OracleModel), ctypes.c_int, ctypes.c_int, _u16p,
                                           ctypes.c_int, _i32p, _i32p, _i16p, _i32p, _f64p, _f64p, ctypes.c_int]
     l.oracle_e4m3_decode.restype = ctypes.c_double
@@ -319,25 +320,29 @@ def prepare_context(model: Model, row_off, feats, t_cap, batch=None, pos_start=N
 FEW_TOKENS = 16   # calls with at most this many positions run the weight-streaming (FP8-capable) path
 
 
-def draft_block(model: Model, kv_store, t_cap, ctx_len, anchor, mask_id, block_len, want_layers=False, fp8=None):
+def draft_block(model: Model, kv_store, t_cap, ctx_len, anchor, mask_id, block_len, want_layers=False, fp8=None,
+                layers=None, x_in=None):
     """Returns hidden [B*L, d] (bf16 bits) and, when asked, the per-layer residual [n_layers, B*L, d].
-    fp8 None: the FP8 projections exactly when the model has FP8 copies and the call has at most 16 positions."""
+    fp8 None: the FP8 projections exactly when the model has FP8 copies and the call has at most 16 positions.
+    layers (l0, l1) with x_in [B*L, d] bf16 bits: only layers l0..l1-1, starting from the residual x_in."""
     sh = model.shape
     ctx_len = _c(ctx_len, np.int32)
     anchor = _c(anchor, np.int32)
     B = len(anchor)
     kv = _c(kv_store, np.uint16)
     hidden = np.empty((B * block_len, sh.d_model), dtype=np.uint16)
-    layers = np.empty((sh.n_layers, B * block_len, sh.d_model), dtype=np.uint16) if want_layers else None
+    lay = np.zeros((sh.n_layers, B * block_len, sh.d_model), dtype=np.uint16) if want_layers else None
     if fp8 is None:
         fp8 = model.fp8 and B * block_len <= FEW_TOKENS
     assert not fp8 or model.fp8
+    l0, l1 = (0, sh.n_layers) if layers is None else layers
+    xi = None if x_in is None else _c(x_in, np.uint16).reshape(B * block_len, sh.d_model)
     rc = lib().oracle_draft_block(ctypes.byref(model.c), B, block_len, _p(kv, _u16p), int(t_cap),
                                   _p(ctx_len, _i32p), _p(anchor, _i32p), int(mask_id), _p(hidden, _u16p),
-                                  _p(layers, _u16p), int(bool(fp8)))
+                                  _p(lay, _u16p), int(bool(fp8)), int(l0), int(l1), _p(xi, _u16p))
     if rc:
         raise ValueError("oracle_draft_block: bad arguments")
-    return (hidden, layers) if want_layers else hidden
+    return (hidden, lay) if want_layers else hidden
 
 
 def constrain_argmax(model: Model, hidden, batch, block_len, layout=None, want_logits=False, fp8=None):

@@ -396,13 +396,15 @@ int oracle_prepare_context(const oracle_model* m, int batch, int total_rows, con
  *   xn = bf16(RMSNorm_mlp(x)); u = bf16(silu(xn . Wg^T) * (xn . Wu^T)); x = bf16(x + u . Wdown^T)
  * hidden_out [B*L, d] = x after the last layer; layer_hidden (optional) [n_layers, B*L, d].
  * fp8 != 0: the four projections take the FP8 form of the f2 section (weights from the q_ and e_ copies, the
- * bf16 activations xn, o, xn, u quantised per 128-element group of each row). */
+ * bf16 activations xn, o, xn, u quantised per 128-element group of each row).
+ * Layers [l0, l1) only, starting from the residual x_in [B*L, d] (bf16) when given, else from the embedding rows
+ * (a stage of the pass fed another implementation's residual stream). */
 int oracle_draft_block(const oracle_model* m, int batch, int L, const uint16_t* kv_store, int t_cap,
                        const int32_t* ctx_len, const int32_t* anchor, int32_t mask_id, uint16_t* hidden_out,
-                       uint16_t* layer_hidden, int fp8) {
+                       uint16_t* layer_hidden, int fp8, int l0, int l1, const uint16_t* x_in) {
   const int d = m->d, h = m->h, nq = m->nq, nkv = m->nkv, F = m->F;
   const int M = batch * L, nqkv = (nq + 2 * nkv) * h, grp = nq / nkv;
-  if (L < 1 || batch < 1 || nq % nkv) return -1;
+  if (L < 1 || batch < 1 || nq % nkv || l0 < 0 || l1 > m->n_layers || l0 >= l1) return -1;
   for (int b = 0; b < batch; b++) {
     if (ctx_len[b] < 0 || ctx_len[b] > t_cap) return -1;
     if (anchor[b] < 0 || anchor[b] >= m->V) return -1;
@@ -422,10 +424,11 @@ int oracle_draft_block(const oracle_model* m, int batch, int L, const uint16_t* 
   for (int b = 0; b < batch; b++)
     for (int j = 0; j < L; j++) {
       int id = j == 0 ? anchor[b] : mask_id;
-      for (int k = 0; k < d; k++) x[((size_t)b * L + j) * d + k] = bf(m->embed[(size_t)id * d + k]);
+      size_t r = (size_t)b * L + j;
+      for (int k = 0; k < d; k++) x[r * d + k] = x_in ? bf(x_in[r * d + k]) : bf(m->embed[(size_t)id * d + k]);
     }
 
-  for (int l = 0; l < m->n_layers; l++) {
+  for (int l = l0; l < l1; l++) {
     for (int r = 0; r < M; r++) {
       oracle_rmsnorm(d, x + (size_t)r * d, m->attn_norm[l], m->eps, xn + (size_t)r * d);
       for (int k = 0; k < d; k++) xn[(size_t)r * d + k] = rbf(xn[(size_t)r * d + k]);

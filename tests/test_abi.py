@@ -147,3 +147,16 @@ def test_speculative_step_calls_reject_bad_arguments(fpd):
     assert lib.fpd_sd_advance(1, 16, 64, a, a, a, None, a, None) == 1
     feats = (ctypes.c_void_p * 1)(a)
     assert lib.fpd_prepare_context_rows(None, 1, 4, a, a, None, feats, a, 64, a, 1 << 20, None) == 1
+
+
+def test_fp8_calls_validate_on_the_host(fpd):
+    """fpd_model_enable_fp8 and fpd_quantize_fp8 reject bad arguments before touching the device."""
+    lib = fpd.lib()
+    a = 1 << 20
+    assert lib.fpd_model_enable_fp8(None, None) == 1
+    assert lib.fpd_model_fp8_enabled(None) == 0
+    assert lib.fpd_quantize_fp8(None, 4, 128, 128, a, a, None) == 1
+    assert lib.fpd_quantize_fp8(a, 4, 100, 128, a, a, None) == 2      # cols not a multiple of 128
+    assert lib.fpd_quantize_fp8(a, 4, 128, 120, a, a, None) == 2      # ld < cols
+    assert lib.fpd_quantize_fp8(a, 0, 128, 128, a, a, None) == 2
+    assert lib.fpd_quantize_fp8(a + 8, 4, 128, 128, a, a, None) == 1  # misaligned source

@@ -225,3 +225,19 @@ def test_fp8_routing_rule(oracle_lib):
     _, _, dl = oracle_lib.constrain_argmax(m, hid, 1, Lc, layout=lay, want_logits=True)
     _, _, bl = oracle_lib.constrain_argmax(m, hid, 1, Lc, layout=lay, want_logits=True, fp8=False)
     np.testing.assert_array_equal(dl, bl)                      # a layout: bf16
+
+
+def test_layer_range_composes(oracle_lib):
+    """Running layers [0, 2) and then [2, n) from that residual equals the whole pass, bf16 and FP8."""
+    s, w, B, L, T, off, feats = _tiny_case()
+    m = oracle_lib.Model(s, w, fp8=True)
+    kv = oracle_lib.prepare_context(m, off, feats, T)
+    args = (kv, T, np.array([T], np.int32), np.array([7], np.int32), s.vocab - 1, L)
+    for fp8 in (False, True):
+        whole, lay = oracle_lib.draft_block(m, *args, want_layers=True, fp8=fp8)
+        first = oracle_lib.draft_block(m, *args, fp8=fp8, layers=(0, 2))
+        np.testing.assert_array_equal(first, lay[1])
+        rest = oracle_lib.draft_block(m, *args, fp8=fp8, layers=(2, s.n_layers), x_in=first)
+        np.testing.assert_array_equal(rest, whole)
+        one = oracle_lib.draft_block(m, *args, fp8=fp8, layers=(3, 4), x_in=lay[2])
+        np.testing.assert_array_equal(one, lay[3])

@@ -1,0 +1,260 @@
+"""GPU: f2, the 8-bit weight copies (FlashDrive §3.4 "Quantization"; reading R25) against the oracle.
+
+  - fpd_quantize_fp8: codes and exponents bit-exact against the oracle's quantiser, on random rows, rows with a
+    row stride, and groups built to sit on the rounding and exponent boundaries;
+  - the few-token drafter pass and the unconstrained LM head on an 8-bit model (the streamed GEMMs with E4M3
+    operands on tcgen05 kind::f8f6f4) against the oracle's FP8 pass, layer by layer, at the tiny shape and at the
+    4B shape's batch-1 text size;
+  - the routing rule: the same 8-bit model keeps the bf16 weights for calls of more than 16 positions."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from _util import (assert_logits, assert_margin, assert_rows_close, assert_tokens, assert_tokens_chain, bits_of,
+                   dev_i32, f64, row_rel_err)
+from test_gpu_parity import _stagewise
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+# Reading R25: one layer of the 8-bit pass fed the same residual.  Its four activation roundings to E4M3 see the
+# GPU's bf16 activations, which differ from the oracle's by one bf16 ulp at some elements (R18).  Such an element
+# changes its E4M3 code with probability about 2^-4 (a code step is 2^4 bf16 ulps) and then moves by 2^4 ulps, so
+# the output differences have about (2^-4 * 2^8)^(1/2) = 4 times the RMS of the bf16 pass: the layer bound is 4 x
+# the 2e-2 hidden bound.  The GEMMs themselves are checked on identical inputs to bf16 output rounding.
+FP8_LAYER_TOL = 4 * 2e-2
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_diffusion_speculative_non_gb300 as p
+    p.lib()
+    return p
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+def _boundary_rows(rng, n, K):
+    """bf16 rows whose groups put amax on the exponent boundaries (448 2^k exactly, just above, 224 2^k) and
+    elements on E4M3 rounding ties (midpoints between neighbouring codes, times 2^k), zero groups and tiny groups."""
+    finite = np.array([(1 + m / 8) * 2.0 ** (e - 7) for e in range(1, 16) for m in range(8) if not (e == 15 and m == 7)])
+    mids = (finite[1:] + finite[:-1]) / 2
+    rows = np.zeros((n, K), np.float32)
+    for r in range(n):
+        for g in range(K // 128):
+            k = int(rng.integers(-30, 10))
+            kind = (r * 7 + g) % 5
+            x = rng.choice(mids, size=128) * rng.choice([-1.0, 1.0], size=128)
+            if kind == 0:
+                x[0] = 448.0
+            elif kind == 1:
+                x[0] = 448.0 * (1 + 2.0 ** -7)     # one bf16 step above: the next exponent
+            elif kind == 2:
+                x = x * 0.5
+                x[0] = 224.0
+            elif kind == 3:
+                x[:] = 0.0
+            else:
+                x = x * 2.0 ** -100              # tiny values: the lower exponent clamp, bf16 subnormals
+            rows[r, g * 128:(g + 1) * 128] = x * 2.0 ** k
+    return synth.f32_to_bf16_bits(rows)
+
+
+def test_quantize_bit_exact(pkg, orc):
+    rng = np.random.default_rng(808)
+    cases = [
+        synth.f32_to_bf16_bits((rng.normal(size=(300, 640)) * 0.02).astype(np.float32)),
+        synth.f32_to_bf16_bits((rng.standard_cauchy(size=(64, 1024))).astype(np.float32)),
+        _boundary_rows(rng, 40, 512),
+    ]
+    for i, bits in enumerate(cases):
+        N, K = bits.shape
+        ld = K + 128 if i == 1 else K                       # a row stride wider than the row
+        src = np.zeros((N, ld), np.uint16)
+        src[:, :K] = bits
+        w = torch.from_numpy(src.view(np.int16)).to(DEV)
+        codes = torch.empty(N, K, dtype=torch.uint8, device=DEV)
+        exps = torch.empty(N, K // 128, dtype=torch.int8, device=DEV)
+        pkg.fpd_quantize_fp8(w, N, K, ld, codes, exps)
+        torch.cuda.synchronize()
+        qc, qe = orc.quantize_fp8(bits)
+        np.testing.assert_array_equal(exps.cpu().numpy(), qe, err_msg=f"case {i} exponents")
+        got = codes.cpu().numpy()
+        bad = np.flatnonzero(got != qc)
+        assert bad.size == 0, (f"case {i}: {bad.size} codes differ, first at {bad[0]}: "
+                               f"{got.ravel()[bad[0]]:#x} vs {qc.ravel()[bad[0]]:#x}")
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 6144, 2560), (16, 2560, 4096), (16, 2560, 9728), (5, 512, 1536),
+                                   (1, 128, 128), (13, 1024, 640)])
+def test_stream_gemm_fp8_against_oracle(pkg, orc, M, N, K):
+    """One 8-bit weight-streaming GEMM (split-K as in production) against the oracle's FP8 linear layer on the same
+    bf16 activations and codes: y = bf16(X . W^T) within the bf16 output rounding and fp32 accumulation."""
+    import ctypes
+    lib = pkg.lib()
+    vp = ctypes.c_void_p
+    lib.fpd_test_stream_gemm.argtypes = [ctypes.c_int] * 4 + [vp] * 6 + [ctypes.c_size_t, vp]
+    lib.fpd_test_stream_gemm.restype = ctypes.c_int
+    lib.fpd_test_stream_gemm_workspace_bytes.argtypes = [ctypes.c_int] * 3
+    lib.fpd_test_stream_gemm_workspace_bytes.restype = ctypes.c_size_t
+    rng = np.random.default_rng(M * 7 + N + K)
+    xb = synth.f32_to_bf16_bits((rng.normal(size=(M, K)) * np.exp2(rng.integers(-3, 3, size=(M, 1)))).astype(np.float32))
+    wb = synth.f32_to_bf16_bits((rng.normal(size=(N, K)) * 0.02).astype(np.float32))
+    X = torch.from_numpy(xb.view(np.int16)).to(DEV)
+    W = torch.from_numpy(wb.view(np.int16)).to(DEV)
+    codes = torch.empty(N, K, dtype=torch.uint8, device=DEV)
+    exps = torch.empty(N, K // 128, dtype=torch.int8, device=DEV)
+    pkg.fpd_quantize_fp8(W, N, K, K, codes, exps)
+    y = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
+    nws = int(lib.fpd_test_stream_gemm_workspace_bytes(N, K, 1))
+    ws = torch.empty(nws, dtype=torch.uint8, device=DEV)
+    cs = torch.cuda.current_stream().cuda_stream
+    assert lib.fpd_test_stream_gemm(1, M, N, K, X.data_ptr(), None, codes.data_ptr(), exps.data_ptr(), y.data_ptr(),
+                                    ws.data_ptr(), nws, cs) == 0
+    torch.cuda.synchronize()
+    assert pkg.fpd_device_status() == 0
+    qc, qe = orc.quantize_fp8(wb)
+    ref = orc.linear_fp8(f64(xb), qc, qe)
+    got = f64(bits_of(y))
+    err = np.abs(got - ref) / np.maximum(np.abs(ref).max(axis=1, keepdims=True), 1e-30)
+    assert err.max() <= 2 ** -8 + 1e-4, f"max error {err.max():.3e} (relative to each row's largest output)"
+    # and the bf16 form of the same kernel on the same weights, against the plain bf16 layer
+    y16 = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
+    nws16 = int(lib.fpd_test_stream_gemm_workspace_bytes(N, K, 0))
+    ws16 = torch.empty(nws16, dtype=torch.uint8, device=DEV)
+    assert lib.fpd_test_stream_gemm(0, M, N, K, X.data_ptr(), W.data_ptr(), None, None, y16.data_ptr(),
+                                    ws16.data_ptr(), nws16, cs) == 0
+    torch.cuda.synchronize()
+    ref16 = orc.linear(f64(xb), wb)
+    e16 = np.abs(f64(bits_of(y16)) - ref16) / np.maximum(np.abs(ref16).max(axis=1, keepdims=True), 1e-30)
+    assert e16.max() <= 2 ** -8 + 1e-4
+    rel = np.sqrt(((ref - ref16) ** 2).mean() / (ref16 ** 2).mean())
+    print(f"{M}x{N}x{K}: fp8 kernel err {err.max():.2e}, bf16 kernel err {e16.max():.2e}, 8-bit vs 16-bit {rel:.3f}")
+
+
+def _prepared(pkg, orc, shape, w, ctx_len, t_cap, L, B, seed, fp8=True):
+    off = np.concatenate([[0], np.cumsum(ctx_len)]).astype(np.int32)
+    feats = synth.make_features(shape, int(off[-1]), seed)
+    dr = pkg.Drafter(shape, w, B, L, t_cap, device=DEV, fp8=fp8)
+    assert pkg.fpd_model_fp8_enabled(dr.handle) == fp8
+    if off[-1] > 0:
+        dr.prepare_context(B, off, feats)
+    om = orc.Model(shape, w, fp8=fp8)
+    kv = orc.prepare_context(om, off, feats, t_cap, batch=B) if off[-1] > 0 else \
+        np.zeros((shape.n_layers, B, 2, shape.n_kv_heads, t_cap, shape.head_dim), np.uint16)
+    return dr, om, kv
+
+
+def _fp8_stagewise(pkg, orc, dr, om, kv_g, t_cap, ctx, anchor, mask_id, L, B, layer_tol=FP8_LAYER_TOL):
+    """Reading R25: the 8-bit pass checked stage by stage.  Layer l of the GPU against the oracle's layer l fed the
+    GPU's residual after layer l - 1 (layer 0: the embedding rows), each within FP8_LAYER_TOL; the LM head
+    and argmax against the oracle's on the GPU's final hidden states (logits 2e-2, ids exact above the 1e-2 margin,
+    margins).  The whole pass from the embedding is reported, and only bounded loosely: rounding activations to 4
+    significant bits turns the one-ulp bf16 differences of R18 into code steps 2^4 larger, so end-to-end
+    differences grow faster than in the bf16 pass."""
+    s = dr.shape
+    lh = torch.empty(s.n_layers, B * L, s.d_model, dtype=torch.bfloat16, device=DEV)
+    hid = dr.draft_block(B, L, dev_i32(ctx), dev_i32(anchor), mask_id, layer_hidden=lh)
+    logits = torch.full((B * (L - 1), s.vocab), float("nan"), dtype=torch.float32, device=DEV)
+    margin = torch.full((B * (L - 1),), float("nan"), dtype=torch.float32, device=DEV)
+    toks = dr.constrain_argmax(B, L, hid, logits_out=logits, margin_out=margin)
+    torch.cuda.synchronize()
+    assert pkg.fpd_device_status() == 0
+    g_lh, g_hid = bits_of(lh), bits_of(hid)
+    np.testing.assert_array_equal(g_lh[-1], g_hid)
+    stage = []
+    for l in range(s.n_layers):
+        x_in = None if l == 0 else g_lh[l - 1]
+        o = orc.draft_block(om, kv_g, t_cap, ctx, anchor, mask_id, L, layers=(l, l + 1), x_in=x_in)
+        stage.append(o)
+        print(f"layer {l} stage error: max row rel err {row_rel_err(f64(g_lh[l]), f64(o)).max():.3e}")
+    for l in range(s.n_layers):
+        assert_rows_close(g_lh[l], stage[l], f"layer {l} (fed the GPU's residual)", tol=layer_tol)
+    whole = orc.draft_block(om, kv_g, t_cap, ctx, anchor, mask_id, L)
+    e = row_rel_err(f64(g_hid), f64(whole)).max()
+    print(f"8-bit pass end to end: max row rel err {e:.3e}")
+    assert e < 0.25
+    o_tok, o_margin, o_log = orc.constrain_argmax(om, g_hid, B, L, want_logits=True)
+    g_log = logits.cpu().numpy()
+    assert_logits(g_log, o_log, "logits (8-bit LM head on the GPU's hidden)")
+    assert_tokens(toks.cpu().numpy(), o_tok, o_margin, "tokens (8-bit LM head on the GPU's hidden)")
+    assert_margin(margin.cpu().numpy(), g_log, o_margin, o_log, "margin")
+    return toks.cpu().numpy()
+
+
+def test_tiny_fp8_text_block(pkg, orc):
+    """Tiny drafter, one request, context 40, block 16: the 8-bit stream GEMMs (QKV, O, gate/up, down, LM head)."""
+    s = synth.TINY
+    w = synth.make_weights(s, 5151)
+    ctx = np.array([40], np.int32)
+    dr, om, kv = _prepared(pkg, orc, s, w, ctx, 40, 16, 1, 5152)
+    kv_g = _stagewise(dr, kv, ctx, 1)
+    _fp8_stagewise(pkg, orc, dr, om, kv_g, 40, ctx, np.array([9], np.int32), s.vocab - 1, 16, 1)
+    dr.close()
+
+
+def test_tiny_fp8_few_token_ragged(pkg, orc):
+    """Three requests of 5 positions (15 in all), one with an empty context: split-K over 8-bit weight atoms."""
+    s = synth.TINY
+    w = synth.make_weights(s, 5252)
+    ctx = np.array([40, 0, 97], np.int32)
+    dr, om, kv = _prepared(pkg, orc, s, w, ctx, 97, 5, 3, 5253)
+    kv_g = _stagewise(dr, kv, ctx, 3)
+    _fp8_stagewise(pkg, orc, dr, om, kv_g, 97, ctx, np.array([3, 4000, 77], np.int32), s.vocab - 1, 5, 3)
+    dr.close()
+
+
+def test_tiny_fp8_model_keeps_bf16_beyond_16_positions(pkg, orc):
+    """The same 8-bit model on 2 x 16 positions (32 block positions, 30 LM-head rows): the bf16 weights throughout,
+    matching the oracle's bf16 pass."""
+    s = synth.TINY
+    w = synth.make_weights(s, 5353)
+    ctx = np.array([33, 50], np.int32)
+    B, L = 2, 16
+    dr, om, kv = _prepared(pkg, orc, s, w, ctx, 50, L, B, 5354)
+    kv_g = _stagewise(dr, kv, ctx, B)
+    anchor = np.array([11, 12], np.int32)
+    hid = dr.draft_block(B, L, dev_i32(ctx), dev_i32(anchor), s.vocab - 1)
+    logits = torch.full((B * (L - 1), s.vocab), float("nan"), dtype=torch.float32, device=DEV)
+    toks = dr.constrain_argmax(B, L, hid, logits_out=logits)
+    torch.cuda.synchronize()
+    assert pkg.fpd_device_status() == 0
+    o_hid = orc.draft_block(om, kv_g, 50, ctx, anchor, s.vocab - 1, L, fp8=False)
+    assert_rows_close(bits_of(hid), o_hid, "hidden, bf16 weights")
+    o_tok, o_margin, o_log = orc.constrain_argmax(om, o_hid, B, L, want_logits=True, fp8=False)
+    g_log = logits.cpu().numpy()
+    assert_logits(g_log, o_log, "logits, bf16 weights")
+    g_tok = toks.cpu().numpy()
+    for b in range(B):
+        rows = slice(b * (L - 1), (b + 1) * (L - 1))
+        assert_tokens_chain(g_tok[b], o_tok[b], o_margin[rows], g_log[rows], o_log[rows], f"request {b} tokens")
+    dr.close()
+
+
+def test_full_fp8_text_block(pkg, orc, full_weights):
+    """4B shape, the batch-1 text workload (context 2048 of random K/V, block 16) on the 8-bit model."""
+    wl = synth.make_workload("text_4b_b1")
+    s = wl.shape
+    kv = synth.make_kv_store(s, 1, wl.t_cap, 2001)
+    dr = pkg.Drafter(s, full_weights, 1, wl.block_len, wl.t_cap, device=DEV, fp8=True)
+    dr.kv_view(1).copy_(torch.from_numpy(kv.view(np.int16)).view(torch.bfloat16))
+    om = orc.Model(s, full_weights, fp8=True)
+    toks = _fp8_stagewise(pkg, orc, dr, om, kv, wl.t_cap, wl.ctx_len, wl.anchor, wl.mask_id, wl.block_len, 1)
+    target, g = synth.make_target_rows(toks, s.vocab, wl.geo_p, 2002)
+    acc, com, val = dr.verify_text(1, wl.block_len, dev_i32(toks), dev_i32(target))
+    assert int(acc.item()) == 1 + min(int(g[0]), wl.block_len - 1)
+    dr.close()
+    # the bf16 pass checked the same way, for scale (its layer errors against R18's 2e-2)
+    dr16 = pkg.Drafter(s, full_weights, 1, wl.block_len, wl.t_cap, device=DEV)
+    dr16.kv_view(1).copy_(torch.from_numpy(kv.view(np.int16)).view(torch.bfloat16))
+    print("bf16 pass, same stages:")
+    _fp8_stagewise(pkg, orc, dr16, orc.Model(s, full_weights), kv, wl.t_cap, wl.ctx_len, wl.anchor, wl.mask_id,
+                   wl.block_len, 1, layer_tol=2e-2)
+    dr16.close()
