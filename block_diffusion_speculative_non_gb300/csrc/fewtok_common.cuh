@@ -123,28 +123,45 @@ __device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
 }
 
 // The activation slice in 8-bit form, in place: bf16 atoms [a0, a0 + na) (na even, <= 4: 64 K each, 16 token rows,
-// 128-byte swizzle) become E4M3 blocks [a0/2, a0/2 + na/2) (128 K each, same row and swizzle layout, written over
+// 128-byte swizzle), RMSNorm-ed on the way when `norm` (y = bf16(x * inv[t] * g[k]), the bf16 storage point of the
+// projection input), become E4M3 blocks [a0/2, a0/2 + na/2) (128 K each, same row and swizzle layout, written over
 // the bytes of atoms a0/2 ..), with s_xs[t * xs_ld + block] = 2^k of token t's group.  Thread et: pair = et / 4
 // (token t = pair % 16, block pair / 16), quarter q = et % 4 covers the block's K elements [32q, 32q + 32).  Rows
-// t >= M are zero.  Every read of the group precedes every write (the first blocks overwrite their own source).
-__device__ __forceinline__ void quant_atoms(uint8_t* act, float* s_xs, int xs_ld, int a0, int na, int M, int et) {
+// t >= M are zero.  Only the first group (a0 = 0) writes over bytes it reads: `first` puts a CTA barrier between
+// its reads and writes.  Each thread fences its writes for the tensor core; the caller then arrives.
+__device__ __forceinline__ void norm_quant_atoms(uint8_t* act, const uint8_t* gbuf, const float* s_inv, float* s_xs,
+                                                 int xs_ld, int a0, int na, int M, int et, bool norm, bool first) {
   const int pair = et >> 2, q = et & 3, t = pair & 15, blk = pair >> 4;
   const bool on = blk < (na >> 1);
+  const int atom = a0 + 2 * blk + (q >> 1);
   float x[32];
 #pragma unroll
   for (int i = 0; i < 32; i++) x[i] = 0.f;
   if (on && t < M) {
-    const uint8_t* src = act + (a0 + 2 * blk + (q >> 1)) * X_ATOM + t * 128;
+    const uint8_t* src = act + atom * X_ATOM + t * 128;
+    const float inv = norm ? s_inv[t] : 1.f;
 #pragma unroll
     for (int c = 0; c < 4; c++) {
       const int lc = (q & 1) * 4 + c;
       const uint4 u = *reinterpret_cast<const uint4*>(src + ((lc ^ (t & 7)) << 4));
       const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&u);
+      if (norm) {
+        const uint4 gu = *reinterpret_cast<const uint4*>(gbuf + atom * G_ATOM + lc * 16);
+        const __nv_bfloat162* gg = reinterpret_cast<const __nv_bfloat162*>(&gu);
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        const float2 f = __bfloat1622float2(e[k]);
-        x[c * 8 + 2 * k] = f.x;
-        x[c * 8 + 2 * k + 1] = f.y;
+        for (int k = 0; k < 4; k++) {
+          const float2 xf = __bfloat1622float2(e[k]), gf = __bfloat1622float2(gg[k]);
+          const float2 y = __bfloat1622float2(__floats2bfloat162_rn(xf.x * inv * gf.x, xf.y * inv * gf.y));
+          x[c * 8 + 2 * k] = y.x;
+          x[c * 8 + 2 * k + 1] = y.y;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const float2 f = __bfloat1622float2(e[k]);
+          x[c * 8 + 2 * k] = f.x;
+          x[c * 8 + 2 * k + 1] = f.y;
+        }
       }
     }
   }
@@ -159,13 +176,14 @@ __device__ __forceinline__ void quant_atoms(uint8_t* act, float* s_xs, int xs_ld
 #pragma unroll
   for (int i = 0; i < 8; i++)
     w[i] = e4m3x2(x[4 * i] * sc, x[4 * i + 1] * sc) | (e4m3x2(x[4 * i + 2] * sc, x[4 * i + 3] * sc) << 16);
-  epi_bar();   // every thread has read its source chunks
+  if (first) epi_bar();   // every thread has read its source chunks
   if (on) {
     uint8_t* dst = act + (a0 / 2 + blk) * X_ATOM + t * 128;
     *reinterpret_cast<uint4*>(dst + (((2 * q) ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
     *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ (t & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
     if (q == 0) s_xs[t * xs_ld + a0 / 2 + blk] = exp2_int(k);
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
 }
 
 // Split-K without a reduce kernel: every CTA stores its fp32 partial tile ([splits][tiles][128 rows][16 tokens],

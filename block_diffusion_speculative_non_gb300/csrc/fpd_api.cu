@@ -447,8 +447,10 @@ fpd_status fpd_model_enable_fp8(fpd_model* m, void* stream) {
     jobs.push_back({m->w.w_down[l], d.d_model, d.d_ff, &m->f8_down[l]});
   }
   jobs.push_back({m->w.lm_head, d.vocab, d.d_model, &m->f8_lm});
+  // exponents block-major [K/128][align_up(N, 128)]: one 128-byte copy brings a weight atom's 128 row exponents
   size_t bytes = 0;
-  for (const Job& j : jobs) bytes = align_up(align_up(bytes, 256) + (size_t)j.N * j.K, 256) + (size_t)j.N * (j.K / 128);
+  for (const Job& j : jobs)
+    bytes = align_up(align_up(bytes, 256) + (size_t)j.N * j.K, 256) + align_up((size_t)j.N, 128) * (j.K / 128);
   void* buf = nullptr;
   cudaError_t e = cudaMalloc(&buf, bytes + 256);
   if (e != cudaSuccess) return cuda_fail(e, "8-bit weight copies");
@@ -459,8 +461,11 @@ fpd_status fpd_model_enable_fp8(fpd_model* m, void* stream) {
     uint8_t* q = (uint8_t*)buf + off;
     off = align_up(off + (size_t)j.N * j.K, 256);
     int8_t* ex = (int8_t*)buf + off;
-    off += (size_t)j.N * (j.K / 128);
-    if (e == cudaSuccess) e = launch_quantize_fp8((const bf16*)j.w, j.N, j.K, j.K, q, ex, m->num_sms, st);
+    const int ld = (int)align_up((size_t)j.N, 128);
+    off += (size_t)ld * (j.K / 128);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ex, 0, (size_t)ld * (j.K / 128), st);
+    if (e == cudaSuccess) e = launch_quantize_fp8((const bf16*)j.w, j.N, j.K, j.K, q, ex, 1, ld, m->num_sms, st);
+    j.dst->ld = ld;
     j.dst->q = q;
     j.dst->e = ex;
   }
@@ -486,7 +491,8 @@ fpd_status fpd_quantize_fp8(const void* w, int rows, int cols, int ld, void* cod
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
-    e = launch_quantize_fp8((const bf16*)w, rows, cols, ld, (uint8_t*)codes, (int8_t*)exps, sms, (cudaStream_t)stream);
+    e = launch_quantize_fp8((const bf16*)w, rows, cols, ld, (uint8_t*)codes, (int8_t*)exps, cols / 128, 1, sms,
+                            (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "fpd_quantize_fp8");
   return scope.done(FPD_OK);
 }
@@ -644,6 +650,7 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
       g.fp8 = m->fp8;
       g.w8 = m->f8_qkv[l].q;
       g.w_exp = m->f8_qkv[l].e;
+      g.exp_ld = m->f8_qkv[l].ld;
       g.N = nqkv;
       g.K = dm;
       g.x = x;
@@ -675,6 +682,7 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
       o.w = (const bf16*)m->w.wo[l];
       o.w8 = m->f8_o[l].q;
       o.w_exp = m->f8_o[l].e;
+      o.exp_ld = m->f8_o[l].ld;
       o.N = dm;
       o.K = nq * h;
       o.x = w.o;
@@ -691,6 +699,7 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
       u.w = (const bf16*)m->w.w_gate_up[l];
       u.w8 = m->f8_gu[l].q;
       u.w_exp = m->f8_gu[l].e;
+      u.exp_ld = m->f8_gu[l].ld;
       u.N = F;
       u.K = dm;
       u.x = x;
@@ -707,6 +716,7 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
       dn.w = (const bf16*)m->w.w_down[l];
       dn.w8 = m->f8_down[l].q;
       dn.w_exp = m->f8_down[l].e;
+      dn.exp_ld = m->f8_down[l].ld;
       dn.K = F;
       dn.x = w.hmid;
       dn.ldx = F;
@@ -863,6 +873,7 @@ static fpd_status constrain_argmax_impl(fpd_model* m, int batch, int L, const vo
     g.fp8 = m->fp8;
     g.w8 = m->f8_lm.q;
     g.w_exp = m->f8_lm.e;
+    g.exp_ld = m->f8_lm.ld;
     g.M = n_rows;
     g.N = d.vocab;
     g.K = d.d_model;

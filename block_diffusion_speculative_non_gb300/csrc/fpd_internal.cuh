@@ -78,7 +78,8 @@ struct Model {
   // 8-bit copies of the weight-streamed matrices (fpd_model_enable_fp8), in one allocation the model owns
   struct F8 {
     const uint8_t* q = nullptr;   // E4M3 codes [rows, K]
-    const int8_t* e = nullptr;    // exponents [rows, K / 128]
+    const int8_t* e = nullptr;    // exponents, block-major [K / 128][ld]
+    int ld = 0;                   // rows rounded up to a multiple of 128
   };
   bool fp8 = false;
   void* fp8_buf = nullptr;

@@ -97,6 +97,8 @@ struct StreamGemm {
   bool fp8 = false;
   const uint8_t* w8 = nullptr;
   const int8_t* w_exp = nullptr;
+  int exp_ld = 0;                 // exponents block-major: (row r, 128-block b) at w_exp[b * exp_ld + r];
+                                  // exp_ld a multiple of 128, >= rows; w_exp 16-byte aligned
 };
 bool stream_shape_ok(const fpd_model_desc& d);
 StreamPlan stream_plan(int tiles, int K, int num_sms, bool split_ok, bool fp8);
@@ -105,8 +107,8 @@ cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st);
 cudaError_t stream_init_attributes();
 cudaError_t launch_embed_ss(bf16* x, float* ss, int* counters, int n_cnt, const bf16* embed, const int32_t* anchor,
                             int32_t mask_id, int B, int L, int d, int V, cudaStream_t st);
-cudaError_t launch_quantize_fp8(const bf16* w, int N, int K, int ld, uint8_t* codes, int8_t* exps, int num_sms,
-                                cudaStream_t st);
+cudaError_t launch_quantize_fp8(const bf16* w, int N, int K, int ld, uint8_t* codes, int8_t* exps, int exp_rs,
+                                int exp_cs, int num_sms, cudaStream_t st);
 cudaError_t launch_stream_decode(int32_t* tokens, float* margin, const unsigned long long* slots, int n_slots,
                                  int n_rows, cudaStream_t st);
 

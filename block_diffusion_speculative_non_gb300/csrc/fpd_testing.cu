@@ -121,7 +121,8 @@ fpd_status fpd_test_stream_gemm(int fp8, int M, int N, int K, const void* X, con
   g.w = (const bf16*)W;
   g.fp8 = fp8 != 0;
   g.w8 = (const uint8_t*)W8;
-  g.w_exp = (const int8_t*)Wexp;
+  g.w_exp = (const int8_t*)Wexp;   // block-major [K/128][N]
+  g.exp_ld = N;
   g.x = (const bf16*)X;
   g.ldx = K;
   g.xform = XF_COPY;

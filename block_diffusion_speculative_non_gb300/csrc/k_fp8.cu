@@ -1,6 +1,7 @@
 // k_fp8.cu — the 8-bit weight copies of the weight-streaming GEMMs (FlashDrive §3.4 "Quantization": low-bit
 // weights cut the bytes a memory-bound decoding step loads).  A bf16 matrix [N, K] (K a multiple of 128) becomes
-// E4M3 codes [N, K] plus one power-of-two exponent per 128 consecutive elements of a row, int8 [N, K / 128]:
+// E4M3 codes [N, K] plus one power-of-two exponent per 128 consecutive elements of a row (int8, at
+// exps[n * exp_rs + block * exp_cs]: [N, K / 128] for the C ABI, block-major [K / 128, N] for the model's copies):
 // k = the smallest integer with amax 2^-k <= 448, code = E4M3 nearest to w 2^-k (ties to even, +0 for zero).
 // The value a code stands for, decode(code) 2^k, is what the 8-bit GEMMs multiply.
 #include "fewtok_common.cuh"
@@ -12,7 +13,7 @@ using namespace fewtok;
 
 // One warp per 128-element group, grid-stride: lane l takes elements 4l .. 4l + 3 (8-byte loads, 4-byte stores).
 __global__ void quantize_fp8_kernel(const bf16* __restrict__ w, int N, int K, int ld, uint8_t* __restrict__ codes,
-                                    int8_t* __restrict__ exps) {
+                                    int8_t* __restrict__ exps, int exp_rs, int exp_cs) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -30,18 +31,18 @@ __global__ void quantize_fp8_kernel(const bf16* __restrict__ w, int N, int K, in
     const float sc = exp2_int(-k);
     const uint32_t c = e4m3x2(a.x * sc, a.y * sc) | (e4m3x2(b.x * sc, b.y * sc) << 16);
     *reinterpret_cast<uint32_t*>(codes + n * K + g * 128 + lane * 4) = c;
-    if (lane == 0) exps[n * (K / 128) + g] = (int8_t)k;
+    if (lane == 0) exps[n * exp_rs + g * exp_cs] = (int8_t)k;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_quantize_fp8(const bf16* w, int N, int K, int ld, uint8_t* codes, int8_t* exps, int num_sms,
-                                cudaStream_t st) {
+cudaError_t launch_quantize_fp8(const bf16* w, int N, int K, int ld, uint8_t* codes, int8_t* exps, int exp_rs,
+                                int exp_cs, int num_sms, cudaStream_t st) {
   if (N < 1 || K < 128 || K % 128 || ld < K || ld % 4) return cudaErrorInvalidValue;
   const long groups = (long)N * (K / 128);
   const int blocks = (int)std::min<long>((groups + 7) / 8, (long)num_sms * 16);
-  return launch_k(quantize_fp8_kernel, blocks, 256, 0, st, w, N, K, ld, codes, exps);
+  return launch_k(quantize_fp8_kernel, blocks, 256, 0, st, w, N, K, ld, codes, exps, exp_rs, exp_cs);
 }
 
 }  // namespace fpd

@@ -36,18 +36,20 @@ constexpr int kMaxStages = 8;                 // (10-14 atoms) measured slower o
 constexpr int kTmemCols = 32;                 // two 16-column accumulators
 constexpr int kAccSlots = 8;                  // 8-bit weights: one 16-column accumulator per weight atom, 8 in flight
 constexpr int kTmemCols8 = kAccSlots * SBN;
+constexpr int kXRing = kMaxStages + kAccSlots;   // 8-bit: weight-row exponents of the last 16 weight atoms (128 B each)
 constexpr int kActGroup = 4;                  // activation atoms per readiness barrier
 constexpr int kMaxActGroups = 12;             // activation slices of up to 48 atoms (K <= 3072)
 constexpr int kXsLd = 2 * kMaxActGroups;      // 8-bit activation scales per token: one per 128-element block
-// misc region: mbarriers full[S], empty[S], act_tma[G], act_ready[G], tfull[8], tempty[8] | TMEM slot, abort,
-// last-CTA flag | inverse RMS per token [16] | context length per request [16] | running top-2 per token [16][2] |
-// 8-bit activation scales [16][kXsLd]
-constexpr int kMiscFlags = 8 * (2 * kMaxStages + 2 * kMaxActGroups + 2 * kAccSlots);
+// misc region: mbarriers full[S], empty[S], act_tma[G], act_ready[G], tfull[8], tempty[8], xfull[16] | TMEM slot,
+// abort, last-CTA flag | inverse RMS per token [16] | context length per request [16] | running top-2 per token
+// [16][2] | 8-bit activation scales [16][kXsLd] | 8-bit weight-exponent ring [16][128]
+constexpr int kMiscFlags = 8 * (2 * kMaxStages + 2 * kMaxActGroups + 2 * kAccSlots + kXRing);
 constexpr int kMiscInv = kMiscFlags + 16;
 constexpr int kMiscCtx = kMiscInv + SBN * 4;
 constexpr int kMiscRun = kMiscCtx + SBN * 4;
 constexpr int kMiscXs = kMiscRun + SBN * 16;
-constexpr int kMiscBytes = kMiscXs + SBN * kXsLd * 4;
+constexpr int kMiscXe = kMiscXs + SBN * kXsLd * 4;
+constexpr int kMiscBytes = kMiscXe + kXRing * SBM;
 
 struct StreamParams {
   CUtensorMap tm_w;            // weights [rows, K] bf16, box 64 x (128, SwiGLU: 64); 8-bit: E4M3 bytes, box 128 x ..
@@ -81,7 +83,8 @@ struct StreamParams {
   // SEPI_ARGMAX
   unsigned long long* slots;   // [gridDim][16][2]
   float* logits;               // [M][N] or null
-  const int8_t* w_exp;         // 8-bit weights: exponents [rows][K / 128]
+  const int8_t* w_exp;         // 8-bit weights: exponents, block-major: (row r, block b) at w_exp[b * exp_ld + r]
+  int exp_ld;                  // a multiple of 128 (>= rows): every atom's 128 (SwiGLU: 2 x 64) rows are one copy
   int w_rows;                  // rows of the weight matrix
   int stages;                  // weight ring depth, kMinStages..kMaxStages
   uint32_t test_extra_tx;      // 0; a test makes the first stage's wait run out with it (bounded-wait check)
@@ -113,9 +116,10 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
   int* s_ctx = reinterpret_cast<int*>(misc + kMiscCtx);
   unsigned long long* s_run = reinterpret_cast<unsigned long long*>(misc + kMiscRun);
   float* s_xs = reinterpret_cast<float*>(misc + kMiscXs);
+  const int8_t* s_xe = reinterpret_cast<const int8_t*>(misc + kMiscXe);
   const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8 * kMaxStages, actt0 = empty0 + 8 * kMaxStages,
                  actr0 = actt0 + 8 * kMaxActGroups, tfull0 = actr0 + 8 * kMaxActGroups,
-                 tempty0 = tfull0 + 8 * kAccSlots;
+                 tempty0 = tfull0 + 8 * kAccSlots, xfull0 = tempty0 + 8 * kAccSlots;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   pdl_trigger();
@@ -136,6 +140,8 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       tc::mbar_init(tfull0 + 8 * a, 1);
       tc::mbar_init(tempty0 + 8 * a, 4);
     }
+    if (FP8)
+      for (int a = 0; a < kXRing; a++) tc::mbar_init(xfull0 + 8 * a, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -182,6 +188,18 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
         } else {
           tc::tma_load_2d(dst, &p.tm_w, kx, tile * SBM, fb);
         }
+        if (FP8) {   // the atom's 128 row exponents into exponent slot issued % kXRing (read by the epilogue)
+          const int xs = issued % kXRing;
+          const uint32_t xb = xfull0 + 8 * xs, xd = tc::smem_u32(s_xe + xs * SBM);
+          const int8_t* src = p.w_exp + (size_t)(kx / 128) * p.exp_ld;
+          tc::mbar_arrive_expect_tx(xb, SBM);
+          if (EPI == SEPI_SWIGLU) {
+            tc::bulk_load(xd, src + tile * 64, 64, xb);
+            tc::bulk_load(xd + 64, src + p.N + tile * 64, 64, xb);
+          } else {
+            tc::bulk_load(xd, src + tile * SBM, SBM, xb);
+          }
+        }
         issued++;
         if (++stage == n_stages) { stage = 0; phase ^= 1; }
         if (++kb == nkb) {
@@ -222,6 +240,9 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
           if (--stage < 0) { stage = n_stages - 1; phase ^= 1; }
           tc::mbar_wait(full0 + 8 * stage, phase);
         }
+        if (FP8)
+          for (int c = issued - 1; c >= 0 && c >= issued - kXRing; c--)
+            tc::mbar_wait(xfull0 + 8 * (c % kXRing), (c / kXRing) & 1);
         if (blockIdx.x < total)
           for (int g = 0; g * kActGroup < nxa0; g++) tc::mbar_wait(actt0 + 8 * g, 0);
       }
@@ -299,7 +320,25 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       s_ctx[et] = clamp_ctx(cl, p.t_cap);
     }
     if (EPI == SEPI_ARGMAX && et < SBN) s_run[2 * et] = s_run[2 * et + 1] = 0ull;
-    if (blockIdx.x < total && (FP8 || p.xform != XF_COPY)) {
+    if (FP8) {
+      // 8-bit: every activation group normed (when the GEMM consumes a normed stream) and quantised in one pass
+      if (blockIdx.x < total) {
+        const int n_groups = (nxa0 + kActGroup - 1) / kActGroup;
+        if (p.xform == XF_NORM_FULL) {   // 1/rms from the whole rows: every group first
+          for (int g = 0; g < n_groups; g++)
+            if (!tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
+          inv_from_rows(act, nxa0, p.K, p.eps, s_inv, et);
+        }
+        epi_bar();   // s_inv complete
+        for (int g = 0; g < n_groups; g++) {
+          const int a0 = g * kActGroup, na = min(kActGroup, nxa0 - a0);
+          if (p.xform != XF_NORM_FULL && !tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
+          norm_quant_atoms(act, gbuf, s_inv, s_xs, kXsLd, a0, na, p.M, et, p.xform != XF_COPY, g == 0);
+          epi_bar();
+          if (et == 0) tc::mbar_arrive(actr0 + 8 * g);
+        }
+      }
+    } else if (blockIdx.x < total && p.xform != XF_COPY) {
       if (p.xform == XF_NORM_FULL) {   // 1/rms from the whole rows: every group first
         for (int g = 0; g * kActGroup < nxa0; g++)
           if (!tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
@@ -307,13 +346,8 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
       }
       epi_bar();   // s_inv complete
       for (int g = 0; g * kActGroup < nxa0; g++) {
-        const int a0 = g * kActGroup, na = min(kActGroup, nxa0 - a0);
-        if (p.xform != XF_NORM_FULL && !tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
-        if (p.xform != XF_COPY) norm_atoms(act, gbuf, s_inv, a0, na, et);
-        if (FP8) {
-          epi_bar();   // the normed rows are complete
-          quant_atoms(act, s_xs, kXsLd, a0, na, p.M, et);
-        }
+        if (p.xform == XF_NORM && !tc::mbar_wait(actt0 + 8 * g, 0)) *abort_flag = 1;
+        norm_atoms(act, gbuf, s_inv, g * kActGroup, min(kActGroup, nxa0 - g * kActGroup), et);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
         epi_bar();
         if (et == 0) tc::mbar_arrive(actr0 + 8 * g);
@@ -331,16 +365,12 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
         // v = sum over the item's weight atoms of (block product) 2^(k_token + k_row); this thread's weight row
 #pragma unroll
         for (int j = 0; j < 16; j++) v[j] = 0.f;
-        const int wrow = EPI == SEPI_SWIGLU
-                             ? (row_in_tile < 64 ? tile * 64 + row_in_tile : p.N + tile * 64 + row_in_tile - 64)
-                             : tile * SBM + row_in_tile;
-        const bool wok = wrow < p.w_rows;
-        const int8_t* we = p.w_exp + (size_t)(wok ? wrow : 0) * (p.K / 128) + k0 / 128;
-        int ew = (wok && nkb > 0) ? we[0] : 0;
         for (int kb = 0; kb < nkb; kb++, c8++) {
-          const int ew_next = (wok && kb + 1 < nkb) ? we[kb + 1] : 0;
-          const int slot = c8 % kAccSlots;
+          const int slot = c8 % kAccSlots, xs = c8 % kXRing;
           if (!*abort_flag && !tc::mbar_wait(tfull0 + 8 * slot, (c8 / kAccSlots) & 1)) *abort_flag = 1;
+          // this atom's row exponent: its slot is rewritten only after this thread's warp frees the accumulator
+          if (!*abort_flag && !tc::mbar_wait(xfull0 + 8 * xs, (c8 / kXRing) & 1)) *abort_flag = 1;
+          const int ew = s_xe[xs * SBM + row_in_tile];
           tc::tc_fence_after();
           float u[16];
           tc::tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + slot * SBN, u);
@@ -350,7 +380,6 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
           const float sw = exp2_int(ew);
 #pragma unroll
           for (int j = 0; j < 16; j++) v[j] = fmaf(u[j], s_xs[j * kXsLd + kb] * sw, v[j]);
-          ew = ew_next;
         }
         if (*abort_flag) {
 #pragma unroll
@@ -571,10 +600,13 @@ cudaError_t launch_stream_gemm(const StreamGemm& g, cudaStream_t st) {
   const int w_rows = g.epi == SEPI_SWIGLU ? 2 * g.N : g.N;
   if (g.M < 1 || g.M > SBN || g.K % SBK || g.plan.k_split / SBK > kActGroup * kMaxActGroups)
     return cudaErrorInvalidValue;
-  if (g.fp8 && (g.K % 128 || g.plan.k_split % 128 || !g.w8 || !g.w_exp)) return cudaErrorInvalidValue;
+  if (g.fp8 && (g.K % 128 || g.plan.k_split % 128 || !g.w8 || !g.w_exp || g.exp_ld % 128 || g.exp_ld < w_rows ||
+                ((uintptr_t)g.w_exp & 15)))
+    return cudaErrorInvalidValue;
   cudaError_t e = g.fp8 ? make_tmap_u8(&p.tm_w, g.w8, w_rows, g.K, g.K, box_rows)
                         : make_tmap(&p.tm_w, g.w, w_rows, g.K, g.K, box_rows);
   p.w_exp = g.w_exp;
+  p.exp_ld = g.exp_ld;
   p.w_rows = w_rows;
   if (e != cudaSuccess) return e;
   if (g.xform == XF_NORM_FULL) {

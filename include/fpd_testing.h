@@ -58,8 +58,9 @@ size_t fpd_test_stream_timeout_workspace_bytes(void);
 /* One weight-streaming GEMM (the few-token path's kernel, residual epilogue) in isolation:
  *   y[M, N] (bf16, updated in place) = bf16(y + X . W^T)
  * X [M, K] bf16 (M <= 16), y [M, N] bf16, N a multiple of 128, with the production split-K plan for N x K.
- * fp8 = 0: W [N, K] bf16 (K a multiple of 64).  fp8 = 1: W8 [N, K] E4M3 codes and Wexp [N, K/128] exponents (the
- * f2 form of fpd.h, K a multiple of 128); X is quantised per token and 128 elements inside the kernel.
+ * fp8 = 0: W [N, K] bf16 (K a multiple of 64).  fp8 = 1: W8 [N, K] E4M3 codes and Wexp the exponents of the f2 form
+ * of fpd.h, block-major [K/128, N] (16-byte aligned; K a multiple of 128); X is quantised per token and 128 elements
+ * inside the kernel.
  * workspace: fpd_test_stream_gemm_workspace_bytes(N, K, fp8) bytes (zeroed by the call).  Asynchronous. */
 fpd_status fpd_test_stream_gemm(int fp8, int M, int N, int K, const void* X, const void* W, const void* W8,
                                 const void* Wexp, void* y, void* workspace, size_t workspace_bytes, void* stream);

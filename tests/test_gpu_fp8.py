@@ -116,7 +116,8 @@ def test_stream_gemm_fp8_against_oracle(pkg, orc, M, N, K):
     nws = int(lib.fpd_test_stream_gemm_workspace_bytes(N, K, 1))
     ws = torch.empty(nws, dtype=torch.uint8, device=DEV)
     cs = torch.cuda.current_stream().cuda_stream
-    assert lib.fpd_test_stream_gemm(1, M, N, K, X.data_ptr(), None, codes.data_ptr(), exps.data_ptr(), y.data_ptr(),
+    exps_t = exps.t().contiguous()                       # the kernel's block-major exponent layout
+    assert lib.fpd_test_stream_gemm(1, M, N, K, X.data_ptr(), None, codes.data_ptr(), exps_t.data_ptr(), y.data_ptr(),
                                     ws.data_ptr(), nws, cs) == 0
     torch.cuda.synchronize()
     assert pkg.fpd_device_status() == 0
