@@ -89,7 +89,7 @@ struct DraftWs {
   bool stream;
   StreamPlan s_qkv, s_o, s_sw, s_down;
   float *ss_a, *ss_b;       // sums of squares of the residual stream [parts][16]
-  int *cnt_qkv, *cnt_o, *cnt_down, n_cnt;
+  int *cnt_qkv, *cnt_o, *cnt_down, *cnt_sw, n_cnt;
 };
 
 // The few-token path takes calls with at most 16 block positions in all.
@@ -108,10 +108,10 @@ DraftWs carve_draft_stream(const Model& m, Carver& c, int B, int L, int t_cap, b
   const int nqkv = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim, nqh = d.n_q_heads * d.head_dim;
   w.s_qkv = stream_plan(nqkv / 128, d.d_model, m.num_sms, true, fp8);
   w.s_o = stream_plan(d.d_model / 128, nqh, m.num_sms, true, fp8);
-  w.s_sw = stream_plan(d.d_ff / 64, d.d_model, m.num_sms, false, fp8);
+  w.s_sw = stream_plan(d.d_ff / 64, d.d_model, m.num_sms, true, fp8);
   w.s_down = stream_plan(d.d_model / 128, d.d_ff, m.num_sms, true, fp8);
   const size_t part = std::max(std::max(stream_part_floats(w.s_qkv), stream_part_floats(w.s_o)),
-                               stream_part_floats(w.s_down));
+                               std::max(stream_part_floats(w.s_down), stream_part_floats(w.s_sw)));
   w.part = c.take<float>(std::max<size_t>(part, 1));
   w.q = c.take<bf16>((size_t)M * nqh);
   w.kblk = c.take<bf16>((size_t)M * d.n_kv_heads * d.head_dim);
@@ -120,10 +120,11 @@ DraftWs carve_draft_stream(const Model& m, Carver& c, int B, int L, int t_cap, b
   w.hmid = c.take<bf16>((size_t)M * d.d_ff);
   w.ss_a = c.take<float>((size_t)(d.d_model / 128) * S);
   w.ss_b = c.take<float>((size_t)(d.d_model / 128) * S);
-  w.n_cnt = w.s_qkv.tiles + 2 * w.s_o.tiles;
+  w.n_cnt = w.s_qkv.tiles + 2 * w.s_o.tiles + w.s_sw.tiles;
   w.cnt_qkv = c.take<int>(w.n_cnt);
   w.cnt_o = w.cnt_qkv ? w.cnt_qkv + w.s_qkv.tiles : nullptr;
   w.cnt_down = w.cnt_o ? w.cnt_o + w.s_o.tiles : nullptr;
+  w.cnt_sw = w.cnt_down ? w.cnt_down + w.s_o.tiles : nullptr;
   attn_plan(B, L, d.n_q_heads, d.n_kv_heads, t_cap, m.num_sms, &w.att_splits, &w.att_chunk);
   w.o_part = c.take<float>((size_t)w.att_splits * M * nqh);
   w.ml = c.take<float2>((size_t)w.att_splits * M * d.n_q_heads);
@@ -709,6 +710,7 @@ static fpd_status draft_block_impl(fpd_model* m, int batch, int L, const void* k
       u.n_ss = dm / 128;
       u.gain = (const bf16*)m->w.mlp_norm[l];
       u.hmid = w.hmid;
+      u.counters = w.cnt_sw;
       FPD_CUDA(launch_stream_gemm(u, st), "gate/up + SwiGLU");
       // down projection + residual
       StreamGemm dn = o;

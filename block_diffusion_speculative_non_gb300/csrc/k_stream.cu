@@ -426,8 +426,9 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_gemm_kernel(const __grid_
             epi_bar();
           }
         }
-      } else if (EPI == SEPI_SWIGLU) {
-        swiglu_epilogue(v, p.hmid, p.N, tile, p.M, scratch, row_in_tile);
+      } else if (EPI == SEPI_SWIGLU) {   // split K when the feature tiles alone leave SMs idle
+        if (splitk_last(v, p.part, p.counters, split, p.splits, tile, p.tiles, row_in_tile, et, s_flag))
+          swiglu_epilogue(v, p.hmid, p.N, tile, p.M, scratch, row_in_tile);
       } else {
         // LM head: ids tile*128 + row, running top-2 per token
         const int vid = tile * SBM + row_in_tile;

@@ -1,9 +1,11 @@
 """GPU: the multi-block text speculative loop and failure detection.
 
 The loop (draft -> argmax -> target row -> verify -> advance -> append of the accepted rows' features) runs K steps
-inside one captured CUDA graph; the oracle then replays the same K steps on the host from the GPU's ids: every
-step's hidden states, logits and ids (chain rule), the synthetic target row, the verification, the context
-bookkeeping (positions, lengths, next anchors) and, at the end, the whole context K/V store.
+inside one captured CUDA graph, which also keeps a copy of the context K/V store at the start of every step; the
+oracle then checks every stage of every step on the GPU's own inputs (reading R21): the block pass on the store the
+GPU held, the LM head and argmax on the GPU's hidden states (ids exact above the 1e-2 margin), the synthetic target
+row, the verification, the context bookkeeping (positions, lengths, next anchors) and the append, i.e. the store
+after the step against the oracle's append of the accepted rows to the store before it.
 (VFlash blog "Method"; FlashDrive §3.2; VFlash paper (zh) §2.2.)
 """
 import ctypes
@@ -13,7 +15,7 @@ import pytest
 import torch
 
 import synth
-from _util import (assert_logits, assert_rows_close, assert_tokens_chain, bits_of, synthetic_target)
+from _util import (assert_logits, assert_rows_close, assert_tokens, bits_of, synthetic_target)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -66,7 +68,8 @@ def _run_loop(pkg, orc, shape, w, ctx0, anchor0, L, K, t_cap, seed):
             "ctx": torch.empty(K, B, dtype=torch.int32, device=DEV),
             "anc": torch.empty(K, B, dtype=torch.int32, device=DEV),
             "pos": torch.empty(K, B, dtype=torch.int32, device=DEV),
-            "log": torch.empty(K, B * (L - 1), V, dtype=torch.float32, device=DEV)}
+            "log": torch.empty(K, B * (L - 1), V, dtype=torch.float32, device=DEV),
+            "kv": torch.empty((K + 1,) + tuple(dr.kv_view(B).shape), dtype=torch.bfloat16, device=DEV)}
     lib = pkg.lib()
     step = [0]
 
@@ -90,31 +93,39 @@ def _run_loop(pkg, orc, shape, w, ctx0, anchor0, L, K, t_cap, seed):
                 assert lib.fpd_test_synthetic_target(B, L, V, tok.data_ptr(), agree_d[k].data_ptr(),
                                                      int(salts[k]), tgt.data_ptr(), cs.cuda_stream) == 0
 
+            bufs["kv"][k].copy_(dr.kv_view(B))
             dr.spec_step(st, feats_d[k], make_target, V - 1, stream=cs, logits_out=bufs["log"][k])
             bufs["ctx"][k].copy_(st.ctx_len)
             bufs["anc"][k].copy_(st.anchor)
             bufs["pos"][k].copy_(st.pos_start)
+        bufs["kv"][K].copy_(dr.kv_view(B))
     g.replay()
     torch.cuda.synchronize()
     assert pkg.fpd_device_status() == 0
     H = {k: v.cpu() for k, v in bufs.items()}
 
-    # ---- oracle: the same K steps from the GPU's ids ----
+    # ---- oracle: every stage of every step on the GPU's inputs ----
     om = orc.Model(shape, w)
-    kv = orc.prepare_context(om, off0, f0, t_cap, batch=B) if off0[-1] > 0 else \
+    kv0 = orc.prepare_context(om, off0, f0, t_cap, batch=B) if off0[-1] > 0 else \
         np.zeros((shape.n_layers, B, 2, shape.n_kv_heads, t_cap, shape.head_dim), np.uint16)
+    g_kv = bits_of(H["kv"])
+    for b in range(B):                                   # the initial preparation
+        T = int(ctx0[b])
+        if T:
+            assert_rows_close(g_kv[0][:, b, :, :, :T].reshape(-1, shape.head_dim),
+                              kv0[:, b, :, :, :T].reshape(-1, shape.head_dim), f"initial store request {b}")
     ctx, anchor = np.array(ctx0, np.int32), np.array(anchor0, np.int32)
     accepted = []
     for k in range(K):
-        o_hid = orc.draft_block(om, kv, t_cap, ctx, anchor, V - 1, L)
-        assert_rows_close(bits_of(H["hid"][k]), o_hid, f"step {k} hidden")
-        o_tok, o_margin, o_log = orc.constrain_argmax(om, o_hid, B, L, want_logits=True)
+        kv_k = np.ascontiguousarray(g_kv[k])
+        o_hid = orc.draft_block(om, kv_k, t_cap, ctx, anchor, V - 1, L)
+        g_hid = bits_of(H["hid"][k])
+        assert_rows_close(g_hid, o_hid, f"step {k} hidden (on the GPU's store)")
+        o_tok, o_margin, o_log = orc.constrain_argmax(om, g_hid, B, L, want_logits=True)
         tok = H["tok"][k].numpy()
         g_log = H["log"][k].numpy()
-        for b in range(B):
-            rows = slice(b * (L - 1), (b + 1) * (L - 1))
-            assert_logits(g_log[rows], o_log[rows], f"step {k} request {b} logits")
-            assert_tokens_chain(tok[b], o_tok[b], o_margin[rows], g_log[rows], o_log[rows], f"step {k} request {b}")
+        assert_logits(g_log, o_log, f"step {k} logits (on the GPU's hidden)")
+        assert_tokens(tok, o_tok, o_margin, f"step {k} ids (on the GPU's hidden)")
         target = synthetic_target(tok, agree[k], int(salts[k]), V)
         np.testing.assert_array_equal(H["tgt"][k].numpy(), target)
         oacc, ocom, _ = orc.verify(0, tok, target)
@@ -126,17 +137,17 @@ def _run_loop(pkg, orc, shape, w, ctx0, anchor0, L, K, t_cap, seed):
         np.testing.assert_array_equal(H["pos"][k].numpy(), pos)
         np.testing.assert_array_equal(H["ctx"][k].numpy(), ctx)
         np.testing.assert_array_equal(H["anc"][k].numpy(), anchor)
-        # the target's features at the anchor and the accepted drafts join the context
+        # the append: the target's features at the anchor and the accepted drafts join the context
         off = np.concatenate([[0], np.cumsum(oacc)]).astype(np.int32)
         rows = [f[np.concatenate([np.arange(b * L, b * L + oacc[b]) for b in range(B)])] for f in feats[k]]
-        kv = orc.prepare_context(om, off, rows, t_cap, batch=B, pos_start=pos, kv_store=kv)
+        want = orc.prepare_context(om, off, rows, t_cap, batch=B, pos_start=pos, kv_store=kv_k.copy())
+        got = g_kv[k + 1]
+        for b in range(B):
+            new_rows = slice(int(pos[b]), int(ctx[b]))
+            assert_rows_close(got[:, b, :, :, new_rows].reshape(-1, shape.head_dim),
+                              want[:, b, :, :, new_rows].reshape(-1, shape.head_dim), f"step {k} append request {b}")
+            np.testing.assert_array_equal(got[:, b, :, :, :int(pos[b])], kv_k[:, b, :, :, :int(pos[b])])
         accepted.append(oacc)
-    got = bits_of(dr.kv_view(B))
-    for b in range(B):
-        T = int(ctx[b])
-        if T:
-            assert_rows_close(got[:, b, :, :, :T].reshape(-1, shape.head_dim),
-                              kv[:, b, :, :, :T].reshape(-1, shape.head_dim), f"final store request {b}")
     dr.close()
     return np.array(accepted)
 
