@@ -568,6 +568,27 @@ static fpd_status prepare_rows_impl(fpd_model* m, int batch, int total_rows, con
     FPD_CUDA(launch_rmsnorm_partials(w.ctx, w.part, pf.splits, g.c_split_stride, (const bf16*)m->w.hidden_norm, R,
                                      d.d_model, d.rms_eps, st),
              "fusion RMSNorm");
+    if (R >= kTokMinRows && kvctx_supported(d)) {
+      // every layer's K/V in one token-tile GEMM whose epilogue norms, rotates and stores (no fp32 round trip)
+      const bf16* kn[FPD_MAX_LAYERS];
+      for (int l = 0; l < d.n_layers; l++) kn[l] = (const bf16*)m->w.k_norm[l];
+      KvCtxGemm kg{};
+      kg.d = &d;
+      kg.ctx = w.ctx;
+      kg.R = R;
+      kg.wqkv = m->w.wqkv;
+      kg.k_norm = kn;
+      kg.rope = m->rope;
+      kg.store = (bf16*)kv_store;
+      kg.batch = batch;
+      kg.t_cap = t_cap;
+      kg.row0 = r0;
+      kg.row_off = row_off;
+      kg.row_cnt = row_cnt;
+      kg.pos_start = pos_start;
+      FPD_CUDA(launch_tc_kvctx(kg, m->num_sms, st), "context K/V GEMM + store epilogue");
+      continue;
+    }
     for (int l = 0; l < d.n_layers; l++) {
       GemmArgs k{};
       k.a[0] = w.ctx;

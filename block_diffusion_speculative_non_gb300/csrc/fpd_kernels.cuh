@@ -33,6 +33,22 @@ TcPlan tc_plan_gemm(int M, int N, int K, int num_sms);
 TcPlan tc_plan_force(int M, int N, int K, int num_sms, int placement);   // placement 0: tokens on 128 rows, 1: weights
 cudaError_t launch_tc_gemm(const GemmArgs& g, const TcPlan& plan, cudaStream_t st);
 TcPlan tc_plan_swiglu(int M, int F, int K, int num_sms);
+// Context K/V of every layer in one token-tile GEMM (a2): rows [row0, row0 + R) of the fused, normed context ctx
+// [R][d] against [Wk; Wv] of all layers, with the K-norm + RoPE and the store writes in the epilogue.
+struct KvCtxGemm {
+  const fpd_model_desc* d;
+  const bf16* ctx;
+  int R;
+  const void* const* wqkv;          // [layers] weights [(H_q + 2 H_kv) h, d]
+  const bf16* const* k_norm;        // [layers] gains [h]
+  const float2* rope;
+  bf16* store;                      // [layers][batch][K|V][H_kv][t_cap][h]
+  int batch, t_cap, row0;
+  const int32_t *row_off, *row_cnt, *pos_start;
+};
+bool kvctx_supported(const fpd_model_desc& d);
+cudaError_t launch_tc_kvctx(const KvCtxGemm& g, int num_sms, cudaStream_t st);
+
 // hmid[M][F] = bf16(silu(x . Wg^T) * (x . Wu^T)) with W = [Wg; Wu] ([2F, K]), one tcgen05 pass
 cudaError_t launch_tc_swiglu(const bf16* x, int M, int K, const bf16* w_gate_up, int F, bf16* hmid, const TcPlan& pl,
                              cudaStream_t st);

@@ -35,7 +35,7 @@ namespace {
 
 constexpr int BM = 128, BK = 64, UMMA_K = 16;
 constexpr int kThreads = 192;
-enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_SWIGLU = 2, EPI_QKV_TOK = 3, EPI_RESID_TOK = 4 };
+enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_SWIGLU = 2, EPI_QKV_TOK = 3, EPI_RESID_TOK = 4, EPI_KV_CTX = 5 };
 
 struct TcParams {
   CUtensorMap tm_x[8];   // activation K-segments (box rows: BN if swap else 128)
@@ -71,6 +71,15 @@ struct TcParams {
   // EPI_RESID_TOK (token tiles): x[m][n] = bf16(x + acc); ss_part[column tile][m] = that tile's sum of x^2
   bf16* xres;
   float* ss_part;
+  // EPI_KV_CTX (token tiles of context rows): the B operand is [Wk; Wv] of every layer side by side, layer l's
+  // kv_cols rows starting at row kv_row_base of wqkv[l] (tm_wl[l]); each context row row0 + m goes to its request's
+  // position in the KV store [layer][b][K|V][g][t_cap][hd], K heads RMS-normed (k_norm_l[l]) and rotated
+  CUtensorMap tm_wl[FPD_MAX_LAYERS];
+  int kv_cols, kv_row_base, n_layers;
+  bf16* store;
+  const bf16* k_norm_l[FPD_MAX_LAYERS];
+  const int32_t *row_off, *row_cnt, *pos_start;
+  int batch, row0;
 };
 
 // A pipeline stage holds KS consecutive 64-element K atoms of both operands: [A atoms][B atoms].  Several
@@ -171,7 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     tc::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    tc::tma_prefetch(&p.tm_w);
+    if (EPI == EPI_KV_CTX)
+      for (int l = 0; l < p.n_layers; l++) tc::tma_prefetch(&p.tm_wl[l]);
+    else
+      tc::tma_prefetch(&p.tm_w);
     for (int s = 0; s < p.n_seg; s++) tc::tma_prefetch(&p.tm_x[s]);
   }
   // The single-lane roles reconverge with their warps first: a CTA barrier reached by part of a diverged
@@ -197,6 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             tc::tma_load_2d(dst + half, &p.tm_w, ka, p.F + f0, fb);
           } else if (SWAP) {
             tc::tma_load_2d(sa + a * C::A_ATOM, &p.tm_w, ka, w.a_row0, fb);
+          } else if (EPI == EPI_KV_CTX) {   // column b_row0 of the side-by-side layers
+            const int layer = w.b_row0 / p.kv_cols;
+            tc::tma_load_2d(sa + C::A_BYTES + a * C::B_ATOM, &p.tm_wl[layer], ka,
+                            w.b_row0 - layer * p.kv_cols + p.kv_row_base, fb);
           } else {
             tc::tma_load_2d(sa + C::A_BYTES + a * C::B_ATOM, &p.tm_w, ka, w.b_row0, fb);
           }
@@ -405,6 +421,94 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               e2[e] = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
             }
             if (mok) {
+              reinterpret_cast<uint4*>(dst + c)[0] = o1[0];
+              reinterpret_cast<uint4*>(dst + c)[1] = o1[1];
+              reinterpret_cast<uint4*>(dst + c + hh)[0] = o2[0];
+              reinterpret_cast<uint4*>(dst + c + hh)[1] = o2[1];
+            }
+          }
+        }
+      } else if (EPI == EPI_KV_CTX) {
+        // context row row0 + m (m = a_row0 + row_in_tile): its request b (row_off[b] <= row < row_off[b + 1]) and
+        // position pos_start[b] + row - row_off[b]; rows past the request's count are skipped, positions outside
+        // [0, t_cap) are recorded and skipped.  tcgen05.ld is warp-wide: every lane loads, valid rows store.
+        const int m = w.a_row0 + row_in_tile;
+        const int grow = p.row0 + m;
+        bool ok = m < p.M;
+        int b = 0, pos = 0;
+        if (ok) {
+          int lo = 0, hi = p.batch;
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.row_off[mid] <= grow) lo = mid; else hi = mid;
+          }
+          b = lo;
+          if (grow >= p.row_off[p.batch] || (p.row_cnt && grow - p.row_off[b] >= p.row_cnt[b])) {
+            ok = false;
+          } else {
+            pos = (p.pos_start ? p.pos_start[b] : 0) + grow - p.row_off[b];
+            if (pos < 0 || pos >= p.t_cap) {
+              record_check(kCheckBadPosition);
+              ok = false;
+            }
+          }
+        }
+        const int layer = w.b_row0 / p.kv_cols;
+        const int hh = p.hd / 2;
+        const float2* rope_row = p.rope + (size_t)(ok ? pos : 0) * hh;
+        const bf16* gain = p.k_norm_l[layer];
+#pragma unroll 1
+        for (int h0 = 0; h0 < BN; h0 += p.hd) {
+          const int hk = (w.b_row0 - layer * p.kv_cols + h0) / p.hd;   // [K heads | V heads] of the layer
+          const int is_v = hk >= p.nkv, g = is_v ? hk - p.nkv : hk;
+          bf16* dst = p.store + (((((size_t)layer * p.batch + b) * 2 + is_v) * p.nkv + g) * (size_t)p.t_cap + pos) * p.hd;
+          if (is_v) {
+#pragma unroll 1
+            for (int c = 0; c < p.hd; c += 16) {
+              float v[16];
+              tc::tmem_ld16(t_acc + h0 + c, v);
+              uint4 pk[2];
+              bf16* pe = reinterpret_cast<bf16*>(pk);
+#pragma unroll
+              for (int e = 0; e < 16; e++) pe[e] = __float2bfloat16_rn(v[e]);
+              if (ok) {
+                reinterpret_cast<uint4*>(dst + c)[0] = pk[0];
+                reinterpret_cast<uint4*>(dst + c)[1] = pk[1];
+              }
+            }
+            continue;
+          }
+          float ss = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < p.hd; c += 16) {
+            float v[16];
+            tc::tmem_ld16(t_acc + h0 + c, v);
+#pragma unroll
+            for (int e = 0; e < 16; e++) ss += v[e] * v[e];
+          }
+          const float inv = rsqrtf(ss / (float)p.hd + p.eps);
+#pragma unroll 1
+          for (int c = 0; c < hh; c += 16) {
+            float a[16], bb[16];
+            tc::tmem_ld16(t_acc + h0 + c, a);
+            tc::tmem_ld16(t_acc + h0 + c + hh, bb);
+            uint4 g1u[2], g2u[2], o1[2], o2[2];
+            g1u[0] = reinterpret_cast<const uint4*>(gain + c)[0];
+            g1u[1] = reinterpret_cast<const uint4*>(gain + c)[1];
+            g2u[0] = reinterpret_cast<const uint4*>(gain + c + hh)[0];
+            g2u[1] = reinterpret_cast<const uint4*>(gain + c + hh)[1];
+            const bf16* g1 = reinterpret_cast<const bf16*>(g1u);
+            const bf16* g2 = reinterpret_cast<const bf16*>(g2u);
+            bf16* e1 = reinterpret_cast<bf16*>(o1);
+            bf16* e2 = reinterpret_cast<bf16*>(o2);
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+              const float2 cs = rope_row[c + e];
+              const float x1 = a[e] * inv * __bfloat162float(g1[e]), x2 = bb[e] * inv * __bfloat162float(g2[e]);
+              e1[e] = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
+              e2[e] = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
+            }
+            if (ok) {
               reinterpret_cast<uint4*>(dst + c)[0] = o1[0];
               reinterpret_cast<uint4*>(dst + c)[1] = o1[1];
               reinterpret_cast<uint4*>(dst + c + hh)[0] = o2[0];
@@ -645,6 +749,8 @@ cudaError_t tc_init_attributes() {
   if (e == cudaSuccess) e = set_attr<256, 4, false, EPI_QKV_TOK>();
   if (e == cudaSuccess) e = set_attr<128, 6, false, EPI_RESID_TOK>();
   if (e == cudaSuccess) e = set_attr<256, 4, false, EPI_RESID_TOK>();
+  if (e == cudaSuccess) e = set_attr<256, 4, false, EPI_KV_CTX>();
+  if (e == cudaSuccess) e = set_attr<128, 6, false, EPI_KV_CTX>();
   return e;
 }
 
@@ -701,6 +807,61 @@ cudaError_t launch_tc_tok(const TokGemm& g, const TcPlan& pl, cudaStream_t st) {
   }
   if (pl.bn == 128) return launch_kernel<128, 6, false, EPI_RESID_TOK>(p, pl.grid, st);
   return launch_kernel<256, 4, false, EPI_RESID_TOK>(p, pl.grid, st);
+}
+
+// Width of the weight tile of the context K/V GEMM: whole heads per tile and whole tiles per layer; 0 if none fits.
+static int kvctx_bn(const fpd_model_desc& d) {
+  const int kv_cols = 2 * d.n_kv_heads * d.head_dim;
+  for (int bn : {256, 128})
+    if (kv_cols % bn == 0 && bn % d.head_dim == 0) return bn;
+  return 0;
+}
+
+bool kvctx_supported(const fpd_model_desc& d) {
+  return kvctx_bn(d) > 0 && (d.head_dim == 128 || d.head_dim == 64) && d.d_model % BK == 0 &&
+         d.n_layers <= FPD_MAX_LAYERS;
+}
+
+cudaError_t launch_tc_kvctx(const KvCtxGemm& g, int num_sms, cudaStream_t st) {
+  if (g.R <= 0) return cudaSuccess;
+  const fpd_model_desc& d = *g.d;
+  const int bn = kvctx_bn(d);
+  if (!kvctx_supported(d)) return cudaErrorInvalidValue;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  const int h = d.head_dim, kv_cols = 2 * d.n_kv_heads * h, nqkv = (d.n_q_heads + 2 * d.n_kv_heads) * h;
+  cudaError_t e = make_tmap(&p.tm_x[0], g.ctx, g.R, d.d_model, d.d_model, BM);
+  for (int l = 0; l < d.n_layers && e == cudaSuccess; l++) {
+    e = make_tmap(&p.tm_wl[l], g.wqkv[l], nqkv, d.d_model, d.d_model, bn);
+    p.k_norm_l[l] = g.k_norm[l];
+  }
+  if (e != cudaSuccess) return e;
+  p.n_seg = 1;
+  p.seg_k = d.d_model;
+  p.M = g.R;
+  p.N = d.n_layers * kv_cols;
+  p.K = d.d_model;
+  p.pt = ceil_div(g.R, BM);
+  p.qt = p.N / bn;
+  p.splits = 1;
+  p.k_split = d.d_model;
+  p.kv_cols = kv_cols;
+  p.kv_row_base = d.n_q_heads * h;
+  p.n_layers = d.n_layers;
+  p.store = g.store;
+  p.rope = g.rope;
+  p.row_off = g.row_off;
+  p.row_cnt = g.row_cnt;
+  p.pos_start = g.pos_start;
+  p.batch = g.batch;
+  p.row0 = g.row0;
+  p.t_cap = g.t_cap;
+  p.nkv = d.n_kv_heads;
+  p.hd = h;
+  p.eps = d.rms_eps;
+  const int grid = std::min(p.pt * p.qt, num_sms);
+  if (bn == 256) return launch_kernel<256, 4, false, EPI_KV_CTX>(p, grid, st);
+  return launch_kernel<128, 6, false, EPI_KV_CTX>(p, grid, st);
 }
 
 TcPlan tc_plan_gemm(int M, int N, int K, int num_sms) {

@@ -8,8 +8,9 @@ hidden states differ by about one bf16 ulp in most elements after five layers; a
 restatement of the drafter (tests/fp32_restatement.py, pinned in tests/test_fp32_evidence.py) already flips ids
 at oracle margins above 1e-2 (up to 0.015) with per-logit errors up to about 5e-2.  So through the chain an id
 may differ only where the oracle margin is below MARGIN_CHAIN = 5e-2 (a fixed number: that restatement's
-largest logit error), at no more than 5 % of the positions of a request (at least one), and every GPU id must be
-the argmax of the GPU's own logits (assert_tokens_chain).  Acceptance lengths and committed tokens are bit-exact
+largest logit error); the ids that differ at margins in [1e-2, 5e-2) -- the ones the stated rule does not already
+exempt -- may be at most 5 % of the positions of a request (at least one); and every GPU id must be the argmax of
+the GPU's own logits (assert_tokens_chain).  Acceptance lengths and committed tokens are bit-exact
 given the ids.
 """
 import numpy as np
@@ -87,7 +88,8 @@ def assert_logits(gpu: np.ndarray, ref: np.ndarray, what: str = "logits", few: i
 def assert_tokens_chain(gpu_tok, ref_tok, margin, gpu_logits, ref_logits, what="tokens"):
     """End-to-end id check: every GPU id is the lowest-id argmax of the GPU's own legal logits; an id that
     differs from the oracle's is accepted only where the oracle margin is below MARGIN_CHAIN, and at most
-    max(1, CHAIN_FLIP_FRAC * positions) ids may differ.  Prints and returns (flips, largest exempted margin)."""
+    max(1, CHAIN_FLIP_FRAC * positions) of the differing ids may have margins at or above MARGIN_EXEMPT (below it
+    the stated rule exempts them outright).  Prints and returns (flips, largest exempted margin)."""
     gpu_tok = np.asarray(gpu_tok).reshape(-1)
     ref_tok = np.asarray(ref_tok).reshape(-1)
     margin = np.asarray(margin).reshape(-1)
@@ -98,11 +100,13 @@ def assert_tokens_chain(gpu_tok, ref_tok, margin, gpu_logits, ref_logits, what="
         assert gpu_tok[r] == ids[int(np.argmax(gl))], f"{what}: row {r} id is not the argmax of the GPU logits"
     flips = np.nonzero(gpu_tok != ref_tok)[0]
     worst = float(margin[flips].max()) if len(flips) else 0.0
-    print(f"{what}: {len(flips)} of {len(gpu_tok)} ids differ from the oracle, largest exempted margin {worst:.4f}")
+    print(f"{what}: {len(flips)} of {len(gpu_tok)} ids differ from the oracle at margins "
+          f"{[round(float(margin[r]), 4) for r in flips]}")
     bad = [(int(r), float(margin[r])) for r in flips if not margin[r] < MARGIN_CHAIN]
     assert not bad, f"{what}: ids differ at oracle margins >= {MARGIN_CHAIN}: {bad[:5]}"
+    band = [r for r in flips if not margin[r] < MARGIN_EXEMPT]
     cap = max(1, int(CHAIN_FLIP_FRAC * len(gpu_tok)))
-    assert len(flips) <= cap, f"{what}: {len(flips)} ids differ, more than {cap}"
+    assert len(band) <= cap, f"{what}: {len(band)} ids differ at margins >= {MARGIN_EXEMPT}, more than {cap}"
     return len(flips), worst
 
 
