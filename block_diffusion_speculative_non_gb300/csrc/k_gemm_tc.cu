@@ -754,13 +754,15 @@ cudaError_t tc_init_attributes() {
   return e;
 }
 
-// Token-tile plan for the fused epilogues (no split-K: the epilogue needs complete sums).  Wide weight tiles
-// (256) when they still give every SM a tile, else 128.
+// Token-tile plan for the fused epilogues (no split-K: the epilogue needs complete sums).  A CTA streams its
+// operands at a rate set by the SM, not by the tile shape, so a tile costs about its operand bytes, (128 + bn) K,
+// and the GEMM about waves x that: the weight-tile width (256 or 128) with the smaller product wins, 256 on ties.
 TcPlan tc_plan_tok(int M, int N, int K, int num_sms) {
   TcPlan pl{};
   pl.swap = false;
   pl.pt = ceil_div(M, BM);
-  pl.bn = pl.pt * ceil_div(N, 256) >= num_sms ? 256 : 128;
+  const long w256 = ceil_div(pl.pt * ceil_div(N, 256), num_sms), w128 = ceil_div(pl.pt * ceil_div(N, 128), num_sms);
+  pl.bn = w256 * (BM + 256) <= w128 * (BM + 128) ? 256 : 128;
   pl.qt = ceil_div(N, pl.bn);
   pl.splits = 1;
   pl.k_split = K;

@@ -427,10 +427,10 @@ def test_full_prepare_then_draft_few_token(pkg, orc, full_weights):
 
 # ---- 4B shape: corner points of the throughput sweep --------------------------------------------------------------
 
-@pytest.mark.parametrize("B,T,L", [(1, 512, 16), (64, 16384, 16), (64, 16384, 385)])
+@pytest.mark.parametrize("B,T,L", [(1, 512, 16), (64, 16384, 16), (64, 16384, 385), (16, 512, 16)])
 def test_sweep_corner(pkg, orc, full_weights, B, T, L):
     """Corners of the sweep (batch {1, 64} x context {512, 16384} x block {16 text, 385 special-token}) at full
-    size.  Requests 0 and B - 1 take their context K/V from the seeded host generator and are checked end to end
+    size, and B 16 x L 16 (256 block rows: the token-tile GEMMs split K three ways, reduced by the last CTA).  Requests 0 and B - 1 take their context K/V from the seeded host generator and are checked end to end
     by the oracle (requests are independent); the others are drawn on the device and only run."""
     base = "text_4b_b1" if L == 16 else "primitive_special_b1"
     wl = synth.make_workload(base, batch=B, t_ctx=T, seed=5100 + B + L)
