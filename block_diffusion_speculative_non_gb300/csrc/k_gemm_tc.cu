@@ -886,7 +886,23 @@ TcPlan tc_plan_gemm(int M, int N, int K, int num_sms) {
   const int tiles = pl.pt * pl.qt;
   const int slots = num_sms * ctas_per_sm;
   int splits = 1;
-  if (tiles < slots) splits = std::max(1, std::min(slots / tiles, nkb / 4));
+  if (2 * tiles <= slots || pl.swap) {
+    if (tiles < slots) splits = std::max(1, std::min(slots / tiles, nkb / 4));
+  } else {
+    // More than half a wave of tiles: split K when the last wave is short.  A split of s costs ceil(tiles s / slots) waves
+    // of K/s each, plus its extra fp32 partial (M N 4 bytes written and read back) spread over the SMs, counted in
+    // the same unit (K elements a tile streams: (128 + bn) 2 bytes each).
+    const double part_k = (double)M * N * 8 / slots / ((BM + pl.bn) * 2);
+    double best = 0.0;
+    for (int s = 1; s <= 4 && (s == 1 || nkb / s >= 8); s++) {
+      const int kb = ceil_div(nkb, s);
+      const double cost = (double)ceil_div(tiles * s, slots) * kb * BK + (s - 1) * part_k;
+      if (s == 1 || cost < best) {
+        best = cost;
+        splits = s;
+      }
+    }
+  }
   const int kb_per = ceil_div(nkb, splits);
   pl.k_split = kb_per * BK;
   pl.splits = ceil_div(nkb, kb_per);

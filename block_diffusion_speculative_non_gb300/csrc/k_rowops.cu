@@ -25,30 +25,71 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 // ---- RMSNorm of fp32 split-K partial sums -> bf16 (fused context) -------------------------------------------------
-__global__ void rmsnorm_partials_kernel(bf16* __restrict__ out, const float* __restrict__ part, int nsplit,
-                                        size_t split_stride, const bf16* __restrict__ g, int d, float eps) {
+// Thread t holds the float4 groups t, t + 256, ... (VPT of them) of row blockIdx.x: the split-K partials are read
+// once (one round trip per split, every thread's groups of a split in flight together), summed in split order,
+// then normed from registers.
+template <int VPT>
+__global__ void __launch_bounds__(256) rmsnorm_partials_kernel(bf16* __restrict__ out, const float* __restrict__ part,
+                                                               int nsplit, size_t split_stride,
+                                                               const bf16* __restrict__ g, int d, float eps) {
   pdl_trigger();
   pdl_wait();
   __shared__ float red[32];
-  const int r = blockIdx.x;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float v = 0.f;
-    for (int s = 0; s < nsplit; s++) v += part[s * split_stride + (size_t)r * d + i];
-    ss += v * v;
+  const int r = blockIdx.x, n4 = d / 4;
+  const float4* src = reinterpret_cast<const float4*>(part + (size_t)r * d);
+  const size_t s4 = split_stride / 4;
+  float4 v[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int i = threadIdx.x + k * 256;
+    v[k] = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  for (int s = 1; s < nsplit; s++) {
+    float4 t[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; k++) {
+      const int i = threadIdx.x + k * 256;
+      t[k] = i < n4 ? __ldcg(src + s * s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < VPT; k++) {
+      v[k].x += t[k].x;
+      v[k].y += t[k].y;
+      v[k].z += t[k].z;
+      v[k].w += t[k].w;
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
   const float inv = rsqrtf(block_sum(ss, red) / (float)d + eps);
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float v = 0.f;
-    for (int s = 0; s < nsplit; s++) v += part[s * split_stride + (size_t)r * d + i];
-    out[(size_t)r * d + i] = __float2bfloat16_rn(v * inv * __bfloat162float(g[i]));
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int i = threadIdx.x + k * 256;
+    if (i < n4) {
+      const uint2 gu = reinterpret_cast<const uint2*>(g)[i];
+      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gu.x));
+      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gu.y));
+      const __nv_bfloat162 o01 = __floats2bfloat162_rn(v[k].x * inv * g01.x, v[k].y * inv * g01.y);
+      const __nv_bfloat162 o23 = __floats2bfloat162_rn(v[k].z * inv * g23.x, v[k].w * inv * g23.y);
+      uint2 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&o01);
+      o.y = *reinterpret_cast<const uint32_t*>(&o23);
+      reinterpret_cast<uint2*>(out + (size_t)r * d)[i] = o;
+    }
   }
 }
 
 cudaError_t launch_rmsnorm_partials(bf16* out, const float* part, int nsplit, size_t split_stride, const bf16* g,
                                     int rows, int d, float eps, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  return launch_k(rmsnorm_partials_kernel, rows, 256, 0, st, out, part, nsplit, split_stride, g, d, eps);
+  if (d % 4 || split_stride % 4 || d > 16384) return cudaErrorInvalidValue;
+  const int n4 = d / 4;
+  if (n4 <= 256) return launch_k(rmsnorm_partials_kernel<1>, rows, 256, 0, st, out, part, nsplit, split_stride, g, d, eps);
+  if (n4 <= 512) return launch_k(rmsnorm_partials_kernel<2>, rows, 256, 0, st, out, part, nsplit, split_stride, g, d, eps);
+  if (n4 <= 1024) return launch_k(rmsnorm_partials_kernel<4>, rows, 256, 0, st, out, part, nsplit, split_stride, g, d, eps);
+  if (n4 <= 2048) return launch_k(rmsnorm_partials_kernel<8>, rows, 256, 0, st, out, part, nsplit, split_stride, g, d, eps);
+  return launch_k(rmsnorm_partials_kernel<16>, rows, 256, 0, st, out, part, nsplit, split_stride, g, d, eps);
 }
 
 // ---- a4 epilogue: sum split-K partials of [q | k | v], q/k RMSNorm + RoPE at pos = ctx_len[b] + j ------------------
