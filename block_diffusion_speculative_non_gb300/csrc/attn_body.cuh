@@ -290,60 +290,72 @@ __device__ __forceinline__ void attn_tile(const AttnArgs& a, bf16* __restrict__ 
   }
 }
 
-// Combines the splits of one (row, q head); running maxima are in base-2 units.  Thread t handles splits
-// t, t + H, ...: the block takes the maximum of the split maxima, then every split's weight 2^(m_s - M) and the
-// denominator sum_s l_s w_s (fixed reduction tree: bit-reproducible); finally every thread sums its column over
-// the splits in split order.
-template <int H, class Sync>
-__device__ __forceinline__ void attn_merge_row(bf16* __restrict__ out, const float* __restrict__ o_part,
-                                               const float2* __restrict__ ml, int nsplit, int rows, int nq, int r,
-                                               int i, int e, float* w_s, float* red, Sync sync) {
-  // threads e >= H (when more threads than head dims run it) only take part in the barriers
-  constexpr int NW = H / 32;
-  const int lane = e & 31, wp = e >> 5;
-  const bool act = e < H;
-  const int ns = nsplit < 128 ? nsplit : 128;   // attn_plan never makes more than 128 splits
+// Combines the splits of one (row, q head) in one warp; running maxima are in base-2 units.  Lane s of a 32-split
+// chunk holds split s's (m, l): the warp takes the maximum M of the split maxima (empty splits, l = 0, carry no
+// weight and their partial is never read), the denominator sum_s l_s 2^(m_s - M) in a fixed xor tree per chunk,
+// chunks in order; then every lane sums its H/32 columns over the splits in split order (8 splits' loads in flight
+// at a time) and divides by the denominator.  Bit-reproducible.
+template <int H>
+__device__ __forceinline__ void attn_merge_warp(bf16* __restrict__ out, const float* __restrict__ o_part,
+                                                const float2* __restrict__ ml, int nsplit, int rows, int nq, int r,
+                                                int i, int lane) {
+  constexpr int DPL = H / 32;
+  const size_t mstride = (size_t)rows * nq;
+  const float2* mp = ml + (size_t)r * nq + i;
   float mx = -INFINITY;
-  for (int s = e; act && s < ns; s += H) {
-    const float2 v = __ldcg(ml + ((size_t)s * rows + r) * nq + i);
-    const float m = v.y > 0.f ? v.x : -INFINITY;   // empty splits carry no weight
-    w_s[s] = m;
-    mx = fmaxf(mx, m);
+  for (int s0 = 0; s0 < nsplit; s0 += 32) {
+    const int s = s0 + lane;
+    const float2 v = s < nsplit ? __ldcg(mp + (size_t)s * mstride) : make_float2(-INFINITY, 0.f);
+    mx = fmaxf(mx, warp_max(v.y > 0.f ? v.x : -INFINITY));
   }
-  mx = warp_max(mx);
-  if (act && lane == 0) red[wp] = mx;
-  sync();
-  mx = red[0];
-#pragma unroll
-  for (int k = 1; k < NW; k++) mx = fmaxf(mx, red[k]);
-  sync();
   float den = 0.f;
-  for (int s = e; act && s < ns; s += H) {
-    const float2 v = __ldcg(ml + ((size_t)s * rows + r) * nq + i);
-    const float wgt = w_s[s] == -INFINITY ? 0.f : exp2f(w_s[s] - mx);
-    den += v.y * wgt;
-    w_s[s] = wgt;
+  for (int s0 = 0; s0 < nsplit; s0 += 32) {
+    const int s = s0 + lane;
+    const float2 v = s < nsplit ? __ldcg(mp + (size_t)s * mstride) : make_float2(-INFINITY, 0.f);
+    den += warp_sum(v.y > 0.f ? v.y * exp2f(v.x - mx) : 0.f);
   }
-  den = warp_sum(den);
-  if (act && lane == 0) red[wp] = den;
-  sync();
-  den = red[0];
+  const float* op = o_part + ((size_t)r * nq + i) * H + lane * DPL;
+  const size_t ostride = mstride * H;
+  float num[DPL];
 #pragma unroll
-  for (int k = 1; k < NW; k++) den += red[k];
-  sync();   // red and w_s may be reused by the caller's next unit once every thread has read them
-  if (!act) return;
-  const float* op = o_part + ((size_t)r * nq + i) * H + e;
-  const size_t sstride = (size_t)rows * nq * H;
-  float num = 0.f;
-  for (int s0 = 0; s0 < ns; s0 += 8) {
-    float t[8];
+  for (int e = 0; e < DPL; e++) num[e] = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += 8) {
+    float t[8][DPL], wgt[8];
 #pragma unroll
-    for (int u = 0; u < 8; u++) t[u] = (s0 + u < ns && w_s[s0 + u] != 0.f) ? __ldcg(op + (size_t)(s0 + u) * sstride) : 0.f;
+    for (int u = 0; u < 8; u++) {
+      const int s = s0 + u;
+      wgt[u] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; e++) t[u][e] = 0.f;
+      if (s < nsplit) {
+        const float2 v = __ldcg(mp + (size_t)s * mstride);
+        wgt[u] = v.y > 0.f ? exp2f(v.x - mx) : 0.f;
+      }
+      if (wgt[u] != 0.f) {
+        if constexpr (DPL == 4) {
+          const float4 f = __ldcg(reinterpret_cast<const float4*>(op + (size_t)s * ostride));
+          t[u][0] = f.x;
+          t[u][1] = f.y;
+          t[u][2] = f.z;
+          t[u][3] = f.w;
+        } else {
+          const float2 f = __ldcg(reinterpret_cast<const float2*>(op + (size_t)s * ostride));
+          t[u][0] = f.x;
+          t[u][1] = f.y;
+        }
+      }
+    }
 #pragma unroll
     for (int u = 0; u < 8; u++)
-      if (s0 + u < ns) num += t[u] * w_s[s0 + u];
+      if (wgt[u] != 0.f)
+#pragma unroll
+        for (int e = 0; e < DPL; e++) num[e] += t[u][e] * wgt[u];
   }
-  out[((size_t)r * nq + i) * H + e] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+  bf16* dst = out + ((size_t)r * nq + i) * H + lane * DPL;
+#pragma unroll
+  for (int e = 0; e < DPL; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) =
+        __floats2bfloat162_rn(den > 0.f ? num[e] / den : 0.f, den > 0.f ? num[e + 1] / den : 0.f);
 }
 
 }  // namespace attn

@@ -20,14 +20,15 @@ __global__ void __launch_bounds__(NWARP * 32) attn_mma_kernel(AttnArgs a, bf16* 
   attn_tile<H>(a, out, blockIdx.x, blockIdx.y, blockIdx.z, threadIdx.x, smem_raw, CtaSync{});
 }
 
+// one warp per (row, q head), 8 per block
 template <int H>
-__global__ void attn_merge_kernel(bf16* __restrict__ out, const float* __restrict__ o_part,
-                                  const float2* __restrict__ ml, int nsplit, int rows, int nq) {
+__global__ void __launch_bounds__(256) attn_merge_kernel(bf16* __restrict__ out, const float* __restrict__ o_part,
+                                                         const float2* __restrict__ ml, int nsplit, int rows, int nq) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float w_s[128];
-  __shared__ float red[4];
-  attn_merge_row<H>(out, o_part, ml, nsplit, rows, nq, blockIdx.x, blockIdx.y, threadIdx.x, w_s, red, CtaSync{});
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (wid >= rows * nq) return;
+  attn_merge_warp<H>(out, o_part, ml, nsplit, rows, nq, wid / nq, wid % nq, threadIdx.x & 31);
 }
 }  // namespace
 
@@ -39,7 +40,7 @@ void attn_plan(int batch, int L, int nq, int nkv, int t_cap, int num_sms, int* s
   const int max_splits = ceil_div(max_keys, KT);
   int s = ceil_div(num_sms, base);   // about one CTA per SM
   s = s < 1 ? 1 : (s > max_splits ? max_splits : s);
-  s = s > 128 ? 128 : s;   // the merge kernel stages at most 128 splits' weights
+  s = s > 128 ? 128 : s;
   const int ch = ceil_div(ceil_div(max_keys, s), KT) * KT;
   *chunk = ch;
   *splits = ceil_div(max_keys, ch);
@@ -54,11 +55,12 @@ cudaError_t attn_init_attributes() {
 }
 
 cudaError_t launch_attn_merge(const AttnArgs& a, bf16* out, cudaStream_t st) {
+  const int blocks = ceil_div(a.rows * a.nq, 8);
   if (a.head_dim == 128)
-    return launch_k(attn_merge_kernel<128>, dim3(a.rows, a.nq), 128, 0, st, out, (const float*)a.o_part,
-                    (const float2*)a.ml, a.splits, a.rows, a.nq);
-  return launch_k(attn_merge_kernel<64>, dim3(a.rows, a.nq), 64, 0, st, out, (const float*)a.o_part,
-                  (const float2*)a.ml, a.splits, a.rows, a.nq);
+    return launch_k(attn_merge_kernel<128>, blocks, 256, 0, st, out, (const float*)a.o_part, (const float2*)a.ml,
+                    a.splits, a.rows, a.nq);
+  return launch_k(attn_merge_kernel<64>, blocks, 256, 0, st, out, (const float*)a.o_part, (const float2*)a.ml,
+                  a.splits, a.rows, a.nq);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, bf16* out, cudaStream_t st) {

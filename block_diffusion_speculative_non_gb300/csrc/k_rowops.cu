@@ -264,36 +264,64 @@ cudaError_t launch_residual_norm(bf16* x, bf16* xn, const float* part, int nspli
 }
 
 // ---- RMSNorm of rows whose sums of squares were left by the residual GEMM epilogue: one warp per row -------------
-__global__ void norm_rows_kernel(bf16* __restrict__ xn, const bf16* __restrict__ x, const float* __restrict__ ss_part,
-                                 int n_part, const bf16* __restrict__ g, int M, int d, float eps) {
+// One 128-thread block per row: warp 0 loads the row's column-tile partials of sum(x^2) (lane t holds part t) and
+// adds them in part order, while every thread already holds its chunks of x and g; one round trip for the loads.
+template <int CPT>
+__global__ void __launch_bounds__(128) norm_rows_kernel(bf16* __restrict__ xn, const bf16* __restrict__ x,
+                                                        const float* __restrict__ ss_part, int n_part,
+                                                        const bf16* __restrict__ g, int M, int d, float eps) {
   pdl_trigger();
   pdl_wait();
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (r >= M) return;
-  float ss = 0.f;
-  for (int t = 0; t < n_part; t++) ss += __ldcg(ss_part + (size_t)t * M + r);   // fixed order: reproducible
-  const float inv = rsqrtf(ss / (float)d + eps);
+  __shared__ float s_inv;
+  const int r = blockIdx.x, tid = threadIdx.x, n8 = d / 8;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)r * d);
   const uint4* gs = reinterpret_cast<const uint4*>(g);
-  uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)r * d);
-  for (int c = lane; c < d / 8; c += 32) {
-    uint4 u = src[c];
-    const uint4 gu = gs[c];
-    __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&u);
-    const __nv_bfloat162* ge = reinterpret_cast<const __nv_bfloat162*>(&gu);
+  uint4 u[CPT], gu[CPT];
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float2 xf = __bfloat1622float2(e[i]), gf = __bfloat1622float2(ge[i]);
-      e[i] = __floats2bfloat162_rn(xf.x * inv * gf.x, xf.y * inv * gf.y);
+  for (int k = 0; k < CPT; k++) {
+    const int c = tid + k * 128;
+    if (c < n8) {
+      u[k] = src[c];
+      gu[k] = gs[c];
     }
-    dst[c] = u;
+  }
+  if (tid < 32) {
+    float ss = 0.f;   // sequential in part order: the same fp32 sum as a one-thread loop
+    for (int t0 = 0; t0 < n_part; t0 += 32) {
+      const float v = t0 + tid < n_part ? __ldcg(ss_part + (size_t)(t0 + tid) * M + r) : 0.f;
+      for (int j = 0; j < 32 && t0 + j < n_part; j++) ss += __shfl_sync(0xffffffffu, v, j);
+    }
+    if (tid == 0) s_inv = rsqrtf(ss / (float)d + eps);
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)r * d);
+#pragma unroll
+  for (int k = 0; k < CPT; k++) {
+    const int c = tid + k * 128;
+    if (c < n8) {
+      __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&u[k]);
+      const __nv_bfloat162* ge = reinterpret_cast<const __nv_bfloat162*>(&gu[k]);
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const float2 xf = __bfloat1622float2(e[i]), gf = __bfloat1622float2(ge[i]);
+        e[i] = __floats2bfloat162_rn(xf.x * inv * gf.x, xf.y * inv * gf.y);
+      }
+      dst[c] = u[k];
+    }
   }
 }
 
 cudaError_t launch_norm_rows(bf16* xn, const bf16* x, const float* ss_part, int n_part, const bf16* g, int M, int d,
                              float eps, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  return launch_k(norm_rows_kernel, ceil_div(M, 8), 256, 0, st, xn, x, ss_part, n_part, g, M, d, eps);
+  if (d % 8 || d > 16384) return cudaErrorInvalidValue;
+  const int n8 = d / 8;
+  if (n8 <= 128) return launch_k(norm_rows_kernel<1>, M, 128, 0, st, xn, x, ss_part, n_part, g, M, d, eps);
+  if (n8 <= 256) return launch_k(norm_rows_kernel<2>, M, 128, 0, st, xn, x, ss_part, n_part, g, M, d, eps);
+  if (n8 <= 512) return launch_k(norm_rows_kernel<4>, M, 128, 0, st, xn, x, ss_part, n_part, g, M, d, eps);
+  if (n8 <= 1024) return launch_k(norm_rows_kernel<8>, M, 128, 0, st, xn, x, ss_part, n_part, g, M, d, eps);
+  return launch_k(norm_rows_kernel<16>, M, 128, 0, st, xn, x, ss_part, n_part, g, M, d, eps);
 }
 
 // ---- embedding gather fused with the first RMSNorm ----------------------------------------------------------------
