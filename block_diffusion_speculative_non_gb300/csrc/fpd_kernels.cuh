@@ -71,7 +71,7 @@ struct TokGemm {
 };
 TcPlan tc_plan_tok(int M, int N, int K, int num_sms);
 cudaError_t launch_tc_tok(const TokGemm& g, const TcPlan& pl, cudaStream_t st);
-// xn[m][k] = bf16(x[m][k] * rsqrt(sum_t ss_part[t][m] / d + eps) * g[k]), one warp per row
+// xn[m][k] = bf16(x[m][k] * rsqrt(sum_t ss_part[t][m] / d + eps) * g[k]), one block per row
 cudaError_t launch_norm_rows(bf16* xn, const bf16* x, const float* ss_part, int n_part, const bf16* g, int M, int d,
                              float eps, cudaStream_t st);
 cudaError_t tc_init_attributes();     // once per process, before any stream capture

@@ -263,7 +263,7 @@ cudaError_t launch_residual_norm(bf16* x, bf16* xn, const float* part, int nspli
   return launch_k(residual_norm_kernel<16>, rows, 1024, 0, st, x, xn, part, nsplit, split_stride, g, d, eps);
 }
 
-// ---- RMSNorm of rows whose sums of squares were left by the residual GEMM epilogue: one warp per row -------------
+// ---- RMSNorm of rows whose sums of squares were left by the residual GEMM epilogue: one block per row -----------
 // One 128-thread block per row: warp 0 loads the row's column-tile partials of sum(x^2) (lane t holds part t) and
 // adds them in part order, while every thread already holds its chunks of x and g; one round trip for the loads.
 template <int CPT>
