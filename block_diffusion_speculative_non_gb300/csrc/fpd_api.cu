@@ -131,8 +131,14 @@ DraftWs carve_draft_stream(const Model& m, Carver& c, int B, int L, int t_cap, b
   return w;
 }
 
-// More than 64 block positions: token tiles on the 128-row MMA operand, epilogues fused into the GEMMs.
-constexpr int kTokMinRows = 65;
+// From 257 block positions: token tiles on the 128-row MMA operand, epilogues fused into the GEMMs.  A projection
+// does about M flops per weight byte, so below the bf16 tensor rate / HBM rate (about 260) a block is HBM-bound,
+// and the weight tiles on the 128-row operand with K split over all SMs (reduced by the row kernels) stream the
+// weights faster than token tiles, which leave SMs idle on the narrow projections (256 rows, 16 x 16 positions:
+// 1.29 -> 1.15 ms per step at context 512, 2.72 -> 2.08 ms at 8192).
+constexpr int kTokMinRows = 257;
+// Context preparation takes the one-GEMM K/V path (EPI_KV_CTX) from 65 rows.
+constexpr int kKvCtxMinRows = 65;
 
 DraftWs carve_draft_tok(const Model& m, Carver& c, int B, int L, int t_cap) {
   const auto& d = m.d;
@@ -568,7 +574,7 @@ static fpd_status prepare_rows_impl(fpd_model* m, int batch, int total_rows, con
     FPD_CUDA(launch_rmsnorm_partials(w.ctx, w.part, pf.splits, g.c_split_stride, (const bf16*)m->w.hidden_norm, R,
                                      d.d_model, d.rms_eps, st),
              "fusion RMSNorm");
-    if (R >= kTokMinRows && kvctx_supported(d)) {
+    if (R >= kKvCtxMinRows && kvctx_supported(d)) {
       // every layer's K/V in one token-tile GEMM whose epilogue norms, rotates and stores (no fp32 round trip)
       const bf16* kn[FPD_MAX_LAYERS];
       for (int l = 0; l < d.n_layers; l++) kn[l] = (const bf16*)m->w.k_norm[l];

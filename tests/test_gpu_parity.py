@@ -170,6 +170,21 @@ def test_tiny_few_token_batch_ragged(pkg, orc):
     dr.close()
 
 
+def test_tiny_medium_batch_weight_tiles(pkg, orc):
+    """Eight requests of 20 positions (160 block rows: below the token-tile threshold, the weight-tile GEMMs with K
+    split over the SMs and the row kernels' reductions), ragged contexts including an empty one."""
+    s = synth.TINY
+    w = synth.make_weights(s, 4343)
+    ctx_len = np.array([40, 0, 97, 1, 128, 64, 5, 77], np.int32)
+    off = np.concatenate([[0], np.cumsum(ctx_len)]).astype(np.int32)
+    B, L = 8, 20
+    dr, om, kv, _ = _prepare_both(pkg, orc, s, w, off, int(ctx_len.max()), L, B, 4344)
+    kv_g = _stagewise(dr, kv, ctx_len, B)
+    _draft_and_compare(pkg, orc, dr, om, kv_g, int(ctx_len.max()), ctx_len, (np.arange(B, dtype=np.int32) * 411 + 3) % s.vocab,
+                       s.vocab - 1, L, B)
+    dr.close()
+
+
 @pytest.mark.parametrize("L,ctx", [(2, 0), (2, 1), (16, 0), (33, 96)])
 def test_tiny_degenerate_blocks(pkg, orc, L, ctx):
     """Shortest block (one proposal), no context at all, and a context filling the store."""
