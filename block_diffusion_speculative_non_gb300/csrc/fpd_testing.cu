@@ -235,3 +235,45 @@ fpd_status fpd_test_attention(int impl, int batch, int L, int nq, int nkv, int h
 }
 
 }  // extern "C"
+
+// ---- launch plans, host only ---------------------------------------------------------------------------------
+extern "C" int fpd_test_plan(int kind, int M, int N, int K, int num_sms, int32_t* out) {
+  if (!out || M < 1 || N < 1 || K < 64 || K % 64 || num_sms < 1) return FPD_ERR_SHAPE;
+  fpd::TcPlan pl{};
+  if (kind == 0) {
+    pl = fpd::tc_plan_gemm(M, N, K, num_sms);
+  } else if (kind == 1) {
+    pl = fpd::tc_plan_tok(M, N, K, num_sms);
+  } else if (kind == 2) {
+    pl = fpd::tc_plan_swiglu(M, N, K, num_sms);
+  } else if (kind == 3) {
+    const fpd::StreamPlan sp = fpd::stream_plan(N, K, num_sms, true, false);
+    pl.swap = true;
+    pl.bn = 16;
+    pl.pt = sp.tiles;
+    pl.qt = 1;
+    pl.splits = sp.splits;
+    pl.k_split = sp.k_split;
+    pl.grid = sp.grid;
+  } else {
+    return FPD_ERR_INVALID_ARG;
+  }
+  out[0] = pl.swap ? 1 : 0;
+  out[1] = pl.bn;
+  out[2] = pl.pt;
+  out[3] = pl.qt;
+  out[4] = pl.splits;
+  out[5] = pl.k_split;
+  out[6] = pl.grid;
+  return FPD_OK;
+}
+
+extern "C" int fpd_test_attn_plan(int impl, int batch, int L, int nq, int nkv, int t_cap, int num_sms, int32_t* splits,
+                                  int32_t* chunk) {
+  if (!splits || !chunk || batch < 1 || L < 1 || nkv < 1 || nq % nkv || t_cap < 1 || num_sms < 1) return FPD_ERR_SHAPE;
+  int s = 1, c = 0;
+  attn_test_plan(impl, batch, L, nq, nkv, t_cap, num_sms, &s, &c);
+  *splits = s;
+  *chunk = c;
+  return FPD_OK;
+}

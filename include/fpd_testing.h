@@ -66,6 +66,17 @@ fpd_status fpd_test_stream_gemm(int fp8, int M, int N, int K, const void* X, con
                                 const void* Wexp, void* y, void* workspace, size_t workspace_bytes, void* stream);
 size_t fpd_test_stream_gemm_workspace_bytes(int N, int K, int fp8);
 
+/* Host only (no GPU, no CUDA call): the launch plan the library picks for a GEMM of M activation rows, N output
+ * features and K reduction length on num_sms SMs.  kind 0: fp32-partial GEMM of the context fusion and the 17-256-row
+ * blocks; 1: token-tile GEMM with a fused epilogue; 2: gate/up + SwiGLU (N = F features); 3: weight-streaming GEMM of
+ * the few-token path (N = output tiles of 128 rows).  out[7] = {weights on the 128-row operand, width of the other
+ * operand's tile, tiles along the 128-row operand, tiles along the other, K splits, K per split, grid}.
+ * Returns FPD_OK, or FPD_ERR_SHAPE / FPD_ERR_INVALID_ARG for arguments outside those ranges. */
+int fpd_test_plan(int kind, int M, int N, int K, int num_sms, int32_t* out);
+/* Host only: the key splits and keys per split of the attention (impl 0: mma.sync tiles, 1: tensor-memory kernel). */
+int fpd_test_attn_plan(int impl, int batch, int L, int nq, int nkv, int t_cap, int num_sms, int32_t* splits,
+                       int32_t* chunk);
+
 #ifdef __cplusplus
 }
 #endif
