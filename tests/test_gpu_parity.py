@@ -395,7 +395,7 @@ def test_full_fixed_width_batch_sampled_requests(pkg, orc, full_weights):
 def test_full_prepare_then_draft_ragged_append(pkg, orc, full_weights):
     """Context preparation chained into the block pass at the 4B shape: four requests with ragged contexts (one
     empty before its append, one receiving nothing in the second), written in two appends, then one 16-position
-    text block per request (64 block rows: the token-tile path).  Each stage is checked against the oracle given
+    text block per request (64 block rows: the weight-tile path).  Each stage is checked against the oracle given
     the same input: the store against the oracle's preparation from the same features, the block pass (every
     request) against the oracle run on the GPU's store, then the greedy verification."""
     s = synth.FULL
