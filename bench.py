@@ -186,8 +186,9 @@ def oracle_sample(wl, w, kv_np, target):
 
 
 class StepRunner:
-    """One workload on one drafter: device inputs, the step as three CUDA graphs (draft | LM head + argmax |
-    verify), and CUDA-event timing of each part on the launching stream."""
+    """One workload on one drafter: device inputs, the step as one CUDA graph (draft, LM head + argmax, verify:
+    the calls' kernels keep their programmatic-dependent-launch overlap across call boundaries) for the timed
+    steps, and the same step as three graphs with CUDA events between them for the per-call breakdown."""
 
     def __init__(self, pkg, dr, wl, dev, prepare=True, kv_seed=None):
         import torch
@@ -269,11 +270,21 @@ class StepRunner:
             with torch.cuda.graph(g, stream=cap):
                 fn(torch.cuda.current_stream(self.dev))
             self.graphs.append(g)
+        self.g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_step, stream=cap):
+            st = torch.cuda.current_stream(self.dev)
+            self.do_draft(st)
+            self.do_argmax(st)
+            self.do_verify(st)
         for _ in range(max(3, warmup)):
             self.step()
+            self.step_parts()
         torch.cuda.synchronize()
 
-    def step(self, ev=None):
+    def step(self):
+        self.g_step.replay()
+
+    def step_parts(self, ev=None):
         g_draft, g_argmax, g_verify = self.graphs
         if ev is not None:
             ev[0].record(self.stream)
@@ -286,18 +297,22 @@ class StepRunner:
         g_verify.replay()
 
     def time_steps(self, steps, barrier=lambda: None):
-        """Device time of `steps` back-to-back steps, plus the mean draft and LM-head call times."""
+        """Device time of `steps` back-to-back steps (the one-graph step), then, after that timed region, the mean
+        draft and LM-head call times from as many three-graph steps with events between the calls."""
         import torch
-        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
         t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
         t0e.record(self.stream)
-        for i in range(steps):
-            self.step(ev[i])
+        for _ in range(steps):
+            self.step()
         t1e.record(self.stream)
         torch.cuda.synchronize()
         barrier()
+        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+        for i in range(steps):
+            self.step_parts(ev[i])
+        torch.cuda.synchronize()
         draft_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
         lm_ms = float(np.mean([b.elapsed_time(c) for _, b, c in ev]))
         return t0e.elapsed_time(t1e), draft_ms, lm_ms
