@@ -76,21 +76,23 @@ struct Smem {
   bf16 v[2][KT * H];
 };
 
-// One 64-key tile of the online softmax for one warp's 16 query rows (rows lane/4 and lane/4 + 8 of its m16
-// fragment): S = Q K^T on mma.sync from the swizzled K tile at ks, keys at or past k_end masked, running maximum
-// (m0, m1) and sum (l0, l1) in base 2, O += (P_hi + P_lo) V from the V tile at vs.  k0: the tile's first key.
-template <int H>
+// One tile of NK keys (64, or 16 for a short last tile: a quarter of the products) of the online softmax for one
+// warp's 16 query rows (rows lane/4 and lane/4 + 8 of its m16 fragment): S = Q K^T on mma.sync from the swizzled K
+// tile at ks, keys at or past k_end masked, running maximum (m0, m1) and sum (l0, l1) in base 2, O += (P_hi + P_lo)
+// V from the V tile at vs.  k0: the tile's first key.
+template <int H, int NK = KT>
 __device__ __forceinline__ void attn_tile_math(uint32_t ks, uint32_t vs, const uint32_t (&qf)[H / 16][4],
                                                float (&o)[H / 8][4], float& m0, float& m1, float& l0, float& l1,
                                                int k0, int k_end, int lane, float sl2) {
   constexpr int NKS = H / 16;   // k-steps over the head dimension
   constexpr int NOT = H / 8;    // 8-wide n-tiles of O
-  // ---- S = Q K^T: 16 rows x 64 keys per warp ----
-  float s[KT / 8][4];
+  // ---- S = Q K^T: 16 rows x NK keys per warp ----
+  static_assert(NK % 16 == 0 && NK <= KT, "tile keys");
+  float s[NK / 8][4];
 #pragma unroll
-  for (int n = 0; n < KT / 8; n++) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+  for (int n = 0; n < NK / 8; n++) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
 #pragma unroll
-  for (int kp = 0; kp < KT / 16; kp++) {
+  for (int kp = 0; kp < NK / 16; kp++) {
 #pragma unroll
     for (int kk = 0; kk < NKS; kk++) {
       // 8x8 matrices: (keys +0..7, dims lo), (keys +0..7, dims hi), (keys +8..15, dims lo), (keys +8..15, dims hi)
@@ -103,9 +105,9 @@ __device__ __forceinline__ void attn_tile_math(uint32_t ks, uint32_t vs, const u
     }
   }
   // ---- online softmax (base 2) ----
-  if (k0 + KT > k_end) {   // a partial tile (warp-uniform): keys past the end get 2^-inf = 0
+  if (k0 + NK > k_end) {   // a partial tile (warp-uniform): keys past the end get 2^-inf = 0
 #pragma unroll
-    for (int n = 0; n < KT / 8; n++) {
+    for (int n = 0; n < NK / 8; n++) {
       const int key = k0 + n * 8 + (lane & 3) * 2;
       if (key >= k_end) s[n][0] = s[n][2] = -INFINITY;
       if (key + 1 >= k_end) s[n][1] = s[n][3] = -INFINITY;
@@ -113,7 +115,7 @@ __device__ __forceinline__ void attn_tile_math(uint32_t ks, uint32_t vs, const u
   }
   float mx0 = -INFINITY, mx1 = -INFINITY;   // raw maxima, scaled once below (sl2 > 0)
 #pragma unroll
-  for (int n = 0; n < KT / 8; n++) {
+  for (int n = 0; n < NK / 8; n++) {
     mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
     mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
   }
@@ -131,7 +133,7 @@ __device__ __forceinline__ void attn_tile_math(uint32_t ks, uint32_t vs, const u
   float ps0 = 0.f, ps1 = 0.f;
   const float n0 = -mn0, n1 = -mn1;
 #pragma unroll
-  for (int n = 0; n < KT / 8; n++) {
+  for (int n = 0; n < NK / 8; n++) {
     s[n][0] = ex2_approx(fmaf(s[n][0], sl2, n0));
     s[n][1] = ex2_approx(fmaf(s[n][1], sl2, n0));
     s[n][2] = ex2_approx(fmaf(s[n][2], sl2, n1));
@@ -150,7 +152,7 @@ __device__ __forceinline__ void attn_tile_math(uint32_t ks, uint32_t vs, const u
   }
   // ---- O += (P_hi + P_lo) V ----
 #pragma unroll
-  for (int kk = 0; kk < KT / 16; kk++) {
+  for (int kk = 0; kk < NK / 16; kk++) {
     uint32_t h0, h1, h2, h3, l0_, l1_, l2_, l3_;
     split_bf16x2(s[2 * kk][0], s[2 * kk][1], h0, l0_);
     split_bf16x2(s[2 * kk][2], s[2 * kk][3], h1, l1_);

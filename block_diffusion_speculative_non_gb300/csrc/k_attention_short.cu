@@ -7,7 +7,8 @@
 // splits are merged through distributed shared memory inside the same kernel: no fp32 partials go to global memory
 // and no merge kernel follows.
 //
-//   - CTA `rank` of the cluster takes 64-key tiles [rank * tpc, (rank + 1) * tpc) of [0, T + L), tpc = ceil(tiles / C).
+//   - CTA `rank` of the cluster takes 64-key tiles [rank * tiles / C, (rank + 1) * tiles / C) of [0, T + L); a last
+//     tile of at most 16 keys runs the 16-key tile math.
 //   - Tiles that hold only context keys are fetched (cp.async, 3-tile ring) before griddepcontrol.wait: the store
 //     and ctx_len are written before the call, and the call's first kernel lets its successors launch only after
 //     its own wait, so they are complete.  Q and the block K/V come from the call's QKV kernel: after the wait.
@@ -96,8 +97,10 @@ __global__ void __launch_bounds__(NWARP * 32) attn_short_kernel(const __grid_con
   int T = a.ctx_len[b];
   T = clamp_ctx(T, a.t_cap);
   const int n_keys = T + a.L;
-  const int nt = ceil_div(n_keys, KT), tpc = ceil_div(nt, C);
-  const int t0 = min(nt, rank * tpc), t1 = min(nt, t0 + tpc), nts = t1 - t0;
+  // tiles spread as evenly as the count allows, the extra ones to the last ranks: with 2048 + 16 keys every CTA
+  // walks 2 full tiles and the last one also the 16-key tail, which takes the short tile math
+  const int nt = ceil_div(n_keys, KT);
+  const int t0 = rank * nt / C, t1 = (rank + 1) * nt / C, nts = t1 - t0;
   const int k_begin = t0 * KT, k_end = min(n_keys, t1 * KT);
   const float sl2 = rsqrtf((float)H) * 1.4426950408889634f;   // 1/sqrt(h) * log2(e): softmax in base 2
 
@@ -168,8 +171,12 @@ __global__ void __launch_bounds__(NWARP * 32) attn_short_kernel(const __grid_con
       for (int kk = 0; kk < NKS; kk++)
         ldsm_x4(swz<H>(q_s, r, kk * 2 + (lane >> 4)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
     }
-    attn_tile_math<H>(smem_addr(sm.k[slot]), smem_addr(sm.v[slot]), qf, o, m0, m1, l0, l1, k_begin + it * KT, k_end,
-                      lane, sl2);
+    if (k_end - (k_begin + it * KT) <= 16)   // a tail of at most 16 keys: a quarter of the products
+      attn_tile_math<H, 16>(smem_addr(sm.k[slot]), smem_addr(sm.v[slot]), qf, o, m0, m1, l0, l1, k_begin + it * KT,
+                            k_end, lane, sl2);
+    else
+      attn_tile_math<H>(smem_addr(sm.k[slot]), smem_addr(sm.v[slot]), qf, o, m0, m1, l0, l1, k_begin + it * KT, k_end,
+                        lane, sl2);
     __syncthreads();   // slot is refilled next
     if (it + SNS < nts) {
       load_kv(slot, k_begin + (it + SNS) * KT);
