@@ -574,8 +574,9 @@ static fpd_status prepare_rows_impl(fpd_model* m, int batch, int total_rows, con
     FPD_CUDA(launch_rmsnorm_partials(w.ctx, w.part, pf.splits, g.c_split_stride, (const bf16*)m->w.hidden_norm, R,
                                      d.d_model, d.rms_eps, st),
              "fusion RMSNorm");
-    if (R >= kKvCtxMinRows && kvctx_supported(d)) {
-      // every layer's K/V in one token-tile GEMM whose epilogue norms, rotates and stores (no fp32 round trip)
+    if (R >= kKvCtxMinRows && !row_cnt && kvctx_supported(d)) {
+      // every layer's K/V in one token-tile GEMM whose epilogue norms, rotates and stores (no fp32 round trip);
+      // appends with device-side row counts (the accepted rows of a speculative step) keep the per-layer path
       const bf16* kn[FPD_MAX_LAYERS];
       for (int l = 0; l < d.n_layers; l++) kn[l] = (const bf16*)m->w.k_norm[l];
       KvCtxGemm kg{};
