@@ -92,13 +92,14 @@ def algorithmic_work(wl, fp8=False):
 
 def profiled_traffic(workload):
     """DRAM bytes per step (dram__bytes_read.sum + dram__bytes_write.sum over every kernel of one step) from the
-    committed ncu summary, or None when no summary covers this workload."""
+    committed ncu summary, or None when no summary covers this workload or a kernel of the step has changed since
+    its counters were taken (the row's `current` cell is not `yes`)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic_per_step.md")
     try:
         for ln in open(path):
             cells = [c.strip() for c in ln.strip().strip("|").split("|")]
-            if len(cells) >= 3 and cells[0] == workload:
-                return int(float(cells[2]))
+            if len(cells) >= 5 and cells[0] == workload:
+                return int(float(cells[2])) if cells[4] == "yes" else None
     except (OSError, ValueError):
         pass
     return None
